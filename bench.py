@@ -1,0 +1,403 @@
+"""Benchmark of the MoE expert layer (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = moe_layer_fwd + moe_layer_bwd over one batch of synthetic tokens
+(router projection, softmax/top-k, counts/offsets/slots, rowwise dispatch,
+grouped SwiGLU GEMMs, combine, and the whole backward), inputs resident in HBM.
+The default workload is the fine-grained layer: T=8192 tokens, d_model=2048,
+32 experts, top-4, d_ff=1024, bf16, seeded random routing.
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs an
+independent replica on its own tokens (the layer has no exchange step), so
+scaling is weak and `value` is the total tokens/s of all ranks; the step time
+is the maximum over ranks.
+
+`--impl reference` times the CPU oracle (float64 numpy, the correctness
+reference of this repository) on a bounded sample of the same workload on the
+host cores; it is a deliberately slow baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "moe_layer_tokens_per_s_fwd_bwd"
+UNIT = "tokens/s"
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Maximum of a per-rank float over all ranks (identity on one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ flops / bytes
+def gemm_flops(cfg) -> dict:
+    """Useful flops of the expert GEMMs per step (no tile padding counted)."""
+    R = cfg.T * cfg.k
+    return {
+        "fwd1": 4.0 * R * cfg.d * cfg.f, "fwd2": 2.0 * R * cfg.d * cfg.f,
+        "dgrad2": 2.0 * R * cfg.d * cfg.f, "wgrad2": 2.0 * R * cfg.d * cfg.f,
+        "dgrad1": 4.0 * R * cfg.d * cfg.f, "wgrad1": 4.0 * R * cfg.d * cfg.f,
+        "router": 2.0 * cfg.T * cfg.d * cfg.E,
+    }
+
+
+# ------------------------------------------------------------------ clocks sampling
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9 and p[1].replace(".", "").isdigit():
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                          if r[3].replace(".", "").isdigit())}
+
+
+# ------------------------------------------------------------------ the oracle arm
+def oracle_sample(cfg, seed: int, budget_s: float = 12.0) -> dict:
+    """Time the CPU oracle's forward+backward on a bounded token sample."""
+    import numpy as np
+
+    from oracle import moe_oracle as O
+    from synth import make_inputs
+
+    inp = make_inputs(cfg, seed=seed)
+    n_tok = 1024
+    sl = slice(0, n_tok)
+    x, dO = inp["x"][sl], inp["d_out"][sl]
+    bias = inp["bias"][sl] if inp["bias"] is not None else None
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        fwd = O.layer_forward(x, inp["w_router"], bias, inp["w_gate"], inp["w_up"], inp["w_down"],
+                              cfg.k)
+        O.layer_backward(fwd, dO, x, inp["w_router"], inp["w_gate"], inp["w_up"], inp["w_down"])
+        done += n_tok
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    cores = int(threads) if threads else (os.cpu_count() or 1)
+    return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_tok} of {cfg.T} tokens of the '{cfg.name}' workload with all {cfg.E} "
+                      f"experts' full weights, forward+backward repeated {done // n_tok}x "
+                      f"({el:.1f} s, float64 numpy/OpenBLAS)",
+            "seconds": el}
+
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    per = []
+    for _ in range(args.warmup):
+        oracle_sample(cfg, 0, budget_s=1.0)
+    for _ in range(args.steps):
+        per.append(oracle_sample(cfg, 0, budget_s=max(2.0, 20.0 / max(args.steps, 1))))
+    v = sum(p["value"] for p in per) / len(per)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(cfg),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": per[0]["cores"], "kind": "oracle",
+                         "sample": per[0]["sample"]},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(cfg):
+    return {"workload": cfg.name, "T": cfg.T, "d_model": cfg.d, "n_experts": cfg.E, "top_k": cfg.k,
+            "d_ff": cfg.f, "precision": cfg.prec, "routing": cfg.routing, "seed": 0,
+            "l2": "inputs larger than L2: expert weights alone are 3*E*d*f*2 bytes per step"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, cfg):
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_softmax_gb300 as m
+    from synth import make_inputs
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    m.init(local)
+    inp = make_inputs(cfg, seed=rank)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, wr, wg, wu, wd, dO = (bf(inp[n]) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out"))
+    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+    s = m.shape(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
+    buf = m.allocate(s)
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.forward(buf, x, wr, bias, wg, wu, wd, out)
+        m.backward(buf, dO, x, wr, wg, wu, wd)
+
+    m.clear_error(buf.ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if m.read_error(buf.ws) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region: K whole steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    ms_max = max_over_ranks(ms, world)
+    value = world * cfg.T / (ms_max / 1000.0)
+
+    # ---- per-stage times (same kernels, called stage by stage, events on the stream)
+    stages = stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=max(3, args.steps))
+    fl = gemm_flops(cfg)
+    gemm_ms = sum(stages[k] for k in ("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"))
+    gemm_fl = sum(fl[k] for k in ("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"))
+    peaks = load_peaks()
+    dom = max(("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"), key=lambda k: stages[k])
+    achieved = fl[dom] / (stages[dom] / 1000.0) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({dom})", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peaks['source']} sustained bf16 (kernel timed inside the step)",
+                "algorithmic": f"{fl[dom] / 1e9:.1f} GFLOP per launch (useful flops, no tile padding)"}
+
+    # ---- end to end through the public API with host buffers
+    e2e = end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, args.steps, world)
+
+    if m.read_error(buf.ws) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    cpu = oracle_sample(cfg, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    launches_per_step = 16 if wr is not None else 14
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(cfg),
+        "gemm": {"tflops": gemm_fl / (gemm_ms / 1000.0) / 1e12, "ms": gemm_ms,
+                 "pct_of_peak": 100.0 * gemm_fl / (gemm_ms / 1000.0) / 1e12 / peak,
+                 "peak_tflops": peak},
+        "stage_ms": {k: round(v, 5) for k, v in stages.items()},
+        "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=5):
+    """Average ms of each stage call, events recorded on the launching stream."""
+    import torch
+    sv, g = buf.saved, buf.grads
+    calls = [
+        ("route", lambda: m.route(s, x, wr, bias, sv["logits"], sv["topk_idx"], sv["gates"],
+                                  sv["counts"], sv["offsets"], sv["tile_offsets"],
+                                  sv["slot_of_route"], sv["route_of_slot"], buf.ws)),
+        ("dispatch", lambda: m.dispatch(s, x, sv["slot_of_route"], sv["counts"], sv["tile_offsets"],
+                                        sv["xd"])),
+        ("fwd1", lambda: m.grouped_gemm(s, m.GEMM_FWD1_SWIGLU, buf.ws, tile_offsets=sv["tile_offsets"],
+                                        a0=sv["xd"], w0=wg, w1=wu, out0=sv["h"], out1=sv["u"],
+                                        out2=sv["a"])),
+        ("fwd2", lambda: m.grouped_gemm(s, m.GEMM_FWD2, buf.ws, tile_offsets=sv["tile_offsets"],
+                                        a0=sv["a"], w0=wd, out0=sv["y"])),
+        ("combine", lambda: m.combine(s, sv["y"], sv["gates"], sv["slot_of_route"], out)),
+        ("combine_bwd", lambda: m.combine_bwd(s, dO, sv["y"], sv["gates"], sv["topk_idx"],
+                                              sv["slot_of_route"], sv["counts"], sv["tile_offsets"],
+                                              g["dy"], g["d_gates"], g["dlogits"])),
+        ("dgrad2", lambda: m.grouped_gemm(s, m.GEMM_DGRAD2_SWIGLU, buf.ws,
+                                          tile_offsets=sv["tile_offsets"], a0=g["dy"], w0=wd,
+                                          aux0=sv["h"], aux1=sv["u"], out0=g["dh"], out1=g["du"])),
+        ("wgrad2", lambda: m.grouped_gemm(s, m.GEMM_WGRAD2, buf.ws, tile_offsets=sv["tile_offsets"],
+                                          a0=g["dy"], a1=sv["a"], out0=g["dw_down"])),
+        ("dgrad1", lambda: m.grouped_gemm(s, m.GEMM_DGRAD1, buf.ws, tile_offsets=sv["tile_offsets"],
+                                          a0=g["dh"], a1=g["du"], w0=wg, w1=wu, out0=g["dxd"])),
+        ("wgrad1", lambda: m.grouped_gemm(s, m.GEMM_WGRAD1, buf.ws, tile_offsets=sv["tile_offsets"],
+                                          a0=g["dh"], a1=g["du"], aux0=sv["xd"], out0=g["dw_gate"],
+                                          out1=g["dw_up"])),
+        ("dispatch_bwd", lambda: m.dispatch_bwd(s, g["dxd"], sv["slot_of_route"], sv["topk_idx"],
+                                                g["dlogits"], wr, g["dx"])),
+        ("router_bwd", lambda: m.router_bwd(s, x, g["dlogits"], sv["route_of_slot"], sv["counts"],
+                                            sv["tile_offsets"], g["dw_router"], buf.ws)),
+    ]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+    for r in range(reps):
+        ev[r][0].record(stream)
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            ev[r][i + 1].record(stream)
+    torch.cuda.synchronize()
+    res = {}
+    for i, (name, _) in enumerate(calls):
+        res[name] = sum(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps)) / reps
+    return res
+
+
+def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world):
+    """Same step through the public API, with the step's inputs (x, dOut) copied
+    from pinned host memory and its results (out, dx) copied back, every step."""
+    import numpy as np
+    import torch
+    hx = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hd = torch.from_numpy(np.ascontiguousarray(inp["d_out"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    ho = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    x = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    dO = torch.empty_like(x)
+    out = torch.empty_like(x)
+
+    def step():
+        x.copy_(hx, non_blocking=True)
+        dO.copy_(hd, non_blocking=True)
+        m.forward(buf, x, wr, bias, wg, wu, wd, out)
+        m.backward(buf, dO, x, wr, wg, wu, wd)
+        ho.copy_(out, non_blocking=True)
+        hdx.copy_(buf.grads["dx"], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    nbytes = 2 * cfg.T * cfg.d * 2
+    return {"value": world * cfg.T / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="fine_grained")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    from synth import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

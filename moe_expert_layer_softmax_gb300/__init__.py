@@ -1,0 +1,301 @@
+"""Python binding of libmoe_gb300.so, the sm_103a MoE expert layer library.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (used for device memory and streams);
+the C entry points have the same names without the `moe_` prefix.  There is no
+fallback: if the library is missing or cannot be loaded, every call raises.
+
+Shapes follow include/moe.h: x [T, d] bf16, W_r [E, d] bf16, W_gate/W_up
+[E, f, d] bf16, W_down [E, d, f] bf16; dispatched row buffers have
+`rows_max(shape)` rows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+BF16, MXFP8 = 0, 1
+TILE_M = 128
+
+GEMM_FWD1_SWIGLU = 0
+GEMM_FWD2 = 1
+GEMM_DGRAD2_SWIGLU = 2
+GEMM_DGRAD1 = 3
+GEMM_WGRAD2 = 4
+GEMM_WGRAD1 = 5
+
+DEVERR_NONFINITE_LOGIT = 0x1
+DEVERR_TIMEOUT = 0x2
+DEVERR_BOUNDS = 0x4
+
+_ERRORS = {-1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_ALIGN",
+           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_NOT_INIT"}
+
+# every symbol the C header declares
+EXPORTS = (
+    "moe_init", "moe_rows_max", "moe_workspace_size", "moe_clear_error", "moe_read_error",
+    "moe_route", "moe_dispatch", "moe_quantize_mxfp8", "moe_grouped_gemm", "moe_combine",
+    "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
+)
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code} ({_ERRORS.get(code, 'unknown')})")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("prec", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("tile_offsets", "a0", "a1", "w0", "w1", "aux0", "aux1",
+                                   "out0", "out1", "out2")]
+
+
+class Saved(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("logits", "topk_idx", "gates", "counts", "offsets",
+                                   "tile_offsets", "slot_of_route", "route_of_slot", "xd", "h",
+                                   "u", "a", "y")]
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("x", "w_router", "logit_bias", "w_gate", "w_up", "w_down",
+                                   "out")]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("d_out", "x", "w_router", "w_gate", "w_up", "w_down", "dx",
+                                   "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates",
+                                   "dlogits", "dy", "dh", "du", "dxd")]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "(the MoE layer has no CPU or eager fallback)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    i32 = ctypes.c_int32
+    sig = {
+        "moe_init": [ctypes.c_int],
+        "moe_rows_max": [P(Shape), P(ctypes.c_int64)],
+        "moe_workspace_size": [P(Shape), P(ctypes.c_size_t)],
+        "moe_clear_error": [_vp, _vp],
+        "moe_read_error": [_vp, P(i32), _vp],
+        "moe_route": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
+        "moe_dispatch": [P(Shape)] + [_vp] * 6 + [_vp],
+        "moe_quantize_mxfp8": [i32, i32, i32, i32, _vp, _vp, _vp, _vp],
+        "moe_grouped_gemm": [P(Shape), i32, P(GemmArgs), _vp, _vp],
+        "moe_combine": [P(Shape)] + [_vp] * 4 + [_vp],
+        "moe_combine_bwd": [P(Shape)] + [_vp] * 10 + [_vp],
+        "moe_dispatch_bwd": [P(Shape)] + [_vp] * 6 + [_vp],
+        "moe_router_bwd": [P(Shape)] + [_vp] * 7 + [_vp],
+        "moe_layer_fwd": [P(Shape), P(FwdArgs), P(Saved), _vp, _vp],
+        "moe_layer_bwd": [P(Shape), P(BwdArgs), P(Saved), _vp, _vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise MoEError(fn, rc)
+
+
+def shape(T, d, E, k, f, prec=BF16) -> Shape:
+    return Shape(int(T), int(d), int(E), int(k), int(f), int(prec))
+
+
+# ------------------------------------------------------------------ set-up
+_inited = set()
+
+
+def init(device: int | None = None):
+    import torch
+    dev = torch.cuda.current_device() if device is None else int(device)
+    if dev in _inited:
+        return
+    with torch.cuda.device(dev):
+        _check("moe_init", load().moe_init(dev))
+    _inited.add(dev)
+
+
+def rows_max(s: Shape) -> int:
+    v = ctypes.c_int64()
+    _check("moe_rows_max", load().moe_rows_max(ctypes.byref(s), ctypes.byref(v)))
+    return v.value
+
+
+def workspace_size(s: Shape) -> int:
+    v = ctypes.c_size_t()
+    _check("moe_workspace_size", load().moe_workspace_size(ctypes.byref(s), ctypes.byref(v)))
+    return v.value
+
+
+def clear_error(ws, stream=None):
+    _check("moe_clear_error", load().moe_clear_error(_ptr(ws), _stream(stream)))
+
+
+def read_error(ws, stream=None) -> int:
+    v = ctypes.c_int32()
+    _check("moe_read_error", load().moe_read_error(_ptr(ws), ctypes.byref(v), _stream(stream)))
+    return v.value
+
+
+# ------------------------------------------------------------------ stage calls
+def route(s, x, w_router, logit_bias, logits, topk_idx, gates, counts, offsets, tile_offsets,
+          slot_of_route, route_of_slot, ws, stream=None):
+    _check("moe_route", load().moe_route(
+        ctypes.byref(s), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(logits), _ptr(topk_idx),
+        _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(tile_offsets), _ptr(slot_of_route),
+        _ptr(route_of_slot), _ptr(ws), _stream(stream)))
+
+
+def dispatch(s, x, slot_of_route, counts, tile_offsets, xd, xd_scales=None, stream=None):
+    _check("moe_dispatch", load().moe_dispatch(
+        ctypes.byref(s), _ptr(x), _ptr(slot_of_route), _ptr(counts), _ptr(tile_offsets), _ptr(xd),
+        _ptr(xd_scales), _stream(stream)))
+
+
+def quantize_mxfp8(batch, rows, cols, block_axis, src, q, scales, stream=None):
+    _check("moe_quantize_mxfp8", load().moe_quantize_mxfp8(
+        int(batch), int(rows), int(cols), int(block_axis), _ptr(src), _ptr(q), _ptr(scales),
+        _stream(stream)))
+
+
+def grouped_gemm(s, op, ws, stream=None, **kw):
+    a = GemmArgs(**{k: _ptr(v) for k, v in kw.items()})
+    _check("moe_grouped_gemm", load().moe_grouped_gemm(ctypes.byref(s), int(op), ctypes.byref(a),
+                                                       _ptr(ws), _stream(stream)))
+
+
+def combine(s, y, gates, slot_of_route, out, stream=None):
+    _check("moe_combine", load().moe_combine(ctypes.byref(s), _ptr(y), _ptr(gates),
+                                             _ptr(slot_of_route), _ptr(out), _stream(stream)))
+
+
+def combine_bwd(s, d_out, y, gates, topk_idx, slot_of_route, counts, tile_offsets, dy, d_gates,
+                dlogits, stream=None):
+    _check("moe_combine_bwd", load().moe_combine_bwd(
+        ctypes.byref(s), _ptr(d_out), _ptr(y), _ptr(gates), _ptr(topk_idx), _ptr(slot_of_route),
+        _ptr(counts), _ptr(tile_offsets), _ptr(dy), _ptr(d_gates), _ptr(dlogits), _stream(stream)))
+
+
+def dispatch_bwd(s, dxd, slot_of_route, topk_idx, dlogits, w_router, dx, stream=None):
+    _check("moe_dispatch_bwd", load().moe_dispatch_bwd(
+        ctypes.byref(s), _ptr(dxd), _ptr(slot_of_route), _ptr(topk_idx), _ptr(dlogits),
+        _ptr(w_router), _ptr(dx), _stream(stream)))
+
+
+def router_bwd(s, x, dlogits, route_of_slot, counts, tile_offsets, dw_router, ws, stream=None):
+    _check("moe_router_bwd", load().moe_router_bwd(
+        ctypes.byref(s), _ptr(x), _ptr(dlogits), _ptr(route_of_slot), _ptr(counts),
+        _ptr(tile_offsets), _ptr(dw_router), _ptr(ws), _stream(stream)))
+
+
+def layer_fwd(s, fwd: FwdArgs, saved: Saved, ws, stream=None):
+    _check("moe_layer_fwd", load().moe_layer_fwd(ctypes.byref(s), ctypes.byref(fwd),
+                                                 ctypes.byref(saved), _ptr(ws), _stream(stream)))
+
+
+def layer_bwd(s, bwd: BwdArgs, saved: Saved, ws, stream=None):
+    _check("moe_layer_bwd", load().moe_layer_bwd(ctypes.byref(s), ctypes.byref(bwd),
+                                                 ctypes.byref(saved), _ptr(ws), _stream(stream)))
+
+
+# ------------------------------------------------------------------ buffers
+@dataclass
+class LayerBuffers:
+    """Caller-owned device buffers of one layer shape (torch allocates them)."""
+
+    shape: Shape
+    rows_max: int
+    ws: object
+    saved: dict
+    grads: dict
+
+    def saved_struct(self) -> Saved:
+        return Saved(**{k: _ptr(v) for k, v in self.saved.items()})
+
+
+def allocate(s: Shape, device=None, with_grads: bool = True) -> LayerBuffers:
+    """Allocate every buffer moe_layer_fwd / moe_layer_bwd need for shape `s`."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    T, d, E, k, f = s.T, s.d_model, s.n_experts, s.top_k, s.d_ff
+    n = rows_max(s)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    ws = torch.zeros(workspace_size(s), dtype=torch.uint8, device=dev)
+    saved = {
+        "logits": torch.empty(T, E, **f32), "topk_idx": torch.empty(T, k, **i32),
+        "gates": torch.empty(T, k, **f32), "counts": torch.empty(E, **i32),
+        "offsets": torch.empty(E + 1, **i32), "tile_offsets": torch.empty(E + 1, **i32),
+        "slot_of_route": torch.empty(T * k, **i32), "route_of_slot": torch.empty(n, **i32),
+        "xd": torch.empty(n, d, **bf), "h": torch.empty(n, f, **bf), "u": torch.empty(n, f, **bf),
+        "a": torch.empty(n, f, **bf), "y": torch.empty(n, d, **bf),
+    }
+    grads = {}
+    if with_grads:
+        grads = {
+            "dx": torch.empty(T, d, **bf), "dw_router": torch.empty(E, d, **f32),
+            "dw_gate": torch.empty(E, f, d, **f32), "dw_up": torch.empty(E, f, d, **f32),
+            "dw_down": torch.empty(E, d, f, **f32), "d_gates": torch.empty(T, k, **f32),
+            "dlogits": torch.empty(T, E, **f32), "dy": torch.empty(n, d, **bf),
+            "dh": torch.empty(n, f, **bf), "du": torch.empty(n, f, **bf),
+            "dxd": torch.empty(n, d, **bf),
+        }
+    return LayerBuffers(s, n, ws, saved, grads)
+
+
+def forward(buf: LayerBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, out, stream=None):
+    fa = FwdArgs(x=_ptr(x), w_router=_ptr(w_router), logit_bias=_ptr(logit_bias),
+                 w_gate=_ptr(w_gate), w_up=_ptr(w_up), w_down=_ptr(w_down), out=_ptr(out))
+    layer_fwd(buf.shape, fa, buf.saved_struct(), buf.ws, stream)
+
+
+def backward(buf: LayerBuffers, d_out, x, w_router, w_gate, w_up, w_down, stream=None):
+    g = buf.grads
+    ba = BwdArgs(d_out=_ptr(d_out), x=_ptr(x), w_router=_ptr(w_router), w_gate=_ptr(w_gate),
+                 w_up=_ptr(w_up), w_down=_ptr(w_down),
+                 **{k: _ptr(v) for k, v in g.items()})
+    layer_bwd(buf.shape, ba, buf.saved_struct(), buf.ws, stream)

@@ -1,0 +1,460 @@
+// C ABI of the MoE expert layer library: argument validation, workspace
+// layout, the stage calls and the whole-layer orchestration.  Every call only
+// enqueues kernels on the caller's stream; none waits for the GPU except
+// moe_read_error.  Declarations and documentation: include/moe.h.
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const moe_shape_t* s) {
+  if (s == nullptr) return MOE_ERR_INVALID;
+  if (s->T < 1 || s->d_model < 1 || s->n_experts < 1 || s->top_k < 1 || s->d_ff < 1)
+    return MOE_ERR_INVALID;
+  if (s->prec != MOE_BF16 && s->prec != MOE_MXFP8) return MOE_ERR_INVALID;
+  if (s->top_k > s->n_experts) return MOE_ERR_INVALID;
+  if (s->n_experts > 256 || s->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (s->d_model % 128 != 0 || s->d_ff % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)s->T * s->top_k >= (int64_t(1) << 31) - (int64_t)s->n_experts * kTileM)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int64_t rows_max_of(const moe_shape_t* s) {
+  const int64_t R = (int64_t)s->T * s->top_k;
+  const int64_t r = R + (int64_t)s->n_experts * (kTileM - 1);
+  return (r + kTileM - 1) / kTileM * kTileM;
+}
+
+int n_route_blocks(const moe_shape_t* s) {
+  return (s->T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+}
+
+// Workspace: [error word | block histograms | route ranks | router-grad partials]
+struct WsLayout {
+  size_t hist, rank, partial, total;
+};
+WsLayout ws_layout(const moe_shape_t* s) {
+  WsLayout w;
+  size_t off = 256;
+  w.hist = off;
+  off += align256((size_t)n_route_blocks(s) * s->n_experts * 4);
+  w.rank = off;
+  off += align256((size_t)s->T * s->top_k * 4);
+  w.partial = off;
+  off += align256((size_t)(rows_max_of(s) / kTileM) * s->d_model * 4);
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+
+int ready_or_error() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MOE_ERR_NOT_INIT;
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                   \
+  do {                                  \
+    int _rc = (expr);                   \
+    if (_rc != MOE_OK) return _rc;      \
+  } while (0)
+
+#define MOE_CUDA(expr)                              \
+  do {                                              \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+#define MOE_NONNULL_ALIGNED(p)                   \
+  do {                                           \
+    if ((p) == nullptr) return MOE_ERR_INVALID;  \
+    if (!aligned16(p)) return MOE_ERR_ALIGN;     \
+  } while (0)
+
+#define MOE_ALIGNED_OR_NULL(p)                             \
+  do {                                                     \
+    if ((p) != nullptr && !aligned16(p)) return MOE_ERR_ALIGN; \
+  } while (0)
+
+int route_impl(const moe_shape_t* s, const void* x, const void* w_router, const float* bias,
+               float* logits, int32_t* topk_idx, float* gates, int32_t* counts, int32_t* offsets,
+               int32_t* tile_offsets, int32_t* slot_of_route, int32_t* route_of_slot, void* ws,
+               cudaStream_t st) {
+  const WsLayout w = ws_layout(s);
+  int32_t* err = at<int32_t>(ws, 0);
+  int32_t* hist = at<int32_t>(ws, w.hist);
+  int32_t* rank = at<int32_t>(ws, w.rank);
+  if (w_router != nullptr) {
+    GemmLaunch g = {};
+    g.op = OP_ROUTER;
+    g.T = s->T; g.d = s->d_model; g.E = s->n_experts; g.f = s->d_ff;
+    g.rows_max = rows_max_of(s);
+    g.a0 = x; g.w0 = w_router; g.bias = bias; g.out0 = logits; g.err = err;
+    MOE_CUDA(launch_grouped_gemm(g, st));
+  }
+  MOE_CUDA(launch_route_topk(logits, s->T, s->n_experts, s->top_k, topk_idx, gates, rank, hist,
+                             err, st));
+  MOE_CUDA(launch_route_scan(hist, n_route_blocks(s), s->n_experts, counts, offsets, tile_offsets,
+                             st));
+  MOE_CUDA(launch_route_slots(topk_idx, rank, hist, counts, tile_offsets, s->T, s->n_experts,
+                              s->top_k, rows_max_of(s), slot_of_route, route_of_slot, err, st));
+  return MOE_OK;
+}
+
+int gemm_impl(const moe_shape_t* s, int op, const moe_gemm_args_t* a, void* ws, cudaStream_t st) {
+  GemmLaunch g = {};
+  g.op = op;
+  g.T = s->T; g.d = s->d_model; g.E = s->n_experts; g.f = s->d_ff;
+  g.rows_max = rows_max_of(s);
+  g.tile_offsets = a->tile_offsets;
+  g.a0 = a->a0; g.a1 = a->a1; g.w0 = a->w0; g.w1 = a->w1;
+  g.aux0 = a->aux0; g.aux1 = a->aux1;
+  g.out0 = a->out0; g.out1 = a->out1; g.out2 = a->out2;
+  g.err = at<int32_t>(ws, 0);
+  MOE_CUDA(launch_grouped_gemm(g, st));
+  return MOE_OK;
+}
+
+int check_gemm_args(int op, const moe_gemm_args_t* a) {
+  if (a == nullptr) return MOE_ERR_INVALID;
+  MOE_NONNULL_ALIGNED(a->tile_offsets);
+  switch (op) {
+    case MOE_GEMM_FWD1_SWIGLU:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->w0); MOE_NONNULL_ALIGNED(a->w1);
+      MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1); MOE_NONNULL_ALIGNED(a->out2);
+      break;
+    case MOE_GEMM_FWD2:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->w0); MOE_NONNULL_ALIGNED(a->out0);
+      break;
+    case MOE_GEMM_DGRAD2_SWIGLU:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->w0); MOE_NONNULL_ALIGNED(a->aux0);
+      MOE_NONNULL_ALIGNED(a->aux1); MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1);
+      break;
+    case MOE_GEMM_DGRAD1:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->a1); MOE_NONNULL_ALIGNED(a->w0);
+      MOE_NONNULL_ALIGNED(a->w1); MOE_NONNULL_ALIGNED(a->out0);
+      break;
+    case MOE_GEMM_WGRAD2:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->a1); MOE_NONNULL_ALIGNED(a->out0);
+      break;
+    case MOE_GEMM_WGRAD1:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->a1); MOE_NONNULL_ALIGNED(a->aux0);
+      MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1);
+      break;
+    default:
+      return MOE_ERR_INVALID;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+const DeviceInfo* device_info() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  return &g_dev[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_init(int device) {
+  if (device < 0 || device >= kMaxDevices) return MOE_ERR_INVALID;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != device) return MOE_ERR_INVALID;
+  int sms = 0;
+  MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+  MOE_CUDA(gemm_init_attributes());
+  g_dev[device].sm_count = sms;
+  g_dev[device].ready = true;
+  return MOE_OK;
+}
+
+int moe_rows_max(const moe_shape_t* shape, int64_t* rows_max) {
+  MOE_TRY(check_shape(shape));
+  if (rows_max == nullptr) return MOE_ERR_INVALID;
+  *rows_max = rows_max_of(shape);
+  return MOE_OK;
+}
+
+int moe_workspace_size(const moe_shape_t* shape, size_t* ws_bytes) {
+  MOE_TRY(check_shape(shape));
+  if (ws_bytes == nullptr) return MOE_ERR_INVALID;
+  *ws_bytes = ws_layout(shape).total;
+  return MOE_OK;
+}
+
+int moe_clear_error(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID;
+  MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_read_error(const void* ws, int32_t* code, void* stream) {
+  if (ws == nullptr || code == nullptr) return MOE_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaMemcpyAsync(code, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+int moe_route(const moe_shape_t* s, const void* x, const void* w_router, const float* logit_bias,
+              float* logits, int32_t* topk_idx, float* gates, int32_t* counts, int32_t* offsets,
+              int32_t* tile_offsets, int32_t* slot_of_route, int32_t* route_of_slot, void* ws,
+              void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  if (w_router != nullptr) {
+    MOE_NONNULL_ALIGNED(x);
+    MOE_NONNULL_ALIGNED(w_router);
+  }
+  MOE_ALIGNED_OR_NULL(logit_bias);
+  MOE_NONNULL_ALIGNED(logits);
+  MOE_NONNULL_ALIGNED(topk_idx);
+  MOE_NONNULL_ALIGNED(gates);
+  MOE_NONNULL_ALIGNED(counts);
+  MOE_NONNULL_ALIGNED(offsets);
+  MOE_NONNULL_ALIGNED(tile_offsets);
+  MOE_NONNULL_ALIGNED(slot_of_route);
+  MOE_NONNULL_ALIGNED(route_of_slot);
+  MOE_NONNULL_ALIGNED(ws);
+  return route_impl(s, x, w_router, logit_bias, logits, topk_idx, gates, counts, offsets,
+                    tile_offsets, slot_of_route, route_of_slot, ws,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_dispatch(const moe_shape_t* s, const void* x, const int32_t* slot_of_route,
+                 const int32_t* counts, const int32_t* tile_offsets, void* xd, uint8_t* xd_scales,
+                 void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_NONNULL_ALIGNED(x);
+  MOE_NONNULL_ALIGNED(slot_of_route);
+  MOE_NONNULL_ALIGNED(counts);
+  MOE_NONNULL_ALIGNED(tile_offsets);
+  MOE_NONNULL_ALIGNED(xd);
+  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (xd_scales != nullptr) return MOE_ERR_INVALID;
+  MOE_CUDA(launch_dispatch_bf16(x, slot_of_route, counts, tile_offsets, s->T, s->d_model,
+                                s->n_experts, s->top_k, xd, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_quantize_mxfp8(int32_t batch, int32_t rows, int32_t cols, int32_t block_axis,
+                       const void* src, uint8_t* q, uint8_t* scales, void* stream) {
+  (void)batch; (void)rows; (void)cols; (void)block_axis; (void)src; (void)q; (void)scales;
+  (void)stream;
+  return MOE_ERR_UNSUPPORTED;
+}
+
+int moe_grouped_gemm(const moe_shape_t* s, int32_t op, const moe_gemm_args_t* args, void* ws,
+                     void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_TRY(check_gemm_args(op, args));
+  MOE_NONNULL_ALIGNED(ws);
+  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  return gemm_impl(s, op, args, ws, static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_shape_t* s, const void* y, const float* gates,
+                const int32_t* slot_of_route, void* out, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_NONNULL_ALIGNED(y);
+  MOE_NONNULL_ALIGNED(gates);
+  MOE_NONNULL_ALIGNED(slot_of_route);
+  MOE_NONNULL_ALIGNED(out);
+  MOE_CUDA(launch_combine(y, gates, slot_of_route, s->T, s->d_model, s->top_k, out,
+                          static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_combine_bwd(const moe_shape_t* s, const void* d_out, const void* y, const float* gates,
+                    const int32_t* topk_idx, const int32_t* slot_of_route, const int32_t* counts,
+                    const int32_t* tile_offsets, void* dy, float* d_gates, float* dlogits,
+                    void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_NONNULL_ALIGNED(d_out);
+  MOE_NONNULL_ALIGNED(y);
+  MOE_NONNULL_ALIGNED(gates);
+  MOE_NONNULL_ALIGNED(topk_idx);
+  MOE_NONNULL_ALIGNED(slot_of_route);
+  MOE_NONNULL_ALIGNED(counts);
+  MOE_NONNULL_ALIGNED(tile_offsets);
+  MOE_NONNULL_ALIGNED(dy);
+  MOE_NONNULL_ALIGNED(d_gates);
+  MOE_ALIGNED_OR_NULL(dlogits);
+  MOE_CUDA(launch_combine_bwd(d_out, y, gates, topk_idx, slot_of_route, counts, tile_offsets, s->T,
+                              s->d_model, s->n_experts, s->top_k, dy, d_gates, dlogits,
+                              static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_dispatch_bwd(const moe_shape_t* s, const void* dxd, const int32_t* slot_of_route,
+                     const int32_t* topk_idx, const float* dlogits, const void* w_router,
+                     void* dx, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_NONNULL_ALIGNED(dxd);
+  MOE_NONNULL_ALIGNED(slot_of_route);
+  MOE_NONNULL_ALIGNED(topk_idx);
+  MOE_NONNULL_ALIGNED(dx);
+  MOE_ALIGNED_OR_NULL(w_router);
+  if (w_router != nullptr) MOE_NONNULL_ALIGNED(dlogits);
+  MOE_CUDA(launch_dispatch_bwd(dxd, slot_of_route, topk_idx, dlogits, w_router, s->T, s->d_model,
+                               s->n_experts, s->top_k, dx, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_router_bwd(const moe_shape_t* s, const void* x, const float* dlogits,
+                   const int32_t* route_of_slot, const int32_t* counts,
+                   const int32_t* tile_offsets, float* dw_router, void* ws, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_NONNULL_ALIGNED(x);
+  MOE_NONNULL_ALIGNED(dlogits);
+  MOE_NONNULL_ALIGNED(route_of_slot);
+  MOE_NONNULL_ALIGNED(counts);
+  MOE_NONNULL_ALIGNED(tile_offsets);
+  MOE_NONNULL_ALIGNED(dw_router);
+  MOE_NONNULL_ALIGNED(ws);
+  const WsLayout w = ws_layout(s);
+  MOE_CUDA(launch_router_bwd(x, dlogits, route_of_slot, counts, tile_offsets, s->T, s->d_model,
+                             s->n_experts, s->top_k, rows_max_of(s) / kTileM,
+                             at<float>(ws, w.partial), dw_router,
+                             static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved_t* sv, void* ws,
+                  void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  if (a == nullptr || sv == nullptr) return MOE_ERR_INVALID;
+  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  MOE_NONNULL_ALIGNED(a->x);
+  MOE_ALIGNED_OR_NULL(a->w_router);
+  MOE_ALIGNED_OR_NULL(a->logit_bias);
+  MOE_NONNULL_ALIGNED(a->w_gate);
+  MOE_NONNULL_ALIGNED(a->w_up);
+  MOE_NONNULL_ALIGNED(a->w_down);
+  MOE_NONNULL_ALIGNED(a->out);
+  MOE_NONNULL_ALIGNED(sv->logits);
+  MOE_NONNULL_ALIGNED(sv->topk_idx);
+  MOE_NONNULL_ALIGNED(sv->gates);
+  MOE_NONNULL_ALIGNED(sv->counts);
+  MOE_NONNULL_ALIGNED(sv->offsets);
+  MOE_NONNULL_ALIGNED(sv->tile_offsets);
+  MOE_NONNULL_ALIGNED(sv->slot_of_route);
+  MOE_NONNULL_ALIGNED(sv->route_of_slot);
+  MOE_NONNULL_ALIGNED(sv->xd);
+  MOE_NONNULL_ALIGNED(sv->h);
+  MOE_NONNULL_ALIGNED(sv->u);
+  MOE_NONNULL_ALIGNED(sv->a);
+  MOE_NONNULL_ALIGNED(sv->y);
+  MOE_NONNULL_ALIGNED(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(route_impl(s, a->x, a->w_router, a->logit_bias, sv->logits, sv->topk_idx, sv->gates,
+                     sv->counts, sv->offsets, sv->tile_offsets, sv->slot_of_route,
+                     sv->route_of_slot, ws, st));
+  MOE_CUDA(launch_dispatch_bf16(a->x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
+                                s->d_model, s->n_experts, s->top_k, sv->xd, st));
+  moe_gemm_args_t g = {};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = sv->xd; g.w0 = a->w_gate; g.w1 = a->w_up;
+  g.out0 = sv->h; g.out1 = sv->u; g.out2 = sv->a;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
+  g = moe_gemm_args_t{};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = sv->a; g.w0 = a->w_down; g.out0 = sv->y;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_FWD2, &g, ws, st));
+  MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->top_k, a->out,
+                          st));
+  return MOE_OK;
+}
+
+int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved_t* sv, void* ws,
+                  void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  if (a == nullptr || sv == nullptr) return MOE_ERR_INVALID;
+  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  MOE_NONNULL_ALIGNED(a->d_out);
+  MOE_NONNULL_ALIGNED(a->x);
+  MOE_ALIGNED_OR_NULL(a->w_router);
+  MOE_NONNULL_ALIGNED(a->w_gate);
+  MOE_NONNULL_ALIGNED(a->w_up);
+  MOE_NONNULL_ALIGNED(a->w_down);
+  MOE_NONNULL_ALIGNED(a->dx);
+  if (a->w_router != nullptr) MOE_NONNULL_ALIGNED(a->dw_router);
+  MOE_NONNULL_ALIGNED(a->dw_gate);
+  MOE_NONNULL_ALIGNED(a->dw_up);
+  MOE_NONNULL_ALIGNED(a->dw_down);
+  MOE_NONNULL_ALIGNED(a->d_gates);
+  MOE_NONNULL_ALIGNED(a->dlogits);
+  MOE_NONNULL_ALIGNED(a->dy);
+  MOE_NONNULL_ALIGNED(a->dh);
+  MOE_NONNULL_ALIGNED(a->du);
+  MOE_NONNULL_ALIGNED(a->dxd);
+  MOE_NONNULL_ALIGNED(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(launch_combine_bwd(a->d_out, sv->y, sv->gates, sv->topk_idx, sv->slot_of_route,
+                              sv->counts, sv->tile_offsets, s->T, s->d_model, s->n_experts,
+                              s->top_k, a->dy, a->d_gates, a->dlogits, st));
+  moe_gemm_args_t g = {};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = a->dy; g.w0 = a->w_down; g.aux0 = sv->h; g.aux1 = sv->u;
+  g.out0 = a->dh; g.out1 = a->du;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_DGRAD2_SWIGLU, &g, ws, st));
+  g = moe_gemm_args_t{};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = a->dy; g.a1 = sv->a; g.out0 = a->dw_down;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_WGRAD2, &g, ws, st));
+  g = moe_gemm_args_t{};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = a->dh; g.a1 = a->du; g.w0 = a->w_gate; g.w1 = a->w_up; g.out0 = a->dxd;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_DGRAD1, &g, ws, st));
+  g = moe_gemm_args_t{};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = a->dh; g.a1 = a->du; g.aux0 = sv->xd; g.out0 = a->dw_gate; g.out1 = a->dw_up;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_WGRAD1, &g, ws, st));
+  MOE_CUDA(launch_dispatch_bwd(a->dxd, sv->slot_of_route, sv->topk_idx, a->dlogits, a->w_router,
+                               s->T, s->d_model, s->n_experts, s->top_k, a->dx, st));
+  if (a->w_router != nullptr) {
+    const WsLayout w = ws_layout(s);
+    MOE_CUDA(launch_router_bwd(a->x, a->dlogits, sv->route_of_slot, sv->counts, sv->tile_offsets,
+                               s->T, s->d_model, s->n_experts, s->top_k,
+                               rows_max_of(s) / kTileM, at<float>(ws, w.partial), a->dw_router,
+                               st));
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,550 @@
+// Device-scheduled grouped GEMM on tcgen05 tensor cores (sm_103a).
+//
+// "Supercharging Olmo-core for Efficient and Scalable MoE Training", Abstract:
+// the expert GEMMs are grouped GEMMs scheduled on the device from routing
+// metadata that never leaves the GPU; the blog "Olmo-core 3: an open training
+// stack for trillion-parameter MoE" (section "Olmo-core 3's answer") adds that
+// they run the uneven per-expert shapes without padding to a common capacity.
+// Here each expert's rows are padded only to the 128-row tile, and the tile
+// schedule is read from the device-resident tile_offsets.
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0     TMA producer: 128-byte-swizzled A/B tiles into a 4-stage ring
+//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
+//              (128 x N x 16 bf16 MMAs, fp32 accumulators in tensor memory,
+//              two 256-column accumulators so the epilogue of one tile
+//              overlaps the main loop of the next)
+//   warps 2-5  epilogue: tcgen05.ld -> fused SwiGLU / SwiGLU-backward / bias /
+//              fp32 -> global stores
+// Every wait is bounded (error word + abort flag); an aborted CTA waits for
+// its own copies in flight and frees its tensor memory before returning.
+//
+// Schedules:
+//   DENSE   (router)       tiles = ceil(T/128) x n_tiles, K = d
+//   MGROUP  (fwd / dgrad)  tiles = tile_offsets[E] x n_tiles; a tile's expert is
+//                          found by binary search in tile_offsets
+//   KGROUP  (wgrad)        tiles = E x (M/128) x n_tiles, the K loop runs over
+//                          the expert's (padded, zero-filled) rows
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+enum Mode { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
+enum Epi { EPI_BF16 = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_F32 = 3, EPI_ROUTER = 4 };
+
+constexpr int kStages = 4;
+constexpr int kBK = 64;                       // bf16 elements of K per stage (128 bytes)
+constexpr int kABytes = kTileM * kBK * 2;     // 16 KB
+constexpr int kBBytesMax = 256 * kBK * 2;     // 32 KB
+constexpr int kStageBytes = kABytes + kBBytesMax;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kMaxE = 256;
+constexpr uint32_t kTmemCols = 512;           // two 256-column fp32 accumulators
+
+struct __align__(8) Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort;
+  int32_t tile_off[kMaxE + 1];
+};
+
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (int)sizeof(Ctl);
+
+struct Params {
+  int mode;
+  int epi;
+  int a_mn, b_mn;        // operand major-ness (1 = M/N-major, 0 = K-major)
+  int b_dual;            // B tile = 128 rows of map B0 + 128 rows of map B1 (K-major)
+  int E;
+  const int32_t* tile_offsets;
+  int m_tiles;           // DENSE: M tiles; KGROUP: M/128 per expert
+  int m_valid;           // DENSE: valid rows (T)
+  int n_tiles;
+  int BN;                // MMA N (256 when b_dual)
+  int n_valid;           // ROUTER: valid columns (E)
+  int k_steps;           // DENSE/MGROUP: K / 64
+  int k_split;           // DENSE/MGROUP: steps >= k_split read maps A1/B1
+  int m_split;           // KGROUP: M tiles >= m_split read A1 and write out1
+  int b_group_rows;      // expert stride in the rows of B's 2-D view
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* aux0;
+  const void* aux1;
+  const float* bias;
+  int64_t ldo;           // leading dimension (elements) of outputs and aux
+  int64_t out_group_stride;  // KGROUP: elements between experts' outputs
+  int32_t* err;
+};
+
+struct TileInfo {
+  int e, m_tile, n_tile, k0row, ks;
+};
+
+MOE_DEV int find_group(const int32_t* off, int E, int m_tile) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= m_tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+MOE_DEV int total_tiles(const Params& p, const int32_t* off) {
+  if (p.mode == MODE_DENSE) return p.m_tiles * p.n_tiles;
+  if (p.mode == MODE_MGROUP) return off[p.E] * p.n_tiles;
+  return p.E * p.m_tiles * p.n_tiles;
+}
+
+MOE_DEV TileInfo decode_tile(const Params& p, const int32_t* off, int t) {
+  TileInfo ti;
+  if (p.mode == MODE_KGROUP) {
+    const int per = p.m_tiles * p.n_tiles;
+    ti.e = t / per;
+    const int r = t - ti.e * per;
+    ti.m_tile = r / p.n_tiles;
+    ti.n_tile = r - ti.m_tile * p.n_tiles;
+    ti.k0row = off[ti.e] * kTileM;
+    ti.ks = (off[ti.e + 1] - off[ti.e]) * (kTileM / kBK);
+  } else {
+    ti.m_tile = t / p.n_tiles;
+    ti.n_tile = t - ti.m_tile * p.n_tiles;
+    ti.e = (p.mode == MODE_MGROUP) ? find_group(off, p.E, ti.m_tile) : 0;
+    ti.k0row = 0;
+    ti.ks = p.k_steps;
+  }
+  return ti;
+}
+
+MOE_DEV float silu_f(float h) { return h / (1.0f + __expf(-h)); }
+
+// ------------------------------------------------------------------ roles
+MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap* tA0,
+                      const CUtensorMap* tA1, const CUtensorMap* tB0, const CUtensorMap* tB1) {
+  const int nt = total_tiles(p, s.tile_off);
+  const uint32_t bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
+  int stage = 0;
+  uint32_t phase = 0;
+  long issued = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; ok && t < nt; t += gridDim.x) {
+    const TileInfo ti = decode_tile(p, s.tile_off, t);
+    for (int ks = 0; ks < ti.ks; ++ks) {
+      if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
+      uint64_t* fb = &s.full[stage];
+      uint8_t* sa = ring + stage * kStageBytes;
+      uint8_t* sb = sa + kABytes;
+      mbar_arrive_expect_tx(fb, bytes);
+      ++issued;
+      if (p.mode == MODE_KGROUP) {
+        const bool hi = ti.m_tile >= p.m_split;
+        const CUtensorMap* ma = hi ? tA1 : tA0;
+        const int mcol = (ti.m_tile - (hi ? p.m_split : 0)) * kTileM;
+        const int krow = ti.k0row + ks * kBK;
+        tma_load_2d(sa, ma, fb, mcol, krow);
+        tma_load_2d(sa + kABytes / 2, ma, fb, mcol + 64, krow);
+        for (int i = 0; i < p.BN / 64; ++i)
+          tma_load_2d(sb + i * 8192, tB0, fb, ti.n_tile * p.BN + 64 * i, krow);
+      } else {
+        const bool src1 = ks >= p.k_split;
+        const int kk = (src1 ? ks - p.k_split : ks) * kBK;
+        tma_load_2d(sa, src1 ? tA1 : tA0, fb, kk, ti.m_tile * kTileM);
+        if (p.b_mn) {
+          const int krow = ti.e * p.b_group_rows + kk;
+          const CUtensorMap* mb = src1 ? tB1 : tB0;
+          for (int i = 0; i < p.BN / 64; ++i)
+            tma_load_2d(sb + i * 8192, mb, fb, ti.n_tile * p.BN + 64 * i, krow);
+        } else if (p.b_dual) {
+          const int row = ti.e * p.b_group_rows + ti.n_tile * 128;
+          tma_load_2d(sb, tB0, fb, kk, row);
+          tma_load_2d(sb + kBBytesMax / 2, tB1, fb, kk, row);
+        } else {
+          tma_load_2d(sb, src1 ? tB1 : tB0, fb, kk, ti.e * p.b_group_rows + ti.n_tile * p.BN);
+        }
+      }
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+  }
+  if (!ok) {
+    // Do not leave the CTA with copies in flight: wait (bounded) for the
+    // full barriers of the last kStages issues.  Earlier issues completed
+    // before their stage was released for reuse.
+    for (long i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
+      const int st = (int)(i % kStages);
+      const uint32_t par = (uint32_t)((i / kStages) & 1);
+      const uint32_t a = smem_u32(&s.full[st]);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(a, par)) {
+        if (globaltimer() - t0 > kWaitLimitNs) break;
+      }
+    }
+  }
+}
+
+MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_base) {
+  const int nt = total_tiles(p, s.tile_off);
+  const int n_mma = p.b_dual ? 256 : p.BN;
+  const uint32_t idesc = idesc_bf16_f32(kTileM, n_mma, p.a_mn, p.b_mn);
+  int stage = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; ok && t < nt; t += gridDim.x, ++it) {
+    const TileInfo ti = decode_tile(p, s.tile_off, t);
+    const int acc = it & 1;
+    const uint32_t use = (uint32_t)(it >> 1);
+    if (!mbar_wait(&s.tempty[acc], (use & 1u) ^ 1u, &s.abort, p.err)) { ok = false; break; }
+    tc_fence_after();
+    const uint32_t tmem_d = tmem_base + (uint32_t)acc * 256u;
+    for (int ks = 0; ks < ti.ks; ++ks) {
+      if (!mbar_wait(&s.full[stage], phase, &s.abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(ring + stage * kStageBytes);
+      const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                   : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+        const uint64_t bd = p.b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                   : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+        tc_mma_bf16(tmem_d, ad, bd, idesc, (ks | k) != 0 ? 1u : 0u);
+      }
+      tc_commit(&s.empty[stage]);
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    tc_commit(&s.tfull[acc]);
+  }
+  // everything this thread issued must be finished before TMEM is freed
+  tc_commit(&s.fin);
+  const uint32_t a = smem_u32(&s.fin);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, 0)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      raise_error(p.err, MOE_DEVERR_TIMEOUT);
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+// Each epilogue thread owns one row of the 128-row tile; `tb` is the TMEM
+// address of that row's accumulator (lane field set, column 0).
+MOE_DEV void store_bf16x32(__nv_bfloat16* dst, const uint32_t* v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    d4[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+  }
+}
+
+MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t tb) {
+  uint32_t v[32];
+  if (p.epi == EPI_BF16) {
+    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) + row * p.ldo + (int64_t)ti.n_tile * p.BN;
+    for (int c = 0; c < p.BN; c += 32) {
+      tmem_ld32(tb + c, v);
+      store_bf16x32(out + c, v);
+    }
+  } else if (p.epi == EPI_SWIGLU_FWD) {
+    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+    const int64_t off = row * p.ldo + (int64_t)ti.n_tile * 128;
+    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) + off;
+    __nv_bfloat16* U = static_cast<__nv_bfloat16*>(p.out1) + off;
+    __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out2) + off;
+    uint32_t w[32];
+    for (int c = 0; c < 128; c += 32) {
+      tmem_ld32x2(tb + c, tb + 128 + c, v, w);
+      uint32_t a[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float h = __uint_as_float(v[i]);
+        const float u = __uint_as_float(w[i]);
+        a[i] = __float_as_uint(silu_f(h) * u);
+      }
+      store_bf16x32(H + c, v);
+      store_bf16x32(U + c, w);
+      store_bf16x32(A + c, a);
+    }
+  } else if (p.epi == EPI_SWIGLU_BWD) {
+    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+    const int64_t off = row * p.ldo + (int64_t)ti.n_tile * p.BN;
+    const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
+    const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
+    __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(p.out0) + off;
+    __nv_bfloat16* dU = static_cast<__nv_bfloat16*>(p.out1) + off;
+    for (int c = 0; c < p.BN; c += 32) {
+      tmem_ld32(tb + c, v);
+      uint32_t gh[32], gu[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float h[8], u[8];
+        unpack8(H[c / 8 + q], h);
+        unpack8(U[c / 8 + q], u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float da = __uint_as_float(v[8 * q + i]);
+          const float sg = 1.0f / (1.0f + __expf(-h[i]));
+          const float si = h[i] * sg;
+          const float ds = sg * (1.0f + h[i] * (1.0f - sg));
+          gh[8 * q + i] = __float_as_uint(da * u[i] * ds);
+          gu[8 * q + i] = __float_as_uint(da * si);
+        }
+      }
+      store_bf16x32(dH + c, gh);
+      store_bf16x32(dU + c, gu);
+    }
+  } else if (p.epi == EPI_F32) {
+    const bool hi = ti.m_tile >= p.m_split;
+    float* out = static_cast<float*>(hi ? p.out1 : p.out0) + (int64_t)ti.e * p.out_group_stride +
+                 ((int64_t)(ti.m_tile - (hi ? p.m_split : 0)) * kTileM + r) * p.ldo +
+                 (int64_t)ti.n_tile * p.BN;
+    for (int c = 0; c < p.BN; c += 32) {
+      float4* d4 = reinterpret_cast<float4*>(out + c);
+      if (ti.ks == 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        tmem_ld32(tb + c, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+  } else {  // EPI_ROUTER: fp32 logits (+ bias), rows < T and columns < E only
+    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+    float* out = static_cast<float*>(p.out0);
+    for (int c = 0; c < p.BN; c += 32) {
+      tmem_ld32(tb + c, v);      // warp-collective: executed by every lane
+      if (row < p.m_valid) {
+        for (int i = 0; i < 32 && c + i < p.n_valid; ++i) {
+          float val = __uint_as_float(v[i]);
+          if (p.bias != nullptr) val += p.bias[row * p.n_valid + c + i];
+          out[row * p.n_valid + c + i] = val;
+        }
+      }
+    }
+  }
+}
+
+MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane) {
+  const int nt = total_tiles(p, s.tile_off);
+  const int quarter = warp & 3;            // TMEM lanes this warp may access
+  const int r = quarter * 32 + lane;
+  int it = 0;
+  for (int t = blockIdx.x; t < nt; t += gridDim.x, ++it) {
+    const TileInfo ti = decode_tile(p, s.tile_off, t);
+    const int acc = it & 1;
+    const uint32_t use = (uint32_t)(it >> 1);
+    if (!mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err)) break;
+    tc_fence_after();
+    const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * 256u;
+    epilogue_tile(p, ti, r, tb);
+    tc_fence_before();
+    mbar_arrive(&s.tempty[acc]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
+                        const __grid_constant__ CUtensorMap tA1,
+                        const __grid_constant__ CUtensorMap tB0,
+                        const __grid_constant__ CUtensorMap tB1, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctl& s = *reinterpret_cast<Ctl*>(ring + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], kEpiThreads);
+    }
+    mbar_init(&s.fin, 1);
+    s.abort = 0;
+    fence_barrier_init();
+  }
+  if (p.mode != MODE_DENSE) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.tile_off[i] = p.tile_offsets[i];
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tA0);
+    prefetch_tensormap(&tA1);
+    prefetch_tensormap(&tB0);
+    prefetch_tensormap(&tB1);
+  }
+  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) producer(p, s, ring, &tA0, &tA1, &tB0, &tB1);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(p, s, ring, tmem_base);
+  } else {
+    epilogue(p, s, tmem_base, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// box of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t gemm_init_attributes() {
+  if (!get_encoder()) return cudaErrorInitializationError;
+  return cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
+}
+
+cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
+  if (!get_encoder()) return cudaErrorInitializationError;
+  const DeviceInfo* di = device_info();
+  if (di == nullptr || !di->ready) return cudaErrorInitializationError;
+  Params p = {};
+  CUtensorMap A0, A1, B0, B1;
+  const uint64_t rows = (uint64_t)g.rows_max;
+  const int d = g.d, f = g.f, E = g.E;
+  bool ok = true;
+  p.E = E;
+  p.tile_offsets = g.tile_offsets;
+  p.err = g.err;
+  p.k_split = 1 << 30;
+  p.m_split = 1 << 30;
+  int64_t max_tiles = 0;
+  switch (g.op) {
+    case OP_FWD1_SWIGLU:
+      p.mode = MODE_MGROUP; p.epi = EPI_SWIGLU_FWD; p.b_dual = 1; p.BN = 256;
+      p.n_tiles = f / 128; p.k_steps = d / kBK; p.b_group_rows = f;
+      ok = make_map(&A0, g.a0, d, rows, 64, 128) && make_map(&B0, g.w0, d, (uint64_t)E * f, 64, 128) &&
+           make_map(&B1, g.w1, d, (uint64_t)E * f, 64, 128);
+      A1 = A0;
+      p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.ldo = f;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_FWD2:
+      p.mode = MODE_MGROUP; p.epi = EPI_BF16; p.BN = (d % 256 == 0) ? 256 : 128;
+      p.n_tiles = d / p.BN; p.k_steps = f / kBK; p.b_group_rows = d;
+      ok = make_map(&A0, g.a0, f, rows, 64, 128) &&
+           make_map(&B0, g.w0, f, (uint64_t)E * d, 64, (uint32_t)p.BN);
+      A1 = A0; B1 = B0;
+      p.out0 = g.out0; p.ldo = d;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_DGRAD2_SWIGLU:
+      p.mode = MODE_MGROUP; p.epi = EPI_SWIGLU_BWD; p.b_mn = 1; p.BN = (f % 256 == 0) ? 256 : 128;
+      p.n_tiles = f / p.BN; p.k_steps = d / kBK; p.b_group_rows = d;
+      ok = make_map(&A0, g.a0, d, rows, 64, 128) && make_map(&B0, g.w0, f, (uint64_t)E * d, 64, 64);
+      A1 = A0; B1 = B0;
+      p.out0 = g.out0; p.out1 = g.out1; p.aux0 = g.aux0; p.aux1 = g.aux1; p.ldo = f;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_DGRAD1:
+      p.mode = MODE_MGROUP; p.epi = EPI_BF16; p.b_mn = 1; p.BN = (d % 256 == 0) ? 256 : 128;
+      p.n_tiles = d / p.BN; p.k_steps = 2 * f / kBK; p.k_split = f / kBK; p.b_group_rows = f;
+      ok = make_map(&A0, g.a0, f, rows, 64, 128) && make_map(&A1, g.a1, f, rows, 64, 128) &&
+           make_map(&B0, g.w0, d, (uint64_t)E * f, 64, 64) &&
+           make_map(&B1, g.w1, d, (uint64_t)E * f, 64, 64);
+      p.out0 = g.out0; p.ldo = d;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_WGRAD2:
+      p.mode = MODE_KGROUP; p.epi = EPI_F32; p.a_mn = 1; p.b_mn = 1;
+      p.BN = (f % 256 == 0) ? 256 : 128; p.m_tiles = d / kTileM; p.n_tiles = f / p.BN;
+      ok = make_map(&A0, g.a0, d, rows, 64, 64) && make_map(&B0, g.a1, f, rows, 64, 64);
+      A1 = A0; B1 = B0;
+      p.out0 = g.out0; p.ldo = f; p.out_group_stride = (int64_t)d * f;
+      max_tiles = (int64_t)E * p.m_tiles * p.n_tiles;
+      break;
+    case OP_WGRAD1:
+      p.mode = MODE_KGROUP; p.epi = EPI_F32; p.a_mn = 1; p.b_mn = 1;
+      p.BN = (d % 256 == 0) ? 256 : 128; p.m_tiles = 2 * f / kTileM; p.m_split = f / kTileM;
+      p.n_tiles = d / p.BN;
+      ok = make_map(&A0, g.a0, f, rows, 64, 64) && make_map(&A1, g.a1, f, rows, 64, 64) &&
+           make_map(&B0, g.aux0, d, rows, 64, 64);
+      B1 = B0;
+      p.out0 = g.out0; p.out1 = g.out1; p.ldo = d; p.out_group_stride = (int64_t)f * d;
+      max_tiles = (int64_t)E * p.m_tiles * p.n_tiles;
+      break;
+    case OP_ROUTER: {
+      p.mode = MODE_DENSE; p.epi = EPI_ROUTER; p.BN = ((E + 15) / 16) * 16;
+      p.n_tiles = 1; p.m_tiles = (g.T + kTileM - 1) / kTileM; p.m_valid = g.T; p.n_valid = E;
+      p.k_steps = d / kBK;
+      ok = make_map(&A0, g.a0, d, (uint64_t)g.T, 64, 128) &&
+           make_map(&B0, g.w0, d, (uint64_t)E, 64, (uint32_t)p.BN);
+      A1 = A0; B1 = B0;
+      p.out0 = g.out0; p.bias = g.bias;
+      max_tiles = p.m_tiles;
+      break;
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  int grid = (int)(max_tiles < di->sm_count ? max_tiles : di->sm_count);
+  if (grid < 1) grid = 1;
+  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

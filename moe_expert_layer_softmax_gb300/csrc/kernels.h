@@ -1,0 +1,84 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+// Every launcher enqueues on `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Tokens handled by one block of the top-k kernel; the per-block expert
+// histograms and route ranks are taken over these tokens.
+constexpr int kRouteTokensPerBlock = 64;
+
+struct DeviceInfo {
+  int sm_count = 0;
+  bool ready = false;
+};
+const DeviceInfo* device_info();
+
+// ---------------------------------------------------------------- routing
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                              float* gates, int32_t* local_rank, int32_t* block_hist,
+                              int32_t* err, cudaStream_t s);
+cudaError_t launch_route_scan(int32_t* block_hist, int n_blocks, int E, int32_t* counts,
+                              int32_t* offsets, int32_t* tile_offsets, cudaStream_t s);
+cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_rank,
+                               const int32_t* block_base, const int32_t* counts,
+                               const int32_t* tile_offsets, int T, int E, int k, int64_t rows_max,
+                               int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
+                               cudaStream_t s);
+
+// ---------------------------------------------------------------- data movement
+cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
+                                 const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                                 int E, int k, void* xd, cudaStream_t s);
+cudaError_t launch_combine(const void* y, const float* gates, const int32_t* slot_of_route, int T,
+                           int d, int k, void* out, cudaStream_t s);
+cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* gates,
+                               const int32_t* topk_idx, const int32_t* slot_of_route,
+                               const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                               int E, int k, void* dy, float* d_gates, float* dlogits,
+                               cudaStream_t s);
+cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
+                                const int32_t* topk_idx, const float* dlogits,
+                                const void* w_router, int T, int d, int E, int k, void* dx,
+                                cudaStream_t s);
+cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t* route_of_slot,
+                              const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                              int E, int k, int64_t tiles_max, float* partial, float* dw_router,
+                              cudaStream_t s);
+
+// ---------------------------------------------------------------- grouped GEMM
+enum GemmOp {
+  OP_FWD1_SWIGLU = 0,
+  OP_FWD2 = 1,
+  OP_DGRAD2_SWIGLU = 2,
+  OP_DGRAD1 = 3,
+  OP_WGRAD2 = 4,
+  OP_WGRAD1 = 5,
+  OP_ROUTER = 6,
+};
+
+struct GemmLaunch {
+  int op;
+  int T, d, E, f;
+  int64_t rows_max;
+  const int32_t* tile_offsets;
+  const void* a0;
+  const void* a1;
+  const void* w0;
+  const void* w1;
+  const void* aux0;
+  const void* aux1;
+  const float* bias;
+  void* out0;
+  void* out1;
+  void* out2;
+  int32_t* err;
+};
+cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t s);
+cudaError_t gemm_init_attributes();
+
+}  // namespace moe

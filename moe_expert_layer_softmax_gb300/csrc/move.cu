@@ -1,0 +1,342 @@
+// Data-movement kernels (sm_103a), all HBM-bound, 16-byte vector accesses:
+//   dispatch      x[t] -> xd[slot(t, j)] for every choice j (rowwise: each token
+//                 row is written straight into its expert's contiguous buffer,
+//                 "Supercharging Olmo-core for Efficient and Scalable MoE
+//                 Training", Abstract) and zero padding rows;
+//   combine       out[t] = sum_j g_tj y[slot(t, j)]  (fp32 sum in j order);
+//   combine_bwd   d_gates, dy, dlogits;
+//   dispatch_bwd  dx[t] = sum_j dxd[slot(t, j)] + sum_j dl_tj W_r[e_tj];
+//   router_bwd    dW_r[e] = sum of dl * x over expert e's routes (two passes:
+//                 per-tile partial sums, then a fixed-order sum over tiles).
+// One warp per token row; a lane moves 8 bf16 (16 bytes) per access.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kMoveThreads = 256;
+constexpr int kWarpsPerBlock = kMoveThreads / 32;
+constexpr int kVec = 8;  // bf16 per 16-byte vector
+
+// Zero row `row` (d bf16) with one warp.
+MOE_DEV void zero_row(uint4* base, int d, int lane) {
+  const int nv = d / kVec;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int c = lane; c < nv; c += 32) base[c] = z;
+}
+
+// Padding rows of expert e: [128*tile_off[e] + counts[e], 128*tile_off[e+1]).
+// `p` enumerates E*128 candidates; returns the row or -1.
+MOE_DEV int pad_row(int p, const int32_t* counts, const int32_t* tile_offsets) {
+  const int e = p / kTileM;
+  const int q = p % kTileM;
+  const int row = tile_offsets[e] * kTileM + counts[e] + q;
+  return (row < tile_offsets[e + 1] * kTileM) ? row : -1;
+}
+
+__global__ void __launch_bounds__(kMoveThreads) dispatch_bf16_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ slot_of_route,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
+    int E, int k, int token_blocks, uint4* __restrict__ xd) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int nv = d / kVec;
+  if (blockIdx.x < token_blocks) {
+    const int t = w;
+    if (t >= T) return;
+    const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
+    const uint4* src = x + (size_t)t * nv;
+    for (int c0 = 0; c0 < nv; c0 += 32 * 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < nv) v[u] = __ldg(src + c);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+        uint4* dst = xd + (size_t)slot * nv;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < nv) dst[c] = v[u];
+        }
+      }
+    }
+  } else {
+    const int p = (blockIdx.x - token_blocks) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (p >= E * kTileM) return;
+    const int row = pad_row(p, counts, tile_offsets);
+    if (row >= 0) zero_row(xd + (size_t)row * nv, d, lane);
+  }
+}
+
+__global__ void __launch_bounds__(kMoveThreads) combine_kernel(
+    const uint4* __restrict__ y, const float* __restrict__ gates,
+    const int32_t* __restrict__ slot_of_route, int T, int d, int k, uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int nv = d / kVec;
+  const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
+  const float my_g = (lane < k) ? gates[(size_t)t * k + lane] : 0.0f;
+  // the column loop is warp-uniform (shuffles inside); lanes past the row end
+  // read column 0 and do not store
+  for (int c0 = 0; c0 < nv; c0 += 32) {
+    const int c = c0 + lane;
+    const bool ok = c < nv;
+    const int cc = ok ? c : 0;
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
+    int j = 0;
+    for (; j + 4 <= k; j += 4) {
+      uint4 v[4];
+      float g[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int slot = __shfl_sync(0xffffffffu, my_slot, j + u);
+        g[u] = __shfl_sync(0xffffffffu, my_g, j + u);
+        v[u] = __ldg(y + (size_t)slot * nv + cc);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float f[kVec];
+        unpack8(v[u], f);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) acc[i] = fmaf(g[u], f[i], acc[i]);
+      }
+    }
+    for (; j < k; ++j) {
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+      const float g = __shfl_sync(0xffffffffu, my_g, j);
+      float f[kVec];
+      unpack8(__ldg(y + (size_t)slot * nv + cc), f);
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    }
+    if (ok) out[(size_t)t * nv + c] = pack8(acc);
+  }
+}
+
+__global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
+    const uint4* __restrict__ d_out, const uint4* __restrict__ y, const float* __restrict__ gates,
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_of_route,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
+    int E, int k, int token_blocks, uint4* __restrict__ dy, float* __restrict__ d_gates,
+    float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int nv = d / kVec;
+  if (blockIdx.x >= token_blocks) {
+    const int p = (blockIdx.x - token_blocks) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (p >= E * kTileM) return;
+    const int row = pad_row(p, counts, tile_offsets);
+    if (row >= 0) zero_row(dy + (size_t)row * nv, d, lane);
+    return;
+  }
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
+  const float my_g = (lane < k) ? gates[(size_t)t * k + lane] : 0.0f;
+  const int my_id = (lane < k) ? topk_idx[(size_t)t * k + lane] : 0;
+  const uint4* dO = d_out + (size_t)t * nv;
+  float my_dg = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+    const float g = __shfl_sync(0xffffffffu, my_g, j);
+    const uint4* yr = y + (size_t)slot * nv;
+    uint4* dyr = dy + (size_t)slot * nv;
+    float part = 0.0f;
+    for (int c = lane; c < nv; c += 32) {
+      float a[kVec], b[kVec], o[kVec];
+      unpack8(__ldg(dO + c), a);
+      unpack8(__ldg(yr + c), b);
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) {
+        part = fmaf(a[i], b[i], part);
+        o[i] = g * a[i];
+      }
+      dyr[c] = pack8(o);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == j) my_dg = part;
+  }
+  // dl_j = g_j (dg_j - sum_i g_i dg_i) on the selected experts
+  float inner = (lane < k) ? my_g * my_dg : 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) inner += __shfl_xor_sync(0xffffffffu, inner, off);
+  const float my_dl = my_g * (my_dg - inner);
+  if (lane < k) d_gates[(size_t)t * k + lane] = my_dg;
+  if (dlogits != nullptr) {
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      float v = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int id = __shfl_sync(0xffffffffu, my_id, j);
+        const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+        if (id == e) v = dl;
+      }
+      if (e < E) dlogits[(size_t)t * E + e] = v;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_kernel(
+    const uint4* __restrict__ dxd, const int32_t* __restrict__ slot_of_route,
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ dlogits,
+    const uint4* __restrict__ w_router, int T, int d, int E, int k, uint4* __restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int nv = d / kVec;
+  const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
+  const int my_id = (lane < k) ? topk_idx[(size_t)t * k + lane] : 0;
+  const float my_dl =
+      (lane < k && w_router != nullptr) ? dlogits[(size_t)t * E + my_id] : 0.0f;
+  for (int c0 = 0; c0 < nv; c0 += 32) {   // warp-uniform (shuffles inside)
+    const int c = c0 + lane;
+    const bool ok = c < nv;
+    const int cc = ok ? c : 0;
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+      float f[kVec];
+      unpack8(__ldg(dxd + (size_t)slot * nv + cc), f);
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) acc[i] += f[i];
+    }
+    if (w_router != nullptr) {
+      for (int j = 0; j < k; ++j) {
+        const int id = __shfl_sync(0xffffffffu, my_id, j);
+        const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+        float f[kVec];
+        unpack8(__ldg(w_router + (size_t)id * nv + cc), f);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
+      }
+    }
+    if (ok) dx[(size_t)t * nv + c] = pack8(acc);
+  }
+}
+
+// Pass 1: partial[m][col] = sum over the real rows s of tile m of
+// dlogits[t(s), e(m)] * x[t(s)][col], for a 1024-column chunk (128 threads x 8).
+constexpr int kRbThreads = 128;
+__global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
+    const uint4* __restrict__ x, const float* __restrict__ dlogits,
+    const int32_t* __restrict__ route_of_slot, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ tile_offsets, int d, int E, int k, float* __restrict__ partial) {
+  const int m = blockIdx.x;
+  if (m >= tile_offsets[E]) return;
+  // expert owning tile m: the largest e with tile_offsets[e] <= m
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_offsets[mid] <= m) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int nv = d / kVec;
+  const int c = blockIdx.y * kRbThreads + threadIdx.x;
+  const int row_end = tile_offsets[e] * kTileM + counts[e];
+  const int r0 = m * kTileM;
+  const int r1 = min(r0 + kTileM, row_end);
+  float acc[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
+  if (c < nv) {
+    for (int r = r0; r < r1; ++r) {
+      const int route = route_of_slot[r];
+      const int t = route / k;
+      const float dl = dlogits[(size_t)t * E + e];
+      float f[kVec];
+      unpack8(__ldg(x + (size_t)t * nv + c), f);
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
+    }
+    float4* dst = reinterpret_cast<float4*>(partial + (size_t)m * d + (size_t)c * kVec);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// Pass 2: dW_r[e][col] = sum over e's tiles in order (zero for empty experts).
+__global__ void __launch_bounds__(256) router_bwd_reduce_kernel(
+    const float* __restrict__ partial, const int32_t* __restrict__ tile_offsets, int d,
+    float* __restrict__ dw) {
+  const int e = blockIdx.y;
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  if (col >= d) return;
+  float s = 0.0f;
+  for (int m = tile_offsets[e]; m < tile_offsets[e + 1]; ++m) s += partial[(size_t)m * d + col];
+  dw[(size_t)e * d + col] = s;
+}
+
+int pad_blocks(int E) { return (E * kTileM + kWarpsPerBlock - 1) / kWarpsPerBlock; }
+
+}  // namespace
+
+cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
+                                 const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                                 int E, int k, void* xd, cudaStream_t s) {
+  const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  dispatch_bf16_kernel<<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+      static_cast<const uint4*>(x), slot_of_route, counts, tile_offsets, T, d, E, k, tb,
+      static_cast<uint4*>(xd));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const float* gates, const int32_t* slot_of_route, int T,
+                           int d, int k, void* out, cudaStream_t s) {
+  const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  combine_kernel<<<tb, kMoveThreads, 0, s>>>(static_cast<const uint4*>(y), gates, slot_of_route, T,
+                                             d, k, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* gates,
+                               const int32_t* topk_idx, const int32_t* slot_of_route,
+                               const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                               int E, int k, void* dy, float* d_gates, float* dlogits,
+                               cudaStream_t s) {
+  const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  combine_bwd_kernel<<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+      static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
+      slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
+      dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
+                                const int32_t* topk_idx, const float* dlogits,
+                                const void* w_router, int T, int d, int E, int k, void* dx,
+                                cudaStream_t s) {
+  const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  dispatch_bwd_kernel<<<tb, kMoveThreads, 0, s>>>(
+      static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
+      static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t* route_of_slot,
+                              const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                              int E, int k, int64_t tiles_max, float* partial, float* dw_router,
+                              cudaStream_t s) {
+  (void)T;
+  const int nv = d / kVec;
+  dim3 g1((unsigned)tiles_max, (unsigned)((nv + kRbThreads - 1) / kRbThreads));
+  router_bwd_partial_kernel<<<g1, kRbThreads, 0, s>>>(static_cast<const uint4*>(x), dlogits,
+                                                      route_of_slot, counts, tile_offsets, d, E, k,
+                                                      partial);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2((unsigned)((d + 255) / 256), (unsigned)E);
+  router_bwd_reduce_kernel<<<g2, 256, 0, s>>>(partial, tile_offsets, d, dw_router);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,236 @@
+// Routing kernels (sm_103a): warp-shuffle softmax/top-k with renormalised gates,
+// per-block expert histograms with stable in-block ranks, the counts/offsets
+// scan, and the slot maps.  All routing metadata stays on the device
+// ("Supercharging Olmo-core for Efficient and Scalable MoE Training", Abstract;
+// Section 24.1: the device-resident metadata removes the host wait without
+// changing the routing calculation).
+//
+// Determinism: a route's slot is (base of its block for its expert) + (its rank
+// among the block's routes of that expert, in (token, choice) order), and the
+// block bases are a scan over blocks in block order.  This is exactly the
+// sequential walk over routes in ascending (t, j) order, independent of timing.
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTopkThreads = 256;  // 8 warps; each warp handles 8 of the block's 64 tokens
+
+// Order used for the selection: larger key first, lower expert id on ties.
+// NaN is treated as -inf so that the selection stays a valid set of k distinct
+// experts; the token is flagged and its gates are zeroed.
+MOE_DEV float route_key(float v) { return (v != v) ? -CUDART_INF_F : v; }
+
+template <int EPL>
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gates, int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
+    int32_t* __restrict__ err) {
+  __shared__ int32_t s_sel[kRouteTokensPerBlock * 32];  // expert of each route of the block
+  __shared__ int32_t s_cnt[256];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * kRouteTokensPerBlock;
+  const int ntok = min(kRouteTokensPerBlock, T - t0);
+
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+
+  for (int tl = warp; tl < ntok; tl += kTopkThreads / 32) {
+    const int t = t0 + tl;
+    const float* row = logits + (size_t)t * E;
+    float key[EPL];
+    uint32_t taken = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      float v = (e < E) ? __ldg(row + e) : 0.0f;
+      if (e < E && !isfinite(v)) bad = true;
+      key[i] = route_key(v);
+      if (e >= E) taken |= 1u << i;
+    }
+    const bool token_bad = __any_sync(0xffffffffu, bad);
+
+    float my_val = 0.0f, lmax = 0.0f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = 0.0f;
+      int bid = -1;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        if (!(taken & (1u << i)) && (bid < 0 || key[i] > bv)) {
+          bv = key[i];
+          bid = lane + 32 * i;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oid = __shfl_xor_sync(0xffffffffu, bid, off);
+        if (oid >= 0 && (bid < 0 || ov > bv || (ov == bv && oid < bid))) {
+          bv = ov;
+          bid = oid;
+        }
+      }
+      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+      if (j == 0) lmax = bv;
+      if (lane == j) {
+        my_val = bv;
+        my_id = bid;
+      }
+      if (lane == 0) s_sel[tl * k + j] = bid;
+    }
+    // gates: softmax over the k selected logits (equal to the full softmax
+    // renormalised over the selection)
+    float ex = (lane < k) ? expf(my_val - lmax) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = my_id;
+      gates[(size_t)t * k + lane] = token_bad ? 0.0f : ex / sum;
+    }
+    if (token_bad && lane == 0) raise_error(err, MOE_DEVERR_NONFINITE_LOGIT);
+  }
+  __syncthreads();
+
+  // Stable ranks of the block's routes within their experts, in route order.
+  if (warp == 0) {
+    const int n = ntok * k;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = 0; base < n; base += 32) {
+      const int r = base + lane;
+      const bool active = r < n;
+      const uint32_t act = __ballot_sync(0xffffffffu, active);
+      if (active) {
+        const int e = s_sel[r];
+        const uint32_t peers = __match_any_sync(act, e);
+        const int rank = s_cnt[e] + __popc(peers & lt_mask);
+        local_rank[(size_t)t0 * k + r] = rank;
+        __syncwarp(act);
+        if ((__ffs(peers) - 1) == lane) s_cnt[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[(size_t)blockIdx.x * E + e] = s_cnt[e];
+}
+
+// One block, one thread per expert.  block_hist[b][e] (routes of expert e in
+// block b) is replaced by the absolute first row of block b's routes of e.
+__global__ void __launch_bounds__(256) route_scan_kernel(int32_t* __restrict__ block_hist,
+                                                         int n_blocks, int E,
+                                                         int32_t* __restrict__ counts,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ tile_offsets) {
+  __shared__ int32_t s_c[256];
+  __shared__ int32_t s_t[256];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int b = 0; b < n_blocks; ++b) {
+      const int h = block_hist[(size_t)b * E + e];
+      block_hist[(size_t)b * E + e] = run;
+      run += h;
+    }
+  }
+  s_c[e] = (e < E) ? run : 0;
+  s_t[e] = (e < E) ? (run + kTileM - 1) / kTileM : 0;
+  __syncthreads();
+  // inclusive Hillis-Steele scans over 256 entries
+  for (int off = 1; off < 256; off <<= 1) {
+    const int c = (e >= off) ? s_c[e - off] : 0;
+    const int t = (e >= off) ? s_t[e - off] : 0;
+    __syncthreads();
+    s_c[e] += c;
+    s_t[e] += t;
+    __syncthreads();
+  }
+  if (e < E) {
+    counts[e] = run;
+    offsets[e + 1] = s_c[e];
+    tile_offsets[e + 1] = s_t[e];
+    const int row0 = (s_t[e] - (run + kTileM - 1) / kTileM) * kTileM;
+    for (int b = 0; b < n_blocks; ++b) block_hist[(size_t)b * E + e] += row0;
+  }
+  if (e == 0) {
+    offsets[0] = 0;
+    tile_offsets[0] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(256) route_slots_kernel(
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ local_rank,
+    const int32_t* __restrict__ block_base, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ tile_offsets, int T, int E, int k, int64_t rows_max,
+    int32_t* __restrict__ slot_of_route, int32_t* __restrict__ route_of_slot,
+    int32_t* __restrict__ err) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t R = (int64_t)T * k;
+  if (i < R) {
+    const int t = (int)(i / k);
+    const int b = t / kRouteTokensPerBlock;
+    const int e = topk_idx[i];
+    const int slot = (e >= 0 && e < E) ? block_base[(size_t)b * E + e] + local_rank[i] : -1;
+    if (slot < 0 || slot >= rows_max) {   // never expected
+      raise_error(err, MOE_DEVERR_BOUNDS);
+      slot_of_route[i] = 0;
+      return;
+    }
+    slot_of_route[i] = slot;
+    route_of_slot[slot] = (int32_t)i;
+  } else if (i < R + (int64_t)E * kTileM) {
+    const int p = (int)(i - R);
+    const int e = p / kTileM;
+    const int q = p % kTileM;
+    const int row = tile_offsets[e] * kTileM + counts[e] + q;
+    if (row < tile_offsets[e + 1] * kTileM) route_of_slot[row] = -1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                              float* gates, int32_t* local_rank, int32_t* block_hist,
+                              int32_t* err, cudaStream_t s) {
+  const int nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  const int epl = (E + 31) / 32;
+  if (epl <= 1)
+    route_topk_kernel<1><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+                                                    block_hist, err);
+  else if (epl <= 2)
+    route_topk_kernel<2><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+                                                    block_hist, err);
+  else if (epl <= 4)
+    route_topk_kernel<4><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+                                                    block_hist, err);
+  else
+    route_topk_kernel<8><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+                                                    block_hist, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan(int32_t* block_hist, int n_blocks, int E, int32_t* counts,
+                              int32_t* offsets, int32_t* tile_offsets, cudaStream_t s) {
+  route_scan_kernel<<<1, 256, 0, s>>>(block_hist, n_blocks, E, counts, offsets, tile_offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_rank,
+                               const int32_t* block_base, const int32_t* counts,
+                               const int32_t* tile_offsets, int T, int E, int k, int64_t rows_max,
+                               int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
+                               cudaStream_t s) {
+  const int64_t n = (int64_t)T * k + (int64_t)E * kTileM;
+  const int nb = (int)((n + 255) / 256);
+  route_slots_kernel<<<nb, 256, 0, s>>>(topk_idx, local_rank, block_base, counts, tile_offsets, T,
+                                        E, k, rows_max, slot_of_route, route_of_slot, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

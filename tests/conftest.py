@@ -27,3 +27,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def moe_gpu():
+    """Build the library, initialise it on cuda:0 and return (module, device)."""
+    import torch
+
+    import moe_expert_layer_softmax_gb300 as m
+    from moe_expert_layer_softmax_gb300 import _build
+
+    _build.build()
+    torch.cuda.set_device(0)
+    m.init(0)
+    return m, torch.device("cuda", 0)

@@ -1,0 +1,165 @@
+"""Whole-layer parity: moe_layer_fwd + moe_layer_bwd through the C ABI against
+the oracle, on small shapes and on the full-size workloads (the same calls and
+launch configuration the benchmark times), plus CUDA-graph capture/replay.
+GPU only."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from synth import CONFIGS, make_inputs
+from gpu_util import f64, max_abs_rel, near_tie_tokens, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+def run_layer(m, dev, inp, k, use_router, logits32=None, backward=True):
+    T, d, E, f = inp["T"], inp["d"], inp["E"], inp["f"]
+    s = m.shape(T, d, E, k, f)
+    buf = m.allocate(s)
+    t = {n: to_dev_bf16(inp[n], dev) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out")}
+    bias = torch.from_numpy(inp["bias"]).to(dev) if (use_router and inp["bias"] is not None) else None
+    if not use_router:
+        buf.saved["logits"].copy_(torch.from_numpy(logits32))
+    wr = t["w_router"] if use_router else None
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    m.clear_error(buf.ws)
+    m.forward(buf, t["x"], wr, bias, t["w_gate"], t["w_up"], t["w_down"], out)
+    if backward:
+        m.backward(buf, t["d_out"], t["x"], wr, t["w_gate"], t["w_up"], t["w_down"])
+    err = m.read_error(buf.ws)
+    res = {"out": f64(out), "err": err}
+    res.update({n: v.cpu().numpy() for n, v in buf.saved.items()
+                if n in ("logits", "topk_idx", "gates", "counts", "offsets", "tile_offsets",
+                         "slot_of_route", "route_of_slot")})
+    if backward:
+        res.update({n: f64(v) for n, v in buf.grads.items()
+                    if n in ("dx", "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits")})
+    return res
+
+
+def compare_grads(g, b, use_router, rows=None):
+    pairs = [("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down")]
+    for mine, ref in pairs:
+        r = max_abs_rel(g[mine], b[ref])
+        assert r <= TOL, (mine, r)
+    sel = slice(None) if rows is None else rows
+    for mine, ref in [("dx", "dx"), ("d_gates", "d_gates"), ("dlogits", "dlogits")]:
+        r = max_abs_rel(g[mine][sel], b[ref][sel])
+        assert r <= TOL, (mine, r)
+    if use_router:
+        r = max_abs_rel(g["dw_router"], b["dW_router"])
+        assert r <= TOL, ("dw_router", r)
+
+
+SMALL = [(256, 128, 8, 2, 256), (300, 256, 6, 2, 384), (1000, 512, 16, 4, 256), (77, 384, 4, 4, 128),
+         (1, 128, 4, 2, 128)]
+
+
+@pytest.mark.parametrize("T,d,E,k,f", SMALL, ids=lambda v: str(v))
+def test_layer_on_shared_logits(moe_gpu, T, d, E, k, f):
+    """Routing bit-exact, every floating-point output within 2e-2."""
+    m, dev = moe_gpu
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=3 * T + d)
+    L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
+    g = run_layer(m, dev, inp, k, use_router=False, logits32=L32)
+    assert g["err"] == 0
+    fwd = O.layer_forward(inp["x"], None, None, inp["w_gate"], inp["w_up"], inp["w_down"], k,
+                          logits=L32)
+    bwd = O.layer_backward(fwd, inp["d_out"], inp["x"], None, inp["w_gate"], inp["w_up"],
+                           inp["w_down"])
+    for n in ("topk_idx", "counts", "offsets", "tile_offsets", "slot_of_route"):
+        np.testing.assert_array_equal(g[n], fwd[n], err_msg=n)
+    assert max_abs_rel(g["out"], fwd["out"]) <= TOL
+    compare_grads(g, bwd, use_router=False)
+
+
+def check_full_path(m, dev, inp, k, backward=True):
+    """Router projection on the device; tokens at a near-tie of the oracle's
+    logits may choose differently and are left out of the per-token checks."""
+    g = run_layer(m, dev, inp, k, use_router=True, backward=backward)
+    assert g["err"] == 0
+    fwd = O.layer_forward(inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                          inp["w_down"], k)
+    assert max_abs_rel(g["logits"], fwd["logits"]) < 1e-5
+    tol = 1e-5 * np.abs(fwd["logits"]).max()
+    tie = near_tie_tokens(fwd["logits"], k, 2 * tol)
+    same = (g["topk_idx"] == fwd["topk_idx"]).all(1)
+    assert same[~tie].all()
+    if same.all():
+        for n in ("counts", "offsets", "tile_offsets", "slot_of_route"):
+            np.testing.assert_array_equal(g[n], fwd[n], err_msg=n)
+    assert max_abs_rel(g["out"][same], fwd["out"][same]) <= TOL
+    if backward:
+        bwd = O.layer_backward(fwd, inp["d_out"], inp["x"], inp["w_router"], inp["w_gate"],
+                               inp["w_up"], inp["w_down"])
+        compare_grads(g, bwd, use_router=True, rows=same)
+    return g
+
+
+@pytest.mark.parametrize("T,d,E,k,f", SMALL[:3], ids=lambda v: str(v))
+def test_layer_with_router_projection(moe_gpu, T, d, E, k, f):
+    m, dev = moe_gpu
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=5 * T + d)
+    check_full_path(m, dev, inp, k)
+
+
+def test_tiny_forward_workload(moe_gpu):
+    """The 256-token, d=128, 8-expert top-2 forward (routing from x.W_r alone, seed 0)."""
+    m, dev = moe_gpu
+    cfg = CONFIGS["tiny_fwd"]
+    inp = make_inputs(cfg, seed=0)
+    check_full_path(m, dev, inp, cfg.k, backward=False)
+
+
+@pytest.mark.parametrize("name", ["fine_grained", "large_pool", "skewed"])
+def test_full_size_workload(moe_gpu, name):
+    """Full-size bf16 workloads, forward and backward, same calls as the benchmark."""
+    m, dev = moe_gpu
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, seed=0)
+    g = check_full_path(m, dev, inp, cfg.k)
+    if name == "skewed":
+        assert (g["counts"] == 0).sum() >= 4
+        empty = np.where(g["counts"] == 0)[0]
+        assert (g["dw_gate"][empty] == 0).all() and (g["dw_down"][empty] == 0).all()
+
+
+def test_graph_capture_replays_bitwise(moe_gpu):
+    """The whole fwd+bwd captures into one CUDA graph (no host sync inside) and
+    replays deterministically."""
+    m, dev = moe_gpu
+    T, d, E, k, f = 512, 256, 8, 2, 256
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=11)
+    s = m.shape(T, d, E, k, f)
+    buf = m.allocate(s)
+    t = {n: to_dev_bf16(inp[n], dev) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out")}
+    bias = torch.from_numpy(inp["bias"]).to(dev)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        m.forward(buf, t["x"], t["w_router"], bias, t["w_gate"], t["w_up"], t["w_down"], out)
+        m.backward(buf, t["d_out"], t["x"], t["w_router"], t["w_gate"], t["w_up"], t["w_down"])
+
+    names = ("dx", "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits")
+    step()
+    torch.cuda.synchronize()
+    eager = [out.clone()] + [buf.grads[n].clone() for n in names]
+    graph = torch.cuda.CUDAGraph()
+    s_cap = torch.cuda.Stream()
+    s_cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_cap):
+        with torch.cuda.graph(graph, stream=s_cap, capture_error_mode="global"):
+            step()
+    torch.cuda.current_stream().wait_stream(s_cap)
+    for _ in range(3):
+        out.zero_()
+        for n in names:
+            buf.grads[n].zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        now = [out] + [buf.grads[n] for n in names]
+        for a, b in zip(eager, now):
+            assert torch.equal(a, b)
+    assert m.read_error(buf.ws) == 0
