@@ -8,14 +8,17 @@
 // Here each expert's rows are padded only to the 128-row tile, and the tile
 // schedule is read from the device-resident tile_offsets.
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: 128-byte-swizzled A/B tiles into a 4-stage ring
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warp 0     TMA producer: 128-byte-swizzled A/B tiles into a ring of as many
+//              stages as fit in 224 KB (4 for 128x256 bf16 tiles, up to 12 for
+//              the narrow router tile)
 //   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
 //              (128 x N x 16 bf16 MMAs, fp32 accumulators in tensor memory,
 //              two 256-column accumulators so the epilogue of one tile
 //              overlaps the main loop of the next)
-//   warps 2-5  epilogue: tcgen05.ld -> fused SwiGLU / SwiGLU-backward / bias /
-//              fp32 -> global stores
+//   warps 2-9  epilogue, two warps per TMEM lane quarter (each takes half of
+//              the tile's columns): tcgen05.ld -> fused SwiGLU /
+//              SwiGLU-backward / bias / fp32 -> global stores
 // Every wait is bounded (error word + abort flag); an aborted CTA waits for
 // its own copies in flight and frees its tensor memory before returning.
 //
@@ -39,19 +42,19 @@ namespace {
 enum Mode { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
 enum Epi { EPI_BF16 = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_F32 = 3, EPI_ROUTER = 4 };
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 12;
+constexpr int kRingBytes = 224 * 1024;
 constexpr int kBK = 64;                       // bf16 elements of K per stage (128 bytes)
 constexpr int kABytes = kTileM * kBK * 2;     // 16 KB
 constexpr int kBBytesMax = 256 * kBK * 2;     // 32 KB
-constexpr int kStageBytes = kABytes + kBBytesMax;
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
 constexpr int kMaxE = 256;
 constexpr uint32_t kTmemCols = 512;           // two 256-column fp32 accumulators
 
 struct __align__(8) Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t fin;
@@ -60,7 +63,7 @@ struct __align__(8) Ctl {
   int32_t tile_off[kMaxE + 1];
 };
 
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (int)sizeof(Ctl);
+constexpr int kSmemBytes = 1024 + kRingBytes + (int)sizeof(Ctl);
 
 struct Params {
   int mode;
@@ -78,6 +81,8 @@ struct Params {
   int k_split;           // DENSE/MGROUP: steps >= k_split read maps A1/B1
   int m_split;           // KGROUP: M tiles >= m_split read A1 and write out1
   int b_group_rows;      // expert stride in the rows of B's 2-D view
+  int stages;            // ring depth
+  int stage_bytes;       // A tile + B tile, a multiple of 1024
   void* out0;
   void* out1;
   void* out2;
@@ -134,7 +139,7 @@ MOE_DEV float silu_f(float h) { return h / (1.0f + __expf(-h)); }
 MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap* tA0,
                       const CUtensorMap* tA1, const CUtensorMap* tB0, const CUtensorMap* tB1) {
   const int nt = total_tiles(p, s.tile_off);
-  const uint32_t bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
+  const uint32_t bytes = (uint32_t)p.stage_bytes;
   int stage = 0;
   uint32_t phase = 0;
   long issued = 0;
@@ -144,7 +149,7 @@ MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap*
     for (int ks = 0; ks < ti.ks; ++ks) {
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
       uint64_t* fb = &s.full[stage];
-      uint8_t* sa = ring + stage * kStageBytes;
+      uint8_t* sa = ring + stage * p.stage_bytes;
       uint8_t* sb = sa + kABytes;
       mbar_arrive_expect_tx(fb, bytes);
       ++issued;
@@ -174,16 +179,16 @@ MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap*
           tma_load_2d(sb, src1 ? tB1 : tB0, fb, kk, ti.e * p.b_group_rows + ti.n_tile * p.BN);
         }
       }
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
   if (!ok) {
     // Do not leave the CTA with copies in flight: wait (bounded) for the
-    // full barriers of the last kStages issues.  Earlier issues completed
+    // full barriers of the last `stages` issues.  Earlier issues completed
     // before their stage was released for reuse.
-    for (long i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
-      const int st = (int)(i % kStages);
-      const uint32_t par = (uint32_t)((i / kStages) & 1);
+    for (long i = (issued > p.stages ? issued - p.stages : 0); i < issued; ++i) {
+      const int st = (int)(i % p.stages);
+      const uint32_t par = (uint32_t)((i / p.stages) & 1);
       const uint32_t a = smem_u32(&s.full[st]);
       const uint64_t t0 = globaltimer();
       while (!mbar_try_wait(a, par)) {
@@ -211,7 +216,7 @@ MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_ba
     for (int ks = 0; ks < ti.ks; ++ks) {
       if (!mbar_wait(&s.full[stage], phase, &s.abort, p.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t a_addr = smem_u32(ring + stage * kStageBytes);
+      const uint32_t a_addr = smem_u32(ring + stage * p.stage_bytes);
       const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k) {
@@ -222,7 +227,7 @@ MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_ba
         tc_mma_bf16(tmem_d, ad, bd, idesc, (ks | k) != 0 ? 1u : 0u);
       }
       tc_commit(&s.empty[stage]);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
     tc_commit(&s.tfull[acc]);
@@ -253,23 +258,25 @@ MOE_DEV void store_bf16x32(__nv_bfloat16* dst, const uint32_t* v) {
   }
 }
 
-MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t tb) {
+// Columns [c0, c1) of the tile, 32 at a time.
+MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t tb, int c0, int c1) {
   uint32_t v[32];
   if (p.epi == EPI_BF16) {
     const int64_t row = (int64_t)ti.m_tile * kTileM + r;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) + row * p.ldo + (int64_t)ti.n_tile * p.BN;
-    for (int c = 0; c < p.BN; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
       tmem_ld32(tb + c, v);
       store_bf16x32(out + c, v);
     }
   } else if (p.epi == EPI_SWIGLU_FWD) {
+    // accumulator columns [0, 128) are H, [128, 256) are U for the same f range
     const int64_t row = (int64_t)ti.m_tile * kTileM + r;
     const int64_t off = row * p.ldo + (int64_t)ti.n_tile * 128;
     __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) + off;
     __nv_bfloat16* U = static_cast<__nv_bfloat16*>(p.out1) + off;
     __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out2) + off;
     uint32_t w[32];
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
       tmem_ld32x2(tb + c, tb + 128 + c, v, w);
       uint32_t a[32];
 #pragma unroll
@@ -289,14 +296,34 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
     const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
     __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(p.out0) + off;
     __nv_bfloat16* dU = static_cast<__nv_bfloat16*>(p.out1) + off;
-    for (int c = 0; c < p.BN; c += 32) {
+    // the H/U loads of the next 32 columns are issued before this chunk's math
+    uint4 hn[4], un[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      hn[q] = H[c0 / 8 + q];
+      un[q] = U[c0 / 8 + q];
+    }
+    for (int c = c0; c < c1; c += 32) {
+      uint4 hc[4], uc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        hc[q] = hn[q];
+        uc[q] = un[q];
+      }
+      if (c + 32 < c1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hn[q] = H[(c + 32) / 8 + q];
+          un[q] = U[(c + 32) / 8 + q];
+        }
+      }
       tmem_ld32(tb + c, v);
       uint32_t gh[32], gu[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float h[8], u[8];
-        unpack8(H[c / 8 + q], h);
-        unpack8(U[c / 8 + q], u);
+        unpack8(hc[q], h);
+        unpack8(uc[q], u);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float da = __uint_as_float(v[8 * q + i]);
@@ -315,7 +342,7 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
     float* out = static_cast<float*>(hi ? p.out1 : p.out0) + (int64_t)ti.e * p.out_group_stride +
                  ((int64_t)(ti.m_tile - (hi ? p.m_split : 0)) * kTileM + r) * p.ldo +
                  (int64_t)ti.n_tile * p.BN;
-    for (int c = 0; c < p.BN; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
       float4* d4 = reinterpret_cast<float4*>(out + c);
       if (ti.ks == 0) {
 #pragma unroll
@@ -331,7 +358,7 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
   } else {  // EPI_ROUTER: fp32 logits (+ bias), rows < T and columns < E only
     const int64_t row = (int64_t)ti.m_tile * kTileM + r;
     float* out = static_cast<float*>(p.out0);
-    for (int c = 0; c < p.BN; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
       tmem_ld32(tb + c, v);      // warp-collective: executed by every lane
       if (row < p.m_valid) {
         for (int i = 0; i < 32 && c + i < p.n_valid; ++i) {
@@ -347,7 +374,18 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
 MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane) {
   const int nt = total_tiles(p, s.tile_off);
   const int quarter = warp & 3;            // TMEM lanes this warp may access
+  const int half = (warp - 2) >> 2;        // which half of the tile's columns
   const int r = quarter * 32 + lane;
+  // column range of this warp: half of the tile (of the H half for SwiGLU)
+  const int width = (p.epi == EPI_SWIGLU_FWD) ? 128 : p.BN;
+  int c0, c1;
+  if (width >= 64) {
+    c0 = half * (width / 2);
+    c1 = c0 + width / 2;
+  } else {                                 // narrow router tile: first half only
+    c0 = 0;
+    c1 = (half == 0) ? width : 0;
+  }
   int it = 0;
   for (int t = blockIdx.x; t < nt; t += gridDim.x, ++it) {
     const TileInfo ti = decode_tile(p, s.tile_off, t);
@@ -356,7 +394,7 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     if (!mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err)) break;
     tc_fence_after();
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * 256u;
-    epilogue_tile(p, ti, r, tb);
+    epilogue_tile(p, ti, r, tb, c0, c1);
     tc_fence_before();
     mbar_arrive(&s.tempty[acc]);
   }
@@ -370,12 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Ctl& s = *reinterpret_cast<Ctl*>(ring + kStages * kStageBytes);
+  Ctl& s = *reinterpret_cast<Ctl*>(ring + kRingBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < p.stages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
@@ -541,6 +579,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
+  p.stage_bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
+  p.stages = kRingBytes / p.stage_bytes;
+  if (p.stages > kMaxStages) p.stages = kMaxStages;
+  if (p.stages < 2 || p.stage_bytes % 1024 != 0) return cudaErrorInvalidValue;
   int grid = (int)(max_tiles < di->sm_count ? max_tiles : di->sm_count);
   if (grid < 1) grid = 1;
   grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);

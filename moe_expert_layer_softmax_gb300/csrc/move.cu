@@ -121,6 +121,10 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
   }
 }
 
+// KM = compile-time bound on k (8 covers every workload; 32 is the generic
+// fallback).  Per 256-column chunk a lane loads dOut once and the k rows of y
+// together, so k + 1 16-byte loads are in flight per lane.
+template <int KM>
 __global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
     const uint4* __restrict__ d_out, const uint4* __restrict__ y, const float* __restrict__ gates,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_of_route,
@@ -141,28 +145,48 @@ __global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
   const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
   const float my_g = (lane < k) ? gates[(size_t)t * k + lane] : 0.0f;
   const int my_id = (lane < k) ? topk_idx[(size_t)t * k + lane] : 0;
+  int slot[KM];
+  float g[KM], part[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    slot[j] = __shfl_sync(0xffffffffu, my_slot, j < k ? j : 0);
+    g[j] = __shfl_sync(0xffffffffu, my_g, j < k ? j : 0);
+    part[j] = 0.0f;
+  }
   const uint4* dO = d_out + (size_t)t * nv;
-  float my_dg = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-    const float g = __shfl_sync(0xffffffffu, my_g, j);
-    const uint4* yr = y + (size_t)slot * nv;
-    uint4* dyr = dy + (size_t)slot * nv;
-    float part = 0.0f;
-    for (int c = lane; c < nv; c += 32) {
-      float a[kVec], b[kVec], o[kVec];
+  for (int c0 = 0; c0 < nv; c0 += 32) {      // warp-uniform
+    const int c = c0 + lane;
+    if (c < nv) {
+      float a[kVec];
       unpack8(__ldg(dO + c), a);
-      unpack8(__ldg(yr + c), b);
+      uint4 yv[KM];
 #pragma unroll
-      for (int i = 0; i < kVec; ++i) {
-        part = fmaf(a[i], b[i], part);
-        o[i] = g * a[i];
+      for (int j = 0; j < KM; ++j)
+        if (j < k) yv[j] = __ldg(y + (size_t)slot[j] * nv + c);
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        if (j < k) {
+          float b[kVec], o[kVec];
+          unpack8(yv[j], b);
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) {
+            part[j] = fmaf(a[i], b[i], part[j]);
+            o[i] = g[j] * a[i];
+          }
+          dy[(size_t)slot[j] * nv + c] = pack8(o);
+        }
       }
-      dyr[c] = pack8(o);
     }
+  }
+  float my_dg = 0.0f;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == j) my_dg = part;
+  for (int j = 0; j < KM; ++j) {
+    if (j < k) {
+      float v = part[j];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == j) my_dg = v;
+    }
   }
   // dl_j = g_j (dg_j - sum_i g_i dg_i) on the selected experts
   float inner = (lane < k) ? my_g * my_dg : 0.0f;
@@ -184,6 +208,7 @@ __global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
   }
 }
 
+template <int KM>
 __global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_kernel(
     const uint4* __restrict__ dxd, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ dlogits,
@@ -196,31 +221,49 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_kernel(
   const int my_id = (lane < k) ? topk_idx[(size_t)t * k + lane] : 0;
   const float my_dl =
       (lane < k && w_router != nullptr) ? dlogits[(size_t)t * E + my_id] : 0.0f;
-  for (int c0 = 0; c0 < nv; c0 += 32) {   // warp-uniform (shuffles inside)
+  int slot[KM], id[KM];
+  float dl[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    const int src = j < k ? j : 0;
+    slot[j] = __shfl_sync(0xffffffffu, my_slot, src);
+    id[j] = __shfl_sync(0xffffffffu, my_id, src);
+    dl[j] = __shfl_sync(0xffffffffu, my_dl, src);
+  }
+  for (int c0 = 0; c0 < nv; c0 += 32) {
     const int c = c0 + lane;
-    const bool ok = c < nv;
-    const int cc = ok ? c : 0;
+    if (c >= nv) continue;
+    uint4 v[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) v[j] = __ldg(dxd + (size_t)slot[j] * nv + c);
     float acc[kVec];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-      float f[kVec];
-      unpack8(__ldg(dxd + (size_t)slot * nv + cc), f);
 #pragma unroll
-      for (int i = 0; i < kVec; ++i) acc[i] += f[i];
-    }
-    if (w_router != nullptr) {
-      for (int j = 0; j < k; ++j) {
-        const int id = __shfl_sync(0xffffffffu, my_id, j);
-        const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
         float f[kVec];
-        unpack8(__ldg(w_router + (size_t)id * nv + cc), f);
+        unpack8(v[j], f);
 #pragma unroll
-        for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
+        for (int i = 0; i < kVec; ++i) acc[i] += f[i];
       }
     }
-    if (ok) dx[(size_t)t * nv + c] = pack8(acc);
+    if (w_router != nullptr) {
+#pragma unroll
+      for (int j = 0; j < KM; ++j)
+        if (j < k) v[j] = __ldg(w_router + (size_t)id[j] * nv + c);
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        if (j < k) {
+          float f[kVec];
+          unpack8(v[j], f);
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl[j], f[i], acc[i]);
+        }
+      }
+    }
+    dx[(size_t)t * nv + c] = pack8(acc);
   }
 }
 
@@ -231,6 +274,8 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
     const uint4* __restrict__ x, const float* __restrict__ dlogits,
     const int32_t* __restrict__ route_of_slot, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ tile_offsets, int d, int E, int k, float* __restrict__ partial) {
+  __shared__ int32_t s_tok[kTileM];
+  __shared__ float s_dl[kTileM];
   const int m = blockIdx.x;
   if (m >= tile_offsets[E]) return;
   // expert owning tile m: the largest e with tile_offsets[e] <= m
@@ -241,27 +286,44 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
   }
   const int e = lo;
   const int nv = d / kVec;
-  const int c = blockIdx.y * kRbThreads + threadIdx.x;
   const int row_end = tile_offsets[e] * kTileM + counts[e];
   const int r0 = m * kTileM;
-  const int r1 = min(r0 + kTileM, row_end);
+  const int nrows = max(0, min(kTileM, row_end - r0));
+  if (threadIdx.x < nrows) {
+    const int t = route_of_slot[r0 + threadIdx.x] / k;
+    s_tok[threadIdx.x] = t;
+    s_dl[threadIdx.x] = dlogits[(size_t)t * E + e];
+  }
+  __syncthreads();
+  const int c = blockIdx.y * kRbThreads + threadIdx.x;
+  if (c >= nv) return;
   float acc[kVec];
 #pragma unroll
   for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
-  if (c < nv) {
-    for (int r = r0; r < r1; ++r) {
-      const int route = route_of_slot[r];
-      const int t = route / k;
-      const float dl = dlogits[(size_t)t * E + e];
+  int r = 0;
+  for (; r + 4 <= nrows; r += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(x + (size_t)s_tok[r + u] * nv + c);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
       float f[kVec];
-      unpack8(__ldg(x + (size_t)t * nv + c), f);
+      unpack8(v[u], f);
+      const float dl = s_dl[r + u];
 #pragma unroll
       for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
     }
-    float4* dst = reinterpret_cast<float4*>(partial + (size_t)m * d + (size_t)c * kVec);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
+  for (; r < nrows; ++r) {
+    float f[kVec];
+    unpack8(__ldg(x + (size_t)s_tok[r] * nv + c), f);
+    const float dl = s_dl[r];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
+  }
+  float4* dst = reinterpret_cast<float4*>(partial + (size_t)m * d + (size_t)c * kVec);
+  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // Pass 2: dW_r[e][col] = sum over e's tiles in order (zero for empty experts).
@@ -304,10 +366,16 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                int E, int k, void* dy, float* d_gates, float* dlogits,
                                cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  combine_bwd_kernel<<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
-      static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
-      slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-      dlogits);
+  if (k <= 8)
+    combine_bwd_kernel<8><<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+        static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
+        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
+        dlogits);
+  else
+    combine_bwd_kernel<32><<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+        static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
+        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
+        dlogits);
   return cudaGetLastError();
 }
 
@@ -316,9 +384,14 @@ cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
                                 const void* w_router, int T, int d, int E, int k, void* dx,
                                 cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  dispatch_bwd_kernel<<<tb, kMoveThreads, 0, s>>>(
-      static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
-      static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
+  if (k <= 8)
+    dispatch_bwd_kernel<8><<<tb, kMoveThreads, 0, s>>>(
+        static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
+        static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
+  else
+    dispatch_bwd_kernel<32><<<tb, kMoveThreads, 0, s>>>(
+        static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
+        static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
   return cudaGetLastError();
 }
 

@@ -121,44 +121,77 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
   for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[(size_t)blockIdx.x * E + e] = s_cnt[e];
 }
 
-// One block, one thread per expert.  block_hist[b][e] (routes of expert e in
-// block b) is replaced by the absolute first row of block b's routes of e.
-__global__ void __launch_bounds__(256) route_scan_kernel(int32_t* __restrict__ block_hist,
-                                                         int n_blocks, int E,
-                                                         int32_t* __restrict__ counts,
-                                                         int32_t* __restrict__ offsets,
-                                                         int32_t* __restrict__ tile_offsets) {
+// One block of 1024 threads.  Thread (p, e) = (tid / Epad, tid % Epad) owns
+// expert e and the p-th contiguous chunk of the top-k blocks.  block_hist[b][e]
+// (routes of expert e in block b) is replaced by the absolute first row of
+// block b's routes of e; counts, offsets and tile_offsets are written.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
+    int32_t* __restrict__ block_hist, int n_blocks, int E, int e_pad,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ tile_offsets) {
+  __shared__ int32_t s_part[kScanThreads];  // [p][e] chunk sums
   __shared__ int32_t s_c[256];
   __shared__ int32_t s_t[256];
-  const int e = threadIdx.x;
-  int run = 0;
+  const int tid = threadIdx.x;
+  const int e = tid % e_pad;
+  const int p = tid / e_pad;
+  const int P = kScanThreads / e_pad;
+  const int cb = (n_blocks + P - 1) / P;
+  const int b0 = min(n_blocks, p * cb);
+  const int b1 = min(n_blocks, b0 + cb);
+  int sum = 0;
+  if (e < E)
+    for (int b = b0; b < b1; ++b) sum += block_hist[(size_t)b * E + e];
+  s_part[tid] = sum;
+  __syncthreads();
+  int prefix = 0, total = 0;
   if (e < E) {
-    for (int b = 0; b < n_blocks; ++b) {
-      const int h = block_hist[(size_t)b * E + e];
-      block_hist[(size_t)b * E + e] = run;
-      run += h;
+    for (int q = 0; q < P; ++q) {
+      const int v = s_part[q * e_pad + e];
+      prefix += (q < p) ? v : 0;
+      total += v;
     }
   }
-  s_c[e] = (e < E) ? run : 0;
-  s_t[e] = (e < E) ? (run + kTileM - 1) / kTileM : 0;
+  if (tid < 256) {
+    s_c[tid] = 0;
+    s_t[tid] = 0;
+  }
   __syncthreads();
-  // inclusive Hillis-Steele scans over 256 entries
+  if (p == 0 && e < E) {
+    s_c[e] = total;
+    s_t[e] = (total + kTileM - 1) / kTileM;
+  }
+  __syncthreads();
+  // inclusive Hillis-Steele scans over 256 entries (threads 0..255)
   for (int off = 1; off < 256; off <<= 1) {
-    const int c = (e >= off) ? s_c[e - off] : 0;
-    const int t = (e >= off) ? s_t[e - off] : 0;
+    int c = 0, t = 0;
+    if (tid < 256 && tid >= off) {
+      c = s_c[tid - off];
+      t = s_t[tid - off];
+    }
     __syncthreads();
-    s_c[e] += c;
-    s_t[e] += t;
+    if (tid < 256) {
+      s_c[tid] += c;
+      s_t[tid] += t;
+    }
     __syncthreads();
   }
   if (e < E) {
-    counts[e] = run;
-    offsets[e + 1] = s_c[e];
-    tile_offsets[e + 1] = s_t[e];
-    const int row0 = (s_t[e] - (run + kTileM - 1) / kTileM) * kTileM;
-    for (int b = 0; b < n_blocks; ++b) block_hist[(size_t)b * E + e] += row0;
+    const int tiles = (total + kTileM - 1) / kTileM;
+    if (p == 0) {
+      counts[e] = total;
+      offsets[e + 1] = s_c[e];
+      tile_offsets[e + 1] = s_t[e];
+    }
+    int base = (s_t[e] - tiles) * kTileM + prefix;
+    for (int b = b0; b < b1; ++b) {
+      const int h = block_hist[(size_t)b * E + e];
+      block_hist[(size_t)b * E + e] = base;
+      base += h;
+    }
   }
-  if (e == 0) {
+  if (tid == 0) {
     offsets[0] = 0;
     tile_offsets[0] = 0;
   }
@@ -217,7 +250,10 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 
 cudaError_t launch_route_scan(int32_t* block_hist, int n_blocks, int E, int32_t* counts,
                               int32_t* offsets, int32_t* tile_offsets, cudaStream_t s) {
-  route_scan_kernel<<<1, 256, 0, s>>>(block_hist, n_blocks, E, counts, offsets, tile_offsets);
+  int e_pad = 4;
+  while (e_pad < E) e_pad <<= 1;   // E <= 256 -> at least 4 chunks per expert
+  route_scan_kernel<<<1, kScanThreads, 0, s>>>(block_hist, n_blocks, E, e_pad, counts, offsets,
+                                               tile_offsets);
   return cudaGetLastError();
 }
 
