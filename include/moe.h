@@ -73,6 +73,7 @@ extern "C" {
 #define MOE_ERR_ALIGN (-3)       /* a device pointer is not 16-byte aligned       */
 #define MOE_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed          */
 #define MOE_ERR_NOT_INIT (-5)    /* moe_init() was not called for this device     */
+#define MOE_ERR_SCRATCH_LIMIT (-6) /* shape needs more than moe_route_noalloc's fixed scratch */
 
 /* bits of the device error word (first int32 of the workspace) */
 #define MOE_DEVERR_NONFINITE_LOGIT 0x1 /* a router logit was NaN/Inf             */
@@ -146,6 +147,29 @@ MOE_API int moe_route(const moe_shape_t* shape, const void* x, const void* w_rou
               const float* logit_bias, float* logits, int32_t* topk_idx, float* gates,
               int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
               int32_t* slot_of_route, int32_t* route_of_slot, void* ws, void* stream);
+
+/* Allocation-free variant of moe_route.  The pages have no counterpart to this
+ * call: it exists for callers that cannot hand the library a workspace buffer
+ * (code running inside a CUDA graph capture, where cudaMalloc is not allowed;
+ * code that must stay out of the allocator because cudaMalloc can synchronise
+ * the device; hosts working inside a fixed, pre-assigned memory budget).
+ *
+ * Same arguments and results as moe_route, without `ws`.  Its scratch (error
+ * word, per-block histograms, per-route ranks) lives in one static device
+ * array of 2 MiB inside the library, kept by every GPU that loads the library
+ * until the process exits.  Shapes needing more scratch than that
+ * (256 + roundup256(ceil(T/64)*E*4) + roundup256(T*k*4) bytes) return
+ * MOE_ERR_SCRATCH_LIMIT and queue nothing.  Nothing is allocated.
+ *   dev_error  device int32 (nullable): receives the call's device error bits.
+ * The first call on a device looks up the array's address with that device
+ * current; make it before any stream capture starts.  All calls share the array
+ * (each clears the error word; the rest is rewritten): calls that overlap on the
+ * GPU race and must be serialised by the caller. */
+MOE_API int moe_route_noalloc(const moe_shape_t* shape, const void* x, const void* w_router,
+                              const float* logit_bias, float* logits, int32_t* topk_idx,
+                              float* gates, int32_t* counts, int32_t* offsets,
+                              int32_t* tile_offsets, int32_t* slot_of_route,
+                              int32_t* route_of_slot, int32_t* dev_error, void* stream);
 
 /* ------------------------------------------------------------ dispatch (a4)
  * Rowwise dispatch: xd[slot_of_route[t*k+j]] = x[t]; padding rows of every

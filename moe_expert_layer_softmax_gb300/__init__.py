@@ -33,13 +33,15 @@ DEVERR_TIMEOUT = 0x2
 DEVERR_BOUNDS = 0x4
 
 _ERRORS = {-1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_ALIGN",
-           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_NOT_INIT"}
+           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_NOT_INIT", -6: "MOE_ERR_SCRATCH_LIMIT"}
+ERR_SCRATCH_LIMIT = -6
 
 # every symbol the C header declares
 EXPORTS = (
     "moe_init", "moe_rows_max", "moe_workspace_size", "moe_clear_error", "moe_read_error",
     "moe_route", "moe_dispatch", "moe_quantize_mxfp8", "moe_grouped_gemm", "moe_combine",
     "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
+    "moe_route_noalloc",
 )
 
 
@@ -100,6 +102,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_clear_error": [_vp, _vp],
         "moe_read_error": [_vp, P(i32), _vp],
         "moe_route": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
+        "moe_route_noalloc": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_dispatch": [P(Shape)] + [_vp] * 6 + [_vp],
         "moe_quantize_mxfp8": [i32, i32, i32, i32, _vp, _vp, _vp, _vp],
         "moe_grouped_gemm": [P(Shape), i32, P(GemmArgs), _vp, _vp],
@@ -187,6 +190,16 @@ def route(s, x, w_router, logit_bias, logits, topk_idx, gates, counts, offsets, 
         ctypes.byref(s), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(logits), _ptr(topk_idx),
         _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(tile_offsets), _ptr(slot_of_route),
         _ptr(route_of_slot), _ptr(ws), _stream(stream)))
+
+
+def route_noalloc(s, x, w_router, logit_bias, logits, topk_idx, gates, counts, offsets,
+                  tile_offsets, slot_of_route, route_of_slot, dev_error=None, stream=None):
+    """moe_route without a workspace: for callers that cannot allocate device
+    memory (see include/moe.h); scratch lives in the library's static array."""
+    _check("moe_route_noalloc", load().moe_route_noalloc(
+        ctypes.byref(s), _ptr(x), _ptr(w_router), _ptr(logit_bias), _ptr(logits), _ptr(topk_idx),
+        _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(tile_offsets), _ptr(slot_of_route),
+        _ptr(route_of_slot), _ptr(dev_error), _stream(stream)))
 
 
 def dispatch(s, x, slot_of_route, counts, tile_offsets, xd, xd_scales=None, stream=None):
