@@ -217,12 +217,15 @@ def run_ours(args, cfg):
 
     x, wr, wg, wu, wd, dO = (bf(inp[n]) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out"))
     bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
-    s = m.shape(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
+    mx = cfg.prec == "mxfp8"
+    s = m.shape(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, prec=m.MXFP8 if mx else m.BF16)
     buf = m.allocate(s)
     out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
+        if mx:   # the weight caches follow every weight update: rebuilt once per step
+            m.build_mx_weights(s, wg, wu, wd, buf.mx_weights)
         m.forward(buf, x, wr, bias, wg, wu, wd, out)
         m.backward(buf, dO, x, wr, wg, wu, wd)
 
@@ -253,7 +256,8 @@ def run_ours(args, cfg):
     value = job_value(world, cfg.T, ms_max)
 
     # ---- per-stage times (same kernels, called stage by stage, events on the stream)
-    stages = stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=max(3, args.steps))
+    stages = stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=max(3, args.steps),
+                         mx=mx)
     fl = gemm_flops(cfg)
     gemm_ms = sum(stages[k] for k in ("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"))
     gemm_fl = sum(fl[k] for k in ("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"))
@@ -261,9 +265,14 @@ def run_ours(args, cfg):
     dom = max(("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"), key=lambda k: stages[k])
     achieved = fl[dom] / (stages[dom] / 1000.0) / 1e12
     peak = peaks["bf16_tflops_sustained"]
+    peak_note = f"{peaks['source']} sustained bf16 (kernel timed inside the step)"
+    if mx and dom in ("fwd1", "fwd2", "dgrad2", "dgrad1"):
+        # dense fp8 is twice the dense bf16 rate on this part (2.25 -> 4.5 PFLOP/s nominal)
+        peak = 2.0 * peaks["bf16_tflops_sustained"]
+        peak_note = f"{peaks['source']} sustained bf16 x 2 (nominal fp8/bf16 ratio)"
     roofline = {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({dom})", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                "peak_source": f"{peaks['source']} sustained bf16 (kernel timed inside the step)",
+                "peak_source": peak_note,
                 "algorithmic": f"{fl[dom] / 1e9:.1f} GFLOP per launch (useful flops, no tile padding)"}
 
     # ---- end to end through the public API with host buffers
@@ -272,16 +281,20 @@ def run_ours(args, cfg):
     if m.read_error(buf.ws) != 0:
         raise RuntimeError("device error word set during the timed region")
 
-    cpu = oracle_sample(cfg, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
-    launches_per_step = 16 if wr is not None else 14
+    # the CPU oracle is timed on the bf16 layer; an MXFP8 sample would be dominated
+    # by re-quantising 1.6 G weight values in numpy, so it is not run there
+    cpu = (oracle_sample(cfg, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline
+                                     and not mx) else None)
+    launches_per_step = (16 if wr is not None else 14) + (9 if mx else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_block(cfg),
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8+bf16" if mx else "bf16",
+        "data": "synthetic", "config": config_block(cfg),
         "gemm": {"tflops": gemm_fl / (gemm_ms / 1000.0) / 1e12, "ms": gemm_ms,
-                 "pct_of_peak": 100.0 * gemm_fl / (gemm_ms / 1000.0) / 1e12 / peak,
-                 "peak_tflops": peak},
+                 "pct_of_bf16_peak": 100.0 * gemm_fl / (gemm_ms / 1000.0) / 1e12
+                 / peaks["bf16_tflops_sustained"],
+                 "bf16_peak_tflops": peaks["bf16_tflops_sustained"]},
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -306,10 +319,12 @@ def load_peaks():
             "source": "fallback"}
 
 
-def stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=5):
+def stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=5, mx=False):
     """Average ms of each stage call, events recorded on the launching stream."""
     import torch
     sv, g = buf.saved, buf.grads
+    if mx:
+        return stage_times_mx(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps)
     calls = [
         ("route", lambda: m.route(s, x, wr, bias, sv["logits"], sv["topk_idx"], sv["gates"],
                                   sv["counts"], sv["offsets"], sv["tile_offsets"],
@@ -353,6 +368,61 @@ def stage_times(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps=5):
     return res
 
 
+def stage_times_mx(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps):
+    """Stage times of the MXFP8 layer (same calls moe_layer_fwd/bwd make)."""
+    import torch
+    sv, g, w, b = buf.saved, buf.grads, buf.mx_weights, buf.mx
+    n, d, f = buf.rows_max, s.d_model, s.d_ff
+    calls = [
+        ("weight_cache", lambda: m.build_mx_weights(s, wg, wu, wd, w)),
+        ("route", lambda: m.route(s, x, wr, bias, sv["logits"], sv["topk_idx"], sv["gates"],
+                                  sv["counts"], sv["offsets"], sv["tile_offsets"],
+                                  sv["slot_of_route"], sv["route_of_slot"], buf.ws)),
+        ("dispatch", lambda: m.dispatch(s, x, sv["slot_of_route"], sv["counts"], sv["tile_offsets"],
+                                        b["xd_q"], b["xd_s"])),
+        ("fwd1", lambda: m.grouped_gemm(s, m.GEMM_FWD1_SWIGLU, buf.ws, tile_offsets=sv["tile_offsets"],
+                                        a0=b["xd_q"], sfa0=b["xd_s"], w0=w["gu_q"], sfb0=w["gu_s"],
+                                        out0=sv["h"], out1=sv["u"], out2=b["a_q"], osf0=b["a_s"])),
+        ("fwd2", lambda: m.grouped_gemm(s, m.GEMM_FWD2, buf.ws, tile_offsets=sv["tile_offsets"],
+                                        a0=b["a_q"], sfa0=b["a_s"], w0=w["down_q"], sfb0=w["down_s"],
+                                        out0=sv["y"])),
+        ("combine", lambda: m.combine(s, sv["y"], sv["gates"], sv["slot_of_route"], out)),
+        ("combine_bwd", lambda: m.combine_bwd(s, dO, sv["y"], sv["gates"], sv["topk_idx"],
+                                              sv["slot_of_route"], sv["counts"], sv["tile_offsets"],
+                                              g["dy"], g["d_gates"], g["dlogits"])),
+        ("quantize_dy", lambda: m.quantize_mxfp8(1, n, d, 1, g["dy"], b["dy_q"], b["dy_s"])),
+        ("dgrad2", lambda: m.grouped_gemm(s, m.GEMM_DGRAD2_SWIGLU, buf.ws,
+                                          tile_offsets=sv["tile_offsets"], a0=b["dy_q"], sfa0=b["dy_s"],
+                                          w0=w["downT_q"], sfb0=w["downT_s"], aux0=sv["h"],
+                                          aux1=sv["u"], out0=g["dh"], out1=g["du"], out2=b["dh_q"],
+                                          out3=b["du_q"], osf0=b["dh_s"], osf1=b["du_s"])),
+        ("dequant_a", lambda: m.dequantize_mxfp8(n, f, b["a_q"], b["a_s"], b["a_dq"])),
+        ("wgrad2", lambda: m.grouped_gemm(s, m.GEMM_WGRAD2, buf.ws, tile_offsets=sv["tile_offsets"],
+                                          a0=g["dy"], a1=b["a_dq"], out0=g["dw_down"])),
+        ("dgrad1", lambda: m.grouped_gemm(s, m.GEMM_DGRAD1, buf.ws, tile_offsets=sv["tile_offsets"],
+                                          a0=b["dh_q"], sfa0=b["dh_s"], a1=b["du_q"], sfa1=b["du_s"],
+                                          w0=w["gateT_q"], sfb0=w["gateT_s"], w1=w["upT_q"],
+                                          sfb1=w["upT_s"], out0=g["dxd"])),
+        ("dequant_xd", lambda: m.dequantize_mxfp8(n, d, b["xd_q"], b["xd_s"], b["xd_dq"])),
+        ("wgrad1", lambda: m.grouped_gemm(s, m.GEMM_WGRAD1, buf.ws, tile_offsets=sv["tile_offsets"],
+                                          a0=g["dh"], a1=g["du"], aux0=b["xd_dq"], out0=g["dw_gate"],
+                                          out1=g["dw_up"])),
+        ("dispatch_bwd", lambda: m.dispatch_bwd(s, g["dxd"], sv["slot_of_route"], sv["topk_idx"],
+                                                g["dlogits"], wr, g["dx"])),
+        ("router_bwd", lambda: m.router_bwd(s, x, g["dlogits"], sv["route_of_slot"], sv["counts"],
+                                            sv["tile_offsets"], g["dw_router"], buf.ws)),
+    ]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+    for r in range(reps):
+        ev[r][0].record(stream)
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            ev[r][i + 1].record(stream)
+    torch.cuda.synchronize()
+    return {name: sum(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps)) / reps
+            for i, (name, _) in enumerate(calls)}
+
+
 def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world):
     """Same step through the public API, with the step's inputs (x, dOut) copied
     from pinned host memory and its results (out, dx) copied back, every step."""
@@ -366,9 +436,13 @@ def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world
     dO = torch.empty_like(x)
     out = torch.empty_like(x)
 
+    mx = buf.mx is not None
+
     def step():
         x.copy_(hx, non_blocking=True)
         dO.copy_(hd, non_blocking=True)
+        if mx:
+            m.build_mx_weights(buf.shape, wg, wu, wd, buf.mx_weights)
         m.forward(buf, x, wr, bias, wg, wu, wd, out)
         m.backward(buf, dO, x, wr, wg, wu, wd)
         ho.copy_(out, non_blocking=True)

@@ -199,6 +199,38 @@ MOE_API int moe_dispatch(const moe_shape_t* shape, const void* x, const int32_t*
 MOE_API int moe_quantize_mxfp8(int32_t batch, int32_t rows, int32_t cols, int32_t block_axis,
                        const void* src, uint8_t* q, uint8_t* scales, void* stream);
 
+/* Inverse of the quantiser for a K-major MXFP8 operand: out[r][k] =
+ * E4M3(q[r][k]) * 2^(scale - 127), stored as bf16 [rows, K] (exact unless the
+ * product leaves the bf16 range).  rows and K multiples of 128.  This is the
+ * global dequantisation that feeds the BF16 weight-gradient GEMMs ("Supercharging
+ * Olmo-core ...", Section 24 Evidence 7 / Table 33). */
+MOE_API int moe_dequantize_mxfp8(int64_t rows, int32_t K, const uint8_t* q, const uint8_t* scales,
+                                 void* out, void* stream);
+
+/* MXFP8 weight caches, quantised once per weight update ("two weight caches",
+ * Section 24 Evidence 10 / Section 24.3): the forward cache is blocked along
+ * d_model for W_gate/W_up and along d_ff for W_down; the data-gradient cache
+ * holds the transposes, blocked along the other axis.  Every array is K-major
+ * for the GEMM that reads it; scales use the MOE_SF layout. */
+typedef struct {
+  uint8_t* gu_q;    /* [E, 2f, d]  W_gate and W_up rows interleaved in 64-row groups:
+                       rows [128j, 128j+64) = W_gate rows [64j, 64j+64),
+                       rows [128j+64, 128j+128) = W_up rows [64j, 64j+64)   */
+  uint8_t* gu_s;    /* scales of gu_q, E * 2f * d/32 bytes                 */
+  uint8_t* down_q;  /* [E, d, f]   W_down, blocks along f                   */
+  uint8_t* down_s;
+  uint8_t* downT_q; /* [E, f, d]   W_down^T, blocks along d                 */
+  uint8_t* downT_s;
+  uint8_t* gateT_q; /* [E, d, f]   W_gate^T, blocks along f                 */
+  uint8_t* gateT_s;
+  uint8_t* upT_q;   /* [E, d, f]   W_up^T, blocks along f                   */
+  uint8_t* upT_s;
+} moe_mx_weights_t;
+
+/* Fill all MXFP8 weight caches from the bf16 master weights (5 quantiser launches). */
+MOE_API int moe_build_mx_weights(const moe_shape_t* shape, const void* w_gate, const void* w_up,
+                                 const void* w_down, const moe_mx_weights_t* cache, void* stream);
+
 /* --------------------------------------------------- grouped GEMMs (a5, a6, a9-a12)
  * Device-scheduled grouped GEMMs on the expert-contiguous buffers.  The tile
  * schedule is read from tile_offsets on the device; no host wait.  Inputs are
@@ -238,7 +270,27 @@ typedef struct {
   void* out0;
   void* out1;
   void* out2;
+  /* MXFP8 only (shape->prec == MOE_MXFP8), see below */
+  const uint8_t* sfa0;
+  const uint8_t* sfa1;
+  const uint8_t* sfb0;
+  const uint8_t* sfb1;
+  void* out3;
+  uint8_t* osf0;
+  uint8_t* osf1;
 } moe_gemm_args_t;
+
+/* With shape->prec == MOE_MXFP8 the data GEMMs run on tcgen05 block-scaled
+ * MXFP8 MMAs (E4M3 x E4M3, E8M0 scales, fp32 accumulation); every a and w operand is
+ * uint8 codes with its scales in the matching sf array (MOE_SF layout):
+ *   FWD1_SWIGLU   a0 = Xd_q [rows,d]; w0 = gu_q cache      out0 = H, out1 = U (bf16),
+ *                                                          out2 = A_q [rows,f], osf0 = its scales
+ *   FWD2          a0 = A_q; w0 = down_q cache              out0 = Y (bf16)
+ *   DGRAD2_SWIGLU a0 = dY_q [rows,d]; w0 = downT_q cache;  out0 = dH, out1 = dU (bf16),
+ *                 aux0 = H, aux1 = U (bf16)                out2 = dH_q, out3 = dU_q, osf0/osf1
+ *   DGRAD1        a0 = dH_q, a1 = dU_q; w0 = gateT_q,      out0 = dXd (bf16)
+ *                 w1 = upT_q
+ * WGRAD1/WGRAD2 stay BF16 (on dequantised activations, moe_dequantize_mxfp8). */
 
 MOE_API int moe_grouped_gemm(const moe_shape_t* shape, int32_t op, const moe_gemm_args_t* args,
                      void* ws, void* stream);
@@ -294,6 +346,24 @@ typedef struct {
   void* y;                /* bf16 [rows_max, d]                          */
 } moe_saved_t;
 
+/* MXFP8 activation buffers (rows_max rows; scales in the MOE_SF layout).
+ * xd_q/xd_s and a_q/a_s are written by the forward and read by the backward;
+ * the rest is backward scratch. */
+typedef struct moe_mx_buffers {
+  uint8_t* xd_q;  /* [rows_max, d] dispatched tokens, quantised once per token */
+  uint8_t* xd_s;
+  uint8_t* a_q;   /* [rows_max, f] SwiGLU output quantised in the GEMM1 epilogue */
+  uint8_t* a_s;
+  uint8_t* dy_q;  /* [rows_max, d] */
+  uint8_t* dy_s;
+  uint8_t* dh_q;  /* [rows_max, f] */
+  uint8_t* dh_s;
+  uint8_t* du_q;  /* [rows_max, f] */
+  uint8_t* du_s;
+  void* xd_dq;    /* bf16 [rows_max, d] dequantised Xd for the weight gradients */
+  void* a_dq;     /* bf16 [rows_max, f] dequantised A for the weight gradients  */
+} moe_mx_buffers_t;
+
 typedef struct {
   const void* x;          /* bf16 [T, d]                                 */
   const void* w_router;   /* bf16 [E, d] or NULL (logits given in saved) */
@@ -302,6 +372,9 @@ typedef struct {
   const void* w_up;       /* bf16 [E, f, d]                              */
   const void* w_down;     /* bf16 [E, d, f]                              */
   void* out;              /* bf16 [T, d]                                 */
+  /* MXFP8 only: weight caches and MXFP8 activation buffers (else NULL) */
+  const moe_mx_weights_t* mx_weights;
+  const struct moe_mx_buffers* mx;
 } moe_fwd_args_t;
 
 typedef struct {
@@ -324,14 +397,22 @@ typedef struct {
   void* dh;               /* bf16 [rows_max, f]                          */
   void* du;               /* bf16 [rows_max, f]                          */
   void* dxd;              /* bf16 [rows_max, d]                          */
+  /* MXFP8 only (else NULL) */
+  const moe_mx_weights_t* mx_weights;
+  const moe_mx_buffers_t* mx;
 } moe_bwd_args_t;
 
-/* route -> dispatch -> FWD1_SWIGLU -> FWD2 -> combine, all on `stream`. */
+/* route -> dispatch -> FWD1_SWIGLU -> FWD2 -> combine, all on `stream`.
+ * MXFP8 mode: the dispatch quantises each token once (Xd_q), GEMM1/GEMM2 run
+ * on the MXFP8 weight cache, saved->xd and saved->a are not used. */
 MOE_API int moe_layer_fwd(const moe_shape_t* shape, const moe_fwd_args_t* args, const moe_saved_t* saved,
                   void* ws, void* stream);
 
 /* combine_bwd -> DGRAD2_SWIGLU -> WGRAD2 -> DGRAD1 -> WGRAD1 -> dispatch_bwd
- * -> router_bwd, all on `stream`, reading what moe_layer_fwd saved. */
+ * -> router_bwd, all on `stream`, reading what moe_layer_fwd saved.
+ * MXFP8 mode: dY is quantised after the combine backward, DGRAD2/DGRAD1 run on
+ * MXFP8 (the second weight cache), and the weight gradients run in BF16 on
+ * dequantised Xd and A. */
 MOE_API int moe_layer_bwd(const moe_shape_t* shape, const moe_bwd_args_t* args, const moe_saved_t* saved,
                   void* ws, void* stream);
 

@@ -41,7 +41,7 @@ EXPORTS = (
     "moe_init", "moe_rows_max", "moe_workspace_size", "moe_clear_error", "moe_read_error",
     "moe_route", "moe_dispatch", "moe_quantize_mxfp8", "moe_grouped_gemm", "moe_combine",
     "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
-    "moe_route_noalloc",
+    "moe_route_noalloc", "moe_dequantize_mxfp8", "moe_build_mx_weights",
 )
 
 
@@ -61,7 +61,22 @@ _vp = ctypes.c_void_p
 
 class GemmArgs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("tile_offsets", "a0", "a1", "w0", "w1", "aux0", "aux1",
-                                   "out0", "out1", "out2")]
+                                   "out0", "out1", "out2", "sfa0", "sfa1", "sfb0", "sfb1",
+                                   "out3", "osf0", "osf1")]
+
+
+MX_WEIGHT_FIELDS = ("gu_q", "gu_s", "down_q", "down_s", "downT_q", "downT_s", "gateT_q",
+                    "gateT_s", "upT_q", "upT_s")
+MX_BUFFER_FIELDS = ("xd_q", "xd_s", "a_q", "a_s", "dy_q", "dy_s", "dh_q", "dh_s", "du_q",
+                    "du_s", "xd_dq", "a_dq")
+
+
+class MxWeights(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in MX_WEIGHT_FIELDS]
+
+
+class MxBuffers(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in MX_BUFFER_FIELDS]
 
 
 class Saved(ctypes.Structure):
@@ -72,13 +87,13 @@ class Saved(ctypes.Structure):
 
 class FwdArgs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("x", "w_router", "logit_bias", "w_gate", "w_up", "w_down",
-                                   "out")]
+                                   "out", "mx_weights", "mx")]
 
 
 class BwdArgs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("d_out", "x", "w_router", "w_gate", "w_up", "w_down", "dx",
                                    "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates",
-                                   "dlogits", "dy", "dh", "du", "dxd")]
+                                   "dlogits", "dy", "dh", "du", "dxd", "mx_weights", "mx")]
 
 
 _lib = None
@@ -105,6 +120,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route_noalloc": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_dispatch": [P(Shape)] + [_vp] * 6 + [_vp],
         "moe_quantize_mxfp8": [i32, i32, i32, i32, _vp, _vp, _vp, _vp],
+        "moe_dequantize_mxfp8": [ctypes.c_int64, i32, _vp, _vp, _vp, _vp],
+        "moe_build_mx_weights": [P(Shape), _vp, _vp, _vp, P(MxWeights), _vp],
         "moe_grouped_gemm": [P(Shape), i32, P(GemmArgs), _vp, _vp],
         "moe_combine": [P(Shape)] + [_vp] * 4 + [_vp],
         "moe_combine_bwd": [P(Shape)] + [_vp] * 10 + [_vp],
@@ -214,6 +231,17 @@ def quantize_mxfp8(batch, rows, cols, block_axis, src, q, scales, stream=None):
         _stream(stream)))
 
 
+def dequantize_mxfp8(rows, K, q, scales, out, stream=None):
+    _check("moe_dequantize_mxfp8", load().moe_dequantize_mxfp8(
+        int(rows), int(K), _ptr(q), _ptr(scales), _ptr(out), _stream(stream)))
+
+
+def build_mx_weights(s, w_gate, w_up, w_down, cache: dict, stream=None):
+    c = MxWeights(**{k: _ptr(cache[k]) for k in MX_WEIGHT_FIELDS})
+    _check("moe_build_mx_weights", load().moe_build_mx_weights(
+        ctypes.byref(s), _ptr(w_gate), _ptr(w_up), _ptr(w_down), ctypes.byref(c), _stream(stream)))
+
+
 def grouped_gemm(s, op, ws, stream=None, **kw):
     a = GemmArgs(**{k: _ptr(v) for k, v in kw.items()})
     _check("moe_grouped_gemm", load().moe_grouped_gemm(ctypes.byref(s), int(op), ctypes.byref(a),
@@ -264,9 +292,20 @@ class LayerBuffers:
     ws: object
     saved: dict
     grads: dict
+    mx_weights: dict | None = None
+    mx: dict | None = None
 
     def saved_struct(self) -> Saved:
         return Saved(**{k: _ptr(v) for k, v in self.saved.items()})
+
+    def mx_structs(self):
+        """(MxWeights, MxBuffers) ctypes structs, or (None, None) in BF16 mode.
+        The structs are kept on the object so their addresses stay valid."""
+        if self.mx is None:
+            return None, None
+        self._mxw = MxWeights(**{k: _ptr(self.mx_weights[k]) for k in MX_WEIGHT_FIELDS})
+        self._mxb = MxBuffers(**{k: _ptr(self.mx.get(k)) for k in MX_BUFFER_FIELDS})
+        return ctypes.addressof(self._mxw), ctypes.addressof(self._mxb)
 
 
 def allocate(s: Shape, device=None, with_grads: bool = True) -> LayerBuffers:
@@ -279,13 +318,16 @@ def allocate(s: Shape, device=None, with_grads: bool = True) -> LayerBuffers:
     i32 = dict(dtype=torch.int32, device=dev)
     f32 = dict(dtype=torch.float32, device=dev)
     ws = torch.zeros(workspace_size(s), dtype=torch.uint8, device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    mx = s.prec == MXFP8
     saved = {
         "logits": torch.empty(T, E, **f32), "topk_idx": torch.empty(T, k, **i32),
         "gates": torch.empty(T, k, **f32), "counts": torch.empty(E, **i32),
         "offsets": torch.empty(E + 1, **i32), "tile_offsets": torch.empty(E + 1, **i32),
         "slot_of_route": torch.empty(T * k, **i32), "route_of_slot": torch.empty(n, **i32),
-        "xd": torch.empty(n, d, **bf), "h": torch.empty(n, f, **bf), "u": torch.empty(n, f, **bf),
-        "a": torch.empty(n, f, **bf), "y": torch.empty(n, d, **bf),
+        "xd": None if mx else torch.empty(n, d, **bf), "h": torch.empty(n, f, **bf),
+        "u": torch.empty(n, f, **bf), "a": None if mx else torch.empty(n, f, **bf),
+        "y": torch.empty(n, d, **bf),
     }
     grads = {}
     if with_grads:
@@ -297,18 +339,37 @@ def allocate(s: Shape, device=None, with_grads: bool = True) -> LayerBuffers:
             "dh": torch.empty(n, f, **bf), "du": torch.empty(n, f, **bf),
             "dxd": torch.empty(n, d, **bf),
         }
-    return LayerBuffers(s, n, ws, saved, grads)
+    mxw = mxb = None
+    if mx:
+        mxw = {"gu_q": torch.empty(E, 2 * f, d, **u8), "gu_s": torch.empty(E * 2 * f * d // 32, **u8),
+               "down_q": torch.empty(E, d, f, **u8), "down_s": torch.empty(E * d * f // 32, **u8),
+               "downT_q": torch.empty(E, f, d, **u8), "downT_s": torch.empty(E * f * d // 32, **u8),
+               "gateT_q": torch.empty(E, d, f, **u8), "gateT_s": torch.empty(E * d * f // 32, **u8),
+               "upT_q": torch.empty(E, d, f, **u8), "upT_s": torch.empty(E * d * f // 32, **u8)}
+        mxb = {"xd_q": torch.empty(n, d, **u8), "xd_s": torch.empty(n * d // 32, **u8),
+               "a_q": torch.empty(n, f, **u8), "a_s": torch.empty(n * f // 32, **u8)}
+        if with_grads:
+            mxb.update({"dy_q": torch.empty(n, d, **u8), "dy_s": torch.empty(n * d // 32, **u8),
+                        "dh_q": torch.empty(n, f, **u8), "dh_s": torch.empty(n * f // 32, **u8),
+                        "du_q": torch.empty(n, f, **u8), "du_s": torch.empty(n * f // 32, **u8),
+                        "xd_dq": torch.empty(n, d, **bf), "a_dq": torch.empty(n, f, **bf)})
+    return LayerBuffers(s, n, ws, saved, grads, mxw, mxb)
 
 
 def forward(buf: LayerBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, out, stream=None):
+    """moe_layer_fwd.  MXFP8 shapes use buf.mx_weights (fill them with
+    build_mx_weights whenever the bf16 weights change)."""
+    mw, mb = buf.mx_structs()
     fa = FwdArgs(x=_ptr(x), w_router=_ptr(w_router), logit_bias=_ptr(logit_bias),
-                 w_gate=_ptr(w_gate), w_up=_ptr(w_up), w_down=_ptr(w_down), out=_ptr(out))
+                 w_gate=_ptr(w_gate), w_up=_ptr(w_up), w_down=_ptr(w_down), out=_ptr(out),
+                 mx_weights=mw, mx=mb)
     layer_fwd(buf.shape, fa, buf.saved_struct(), buf.ws, stream)
 
 
 def backward(buf: LayerBuffers, d_out, x, w_router, w_gate, w_up, w_down, stream=None):
     g = buf.grads
+    mw, mb = buf.mx_structs()
     ba = BwdArgs(d_out=_ptr(d_out), x=_ptr(x), w_router=_ptr(w_router), w_gate=_ptr(w_gate),
-                 w_up=_ptr(w_up), w_down=_ptr(w_down),
+                 w_up=_ptr(w_up), w_down=_ptr(w_down), mx_weights=mw, mx=mb,
                  **{k: _ptr(v) for k, v in g.items()})
     layer_bwd(buf.shape, ba, buf.saved_struct(), buf.ws, stream)

@@ -126,6 +126,17 @@ int route_impl(const moe_shape_t* s, const void* x, const void* w_router, const 
 int gemm_impl(const moe_shape_t* s, int op, const moe_gemm_args_t* a, void* ws, cudaStream_t st) {
   GemmLaunch g = {};
   g.op = op;
+  if (s->prec == MOE_MXFP8) {
+    switch (op) {
+      case MOE_GEMM_FWD1_SWIGLU: g.op = OP_MX_FWD1_SWIGLU; break;
+      case MOE_GEMM_FWD2: g.op = OP_MX_FWD2; break;
+      case MOE_GEMM_DGRAD2_SWIGLU: g.op = OP_MX_DGRAD2_SWIGLU; break;
+      case MOE_GEMM_DGRAD1: g.op = OP_MX_DGRAD1; break;
+      default: break;   // weight gradients stay BF16
+    }
+  }
+  g.sfa0 = a->sfa0; g.sfa1 = a->sfa1; g.sfb0 = a->sfb0; g.sfb1 = a->sfb1;
+  g.out3 = a->out3; g.osf0 = a->osf0; g.osf1 = a->osf1;
   g.T = s->T; g.d = s->d_model; g.E = s->n_experts; g.f = s->d_ff;
   g.rows_max = rows_max_of(s);
   g.tile_offsets = a->tile_offsets;
@@ -134,6 +145,56 @@ int gemm_impl(const moe_shape_t* s, int op, const moe_gemm_args_t* a, void* ws, 
   g.out0 = a->out0; g.out1 = a->out1; g.out2 = a->out2;
   g.err = at<int32_t>(ws, 0);
   MOE_CUDA(launch_grouped_gemm(g, st));
+  return MOE_OK;
+}
+
+// Operands of the MXFP8 data GEMMs (codes, scales and outputs).
+int check_gemm_args_mx(int op, const moe_gemm_args_t* a) {
+  if (a == nullptr) return MOE_ERR_INVALID;
+  MOE_NONNULL_ALIGNED(a->tile_offsets);
+  switch (op) {
+    case MOE_GEMM_FWD1_SWIGLU:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->sfa0); MOE_NONNULL_ALIGNED(a->w0);
+      MOE_NONNULL_ALIGNED(a->sfb0); MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1);
+      MOE_NONNULL_ALIGNED(a->out2); MOE_NONNULL_ALIGNED(a->osf0);
+      break;
+    case MOE_GEMM_FWD2:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->sfa0); MOE_NONNULL_ALIGNED(a->w0);
+      MOE_NONNULL_ALIGNED(a->sfb0); MOE_NONNULL_ALIGNED(a->out0);
+      break;
+    case MOE_GEMM_DGRAD2_SWIGLU:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->sfa0); MOE_NONNULL_ALIGNED(a->w0);
+      MOE_NONNULL_ALIGNED(a->sfb0); MOE_NONNULL_ALIGNED(a->aux0); MOE_NONNULL_ALIGNED(a->aux1);
+      MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1); MOE_NONNULL_ALIGNED(a->out2);
+      MOE_NONNULL_ALIGNED(a->out3); MOE_NONNULL_ALIGNED(a->osf0); MOE_NONNULL_ALIGNED(a->osf1);
+      break;
+    case MOE_GEMM_DGRAD1:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->sfa0); MOE_NONNULL_ALIGNED(a->a1);
+      MOE_NONNULL_ALIGNED(a->sfa1); MOE_NONNULL_ALIGNED(a->w0); MOE_NONNULL_ALIGNED(a->sfb0);
+      MOE_NONNULL_ALIGNED(a->w1); MOE_NONNULL_ALIGNED(a->sfb1); MOE_NONNULL_ALIGNED(a->out0);
+      break;
+    default:
+      return MOE_ERR_INVALID;
+  }
+  return MOE_OK;
+}
+
+bool is_mx_data_gemm(int op) {
+  return op == MOE_GEMM_FWD1_SWIGLU || op == MOE_GEMM_FWD2 || op == MOE_GEMM_DGRAD2_SWIGLU ||
+         op == MOE_GEMM_DGRAD1;
+}
+
+int check_mx_buffers(const moe_mx_weights_t* w, const moe_mx_buffers_t* b, bool bwd) {
+  if (w == nullptr || b == nullptr) return MOE_ERR_INVALID;
+  const void* wp[] = {w->gu_q, w->gu_s, w->down_q, w->down_s, w->downT_q, w->downT_s,
+                      w->gateT_q, w->gateT_s, w->upT_q, w->upT_s};
+  for (const void* p : wp) MOE_NONNULL_ALIGNED(p);
+  MOE_NONNULL_ALIGNED(b->xd_q); MOE_NONNULL_ALIGNED(b->xd_s);
+  MOE_NONNULL_ALIGNED(b->a_q); MOE_NONNULL_ALIGNED(b->a_s);
+  if (bwd) {
+    const void* bp[] = {b->dy_q, b->dy_s, b->dh_q, b->dh_s, b->du_q, b->du_s, b->xd_dq, b->a_dq};
+    for (const void* p : bp) MOE_NONNULL_ALIGNED(p);
+  }
   return MOE_OK;
 }
 
@@ -258,7 +319,13 @@ int moe_dispatch(const moe_shape_t* s, const void* x, const int32_t* slot_of_rou
   MOE_NONNULL_ALIGNED(counts);
   MOE_NONNULL_ALIGNED(tile_offsets);
   MOE_NONNULL_ALIGNED(xd);
-  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (s->prec == MOE_MXFP8) {
+    MOE_NONNULL_ALIGNED(xd_scales);
+    MOE_CUDA(launch_dispatch_mxfp8(x, slot_of_route, counts, tile_offsets, s->T, s->d_model,
+                                   s->n_experts, s->top_k, static_cast<uint8_t*>(xd), xd_scales,
+                                   static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+  }
   if (xd_scales != nullptr) return MOE_ERR_INVALID;
   MOE_CUDA(launch_dispatch_bf16(x, slot_of_route, counts, tile_offsets, s->T, s->d_model,
                                 s->n_experts, s->top_k, xd, static_cast<cudaStream_t>(stream)));
@@ -267,18 +334,63 @@ int moe_dispatch(const moe_shape_t* s, const void* x, const int32_t* slot_of_rou
 
 int moe_quantize_mxfp8(int32_t batch, int32_t rows, int32_t cols, int32_t block_axis,
                        const void* src, uint8_t* q, uint8_t* scales, void* stream) {
-  (void)batch; (void)rows; (void)cols; (void)block_axis; (void)src; (void)q; (void)scales;
-  (void)stream;
-  return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(ready_or_error());
+  if (batch < 1 || rows < 1 || cols < 1 || (block_axis != 0 && block_axis != 1))
+    return MOE_ERR_INVALID;
+  if (rows % 128 != 0 || cols % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NONNULL_ALIGNED(src);
+  MOE_NONNULL_ALIGNED(q);
+  MOE_NONNULL_ALIGNED(scales);
+  MOE_CUDA(launch_quantize_mxfp8(batch, rows, cols, block_axis, src, q, scales,
+                                 static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_dequantize_mxfp8(int64_t rows, int32_t K, const uint8_t* q, const uint8_t* scales,
+                         void* out, void* stream) {
+  MOE_TRY(ready_or_error());
+  if (rows < 1 || K < 1) return MOE_ERR_INVALID;
+  if (rows % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NONNULL_ALIGNED(q);
+  MOE_NONNULL_ALIGNED(scales);
+  MOE_NONNULL_ALIGNED(out);
+  MOE_CUDA(launch_dequantize_mxfp8(q, scales, rows, K, out, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_build_mx_weights(const moe_shape_t* s, const void* w_gate, const void* w_up,
+                         const void* w_down, const moe_mx_weights_t* c, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  if (c == nullptr) return MOE_ERR_INVALID;
+  MOE_NONNULL_ALIGNED(w_gate);
+  MOE_NONNULL_ALIGNED(w_up);
+  MOE_NONNULL_ALIGNED(w_down);
+  const void* ptrs[] = {c->gu_q, c->gu_s, c->down_q, c->down_s, c->downT_q, c->downT_s,
+                        c->gateT_q, c->gateT_s, c->upT_q, c->upT_s};
+  for (const void* p : ptrs) MOE_NONNULL_ALIGNED(p);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int E = s->n_experts, d = s->d_model, f = s->d_ff;
+  // forward cache: gate/up along d, interleaved in 64-row groups; down along f
+  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 1, w_gate, c->gu_q, c->gu_s, st, 64, 0));
+  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 1, w_up, c->gu_q, c->gu_s, st, 64, 64));
+  MOE_CUDA(launch_quantize_mxfp8(E, d, f, 1, w_down, c->down_q, c->down_s, st));
+  // data-gradient cache: the transposes, blocked along the other axis
+  MOE_CUDA(launch_quantize_mxfp8(E, d, f, 0, w_down, c->downT_q, c->downT_s, st));
+  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 0, w_gate, c->gateT_q, c->gateT_s, st));
+  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 0, w_up, c->upT_q, c->upT_s, st));
+  return MOE_OK;
 }
 
 int moe_grouped_gemm(const moe_shape_t* s, int32_t op, const moe_gemm_args_t* args, void* ws,
                      void* stream) {
   MOE_TRY(check_shape(s));
   MOE_TRY(ready_or_error());
-  MOE_TRY(check_gemm_args(op, args));
+  if (s->prec == MOE_MXFP8 && is_mx_data_gemm(op))
+    MOE_TRY(check_gemm_args_mx(op, args));
+  else
+    MOE_TRY(check_gemm_args(op, args));
   MOE_NONNULL_ALIGNED(ws);
-  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return gemm_impl(s, op, args, ws, static_cast<cudaStream_t>(stream));
 }
 
@@ -358,7 +470,8 @@ int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved
   MOE_TRY(check_shape(s));
   MOE_TRY(ready_or_error());
   if (a == nullptr || sv == nullptr) return MOE_ERR_INVALID;
-  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool mx = s->prec == MOE_MXFP8;
+  if (mx) MOE_TRY(check_mx_buffers(a->mx_weights, a->mx, false));
   MOE_NONNULL_ALIGNED(a->x);
   MOE_ALIGNED_OR_NULL(a->w_router);
   MOE_ALIGNED_OR_NULL(a->logit_bias);
@@ -374,16 +487,36 @@ int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved
   MOE_NONNULL_ALIGNED(sv->tile_offsets);
   MOE_NONNULL_ALIGNED(sv->slot_of_route);
   MOE_NONNULL_ALIGNED(sv->route_of_slot);
-  MOE_NONNULL_ALIGNED(sv->xd);
+  if (!mx) {
+    MOE_NONNULL_ALIGNED(sv->xd);
+    MOE_NONNULL_ALIGNED(sv->a);
+  }
   MOE_NONNULL_ALIGNED(sv->h);
   MOE_NONNULL_ALIGNED(sv->u);
-  MOE_NONNULL_ALIGNED(sv->a);
   MOE_NONNULL_ALIGNED(sv->y);
   MOE_NONNULL_ALIGNED(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MOE_TRY(route_impl(s, a->x, a->w_router, a->logit_bias, sv->logits, sv->topk_idx, sv->gates,
                      sv->counts, sv->offsets, sv->tile_offsets, sv->slot_of_route,
                      sv->route_of_slot, ws, st));
+  if (mx) {
+    const moe_mx_weights_t* w = a->mx_weights;
+    const moe_mx_buffers_t* b = a->mx;
+    MOE_CUDA(launch_dispatch_mxfp8(a->x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
+                                   s->d_model, s->n_experts, s->top_k, b->xd_q, b->xd_s, st));
+    moe_gemm_args_t g = {};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = b->xd_q; g.sfa0 = b->xd_s; g.w0 = w->gu_q; g.sfb0 = w->gu_s;
+    g.out0 = sv->h; g.out1 = sv->u; g.out2 = b->a_q; g.osf0 = b->a_s;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
+    g = moe_gemm_args_t{};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = b->a_q; g.sfa0 = b->a_s; g.w0 = w->down_q; g.sfb0 = w->down_s; g.out0 = sv->y;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_FWD2, &g, ws, st));
+    MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->top_k,
+                            a->out, st));
+    return MOE_OK;
+  }
   MOE_CUDA(launch_dispatch_bf16(a->x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
                                 s->d_model, s->n_experts, s->top_k, sv->xd, st));
   moe_gemm_args_t g = {};
@@ -405,7 +538,8 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   MOE_TRY(check_shape(s));
   MOE_TRY(ready_or_error());
   if (a == nullptr || sv == nullptr) return MOE_ERR_INVALID;
-  if (s->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool mx = s->prec == MOE_MXFP8;
+  if (mx) MOE_TRY(check_mx_buffers(a->mx_weights, a->mx, true));
   MOE_NONNULL_ALIGNED(a->d_out);
   MOE_NONNULL_ALIGNED(a->x);
   MOE_ALIGNED_OR_NULL(a->w_router);
@@ -428,6 +562,35 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   MOE_CUDA(launch_combine_bwd(a->d_out, sv->y, sv->gates, sv->topk_idx, sv->slot_of_route,
                               sv->counts, sv->tile_offsets, s->T, s->d_model, s->n_experts,
                               s->top_k, a->dy, a->d_gates, a->dlogits, st));
+  if (mx) {
+    const moe_mx_weights_t* w = a->mx_weights;
+    const moe_mx_buffers_t* b = a->mx;
+    const int64_t rows = rows_max_of(s);
+    MOE_CUDA(launch_quantize_mxfp8(1, (int)rows, s->d_model, 1, a->dy, b->dy_q, b->dy_s, st));
+    moe_gemm_args_t g = {};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = b->dy_q; g.sfa0 = b->dy_s; g.w0 = w->downT_q; g.sfb0 = w->downT_s;
+    g.aux0 = sv->h; g.aux1 = sv->u;
+    g.out0 = a->dh; g.out1 = a->du; g.out2 = b->dh_q; g.out3 = b->du_q;
+    g.osf0 = b->dh_s; g.osf1 = b->du_s;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_DGRAD2_SWIGLU, &g, ws, st));
+    MOE_CUDA(launch_dequantize_mxfp8(b->a_q, b->a_s, rows, s->d_ff, b->a_dq, st));
+    g = moe_gemm_args_t{};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = a->dy; g.a1 = b->a_dq; g.out0 = a->dw_down;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_WGRAD2, &g, ws, st));
+    g = moe_gemm_args_t{};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = b->dh_q; g.sfa0 = b->dh_s; g.a1 = b->du_q; g.sfa1 = b->du_s;
+    g.w0 = w->gateT_q; g.sfb0 = w->gateT_s; g.w1 = w->upT_q; g.sfb1 = w->upT_s;
+    g.out0 = a->dxd;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_DGRAD1, &g, ws, st));
+    MOE_CUDA(launch_dequantize_mxfp8(b->xd_q, b->xd_s, rows, s->d_model, b->xd_dq, st));
+    g = moe_gemm_args_t{};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = a->dh; g.a1 = a->du; g.aux0 = b->xd_dq; g.out0 = a->dw_gate; g.out1 = a->dw_up;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_WGRAD1, &g, ws, st));
+  } else {
   moe_gemm_args_t g = {};
   g.tile_offsets = sv->tile_offsets;
   g.a0 = a->dy; g.w0 = a->w_down; g.aux0 = sv->h; g.aux1 = sv->u;
@@ -445,6 +608,7 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   g.tile_offsets = sv->tile_offsets;
   g.a0 = a->dh; g.a1 = a->du; g.aux0 = sv->xd; g.out0 = a->dw_gate; g.out1 = a->dw_up;
   MOE_TRY(gemm_impl(s, MOE_GEMM_WGRAD1, &g, ws, st));
+  }
   MOE_CUDA(launch_dispatch_bwd(a->dxd, sv->slot_of_route, sv->topk_idx, a->dlogits, a->w_router,
                                s->T, s->d_model, s->n_experts, s->top_k, a->dx, st));
   if (a->w_router != nullptr) {

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -151,6 +152,57 @@ MOE_DEV void tc_mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32
       : "memory");
 }
 
+// Block-scaled MXFP8 MMA (E4M3 x E4M3, E8M0 scales in tensor memory, one
+// scale per 32 K-values; the scale byte of this K=32 step is chosen by the
+// scale-factor ids in the instruction descriptor).
+MOE_DEV void tc_mma_mxf8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                         uint32_t tmem_sfa, uint32_t tmem_sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(tmem_sfa), "r"(tmem_sfb)
+      : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A/B, UE8M0 scales,
+// fp32 accumulation, K-major operands; sf_id picks the scale byte.
+MOE_DEV uint32_t idesc_mxf8(int M, int N, int sf_id) {
+  uint32_t d = 0;
+  d |= (uint32_t)(sf_id & 3) << 4;    // B scale-factor byte
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= 1u << 23;                      // scale type: UE8M0
+  d |= (uint32_t)(M >> 4) << 24;
+  d |= (uint32_t)(sf_id & 3) << 29;   // A scale-factor byte
+  return d;
+}
+
+// Copy 32 rows x 16 bytes of shared memory into tensor-memory lanes 0-31 and
+// replicate them to the other three lane quarters.
+MOE_DEV void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Shared-memory descriptor without swizzle: 16-byte rows, 8-row groups 128 B apart.
+MOE_DEV uint64_t smem_desc_noswz(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Plain bulk copy global -> shared, completion counted on `bar`.
+MOE_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 MOE_DEV void tc_commit(uint64_t* bar) {
@@ -199,6 +251,52 @@ MOE_DEV void tmem_ld32x2(uint32_t taddr0, uint32_t taddr1, uint32_t* r, uint32_t
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]), "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
       : "r"(taddr0), "r"(taddr1)
       : "memory");
+}
+
+// ------------------------------------------------------------------ MXFP8
+// One E8M0 scale per 32 consecutive values along the contraction axis:
+// 2^s with s the smallest integer such that amax <= 448 * 2^s, clamped to
+// [-127, 127] (s = 0 for an all-zero block); codes are E4M3(v / 2^s), round
+// to nearest even, saturating.  With amax = fr * 2^ex (fr in [0.5, 1)) and
+// 448 = 0.875 * 2^9: s = ex - 9 when fr <= 0.875, else ex - 8.
+MOE_DEV int mx_scale_exp(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  if (!isfinite(amax)) return 127;
+  int ex;
+  const float fr = frexpf(amax, &ex);
+  const int s = (fr <= 0.875f) ? ex - 9 : ex - 8;
+  return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// Two floats -> two E4M3 bytes (lo in the low byte), RNE, satfinite.
+MOE_DEV uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// Two E4M3 bytes (low byte first) -> two floats (exact).
+MOE_DEV void e4m3x2_to_f32(uint32_t two, float& lo, float& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(two & 0xFFFFu)));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  lo = __low2float(h);
+  hi = __high2float(h);
+}
+
+// Quantise 8 values (already divided by the block scale) to 8 E4M3 bytes.
+MOE_DEV uint2 e4m3x8(const float* v) {
+  return make_uint2(e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16),
+                    e4m3x2(v[4], v[5]) | (e4m3x2(v[6], v[7]) << 16));
+}
+
+// Byte offset of the scale of (row r, K-block b) of a K-major operand with
+// `kblocks` = K/32 blocks per row, in the layout the MXFP8 GEMM copies to
+// tensor memory: 128-row x 4-block atoms of 512 bytes; inside an atom, row r
+// and block b sit at (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4).
+MOE_DEV size_t sf_offset(int64_t r, int b, int kblocks) {
+  return ((size_t)(r >> 7) * (size_t)(kblocks >> 2) + (size_t)(b >> 2)) * 512u +
+         (size_t)(r & 31) * 16u + (size_t)((r & 127) >> 5) * 4u + (size_t)(b & 3);
 }
 
 }  // namespace moe

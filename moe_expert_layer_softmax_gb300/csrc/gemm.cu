@@ -40,7 +40,11 @@ namespace moe {
 namespace {
 
 enum Mode { MODE_DENSE = 0, MODE_MGROUP = 1, MODE_KGROUP = 2 };
-enum Epi { EPI_BF16 = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_F32 = 3, EPI_ROUTER = 4 };
+enum Epi {
+  EPI_BF16 = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_F32 = 3, EPI_ROUTER = 4,
+  EPI_SWIGLU_FWD_MX = 5,  // H, U bf16 + A quantised to MXFP8 (one block per 32 columns)
+  EPI_SWIGLU_BWD_MX = 6,  // dH, dU bf16 + both quantised to MXFP8
+};
 
 constexpr int kMaxStages = 12;
 constexpr int kRingBytes = 224 * 1024;
@@ -82,7 +86,20 @@ struct Params {
   int m_split;           // KGROUP: M tiles >= m_split read A1 and write out1
   int b_group_rows;      // expert stride in the rows of B's 2-D view
   int stages;            // ring depth
-  int stage_bytes;       // A tile + B tile, a multiple of 1024
+  int stage_bytes;       // stage stride in the ring, a multiple of 1024
+  int tx_bytes;          // bytes the producer's copies deliver per stage
+  int kstep;             // K elements per stage: 64 bf16 or 128 fp8 (128 bytes either way)
+  int acc_cols;          // TMEM columns per accumulator (256, or 128 for MXFP8 tiles)
+  // MXFP8 operands: scales in the sf_offset layout, sf_k* = K / 128 atoms per row block
+  const uint8_t* sfa0;
+  const uint8_t* sfa1;
+  const uint8_t* sfb0;
+  const uint8_t* sfb1;
+  int sf_ka, sf_kb;
+  void* out3;
+  uint8_t* osf0;         // scales of quantised outputs (sf_offset layout, osf_kb blocks/row)
+  uint8_t* osf1;
+  int osf_kb;
   void* out0;
   void* out1;
   void* out2;
@@ -136,10 +153,56 @@ MOE_DEV TileInfo decode_tile(const Params& p, const int32_t* off, int t) {
 MOE_DEV float silu_f(float h) { return h / (1.0f + __expf(-h)); }
 
 // ------------------------------------------------------------------ roles
+// One stage's TMA loads (and, for MXFP8, the stage's scale atoms).
+template <bool MX>
+MOE_DEV void stage_loads(const Params& p, const TileInfo& ti, int ks, uint8_t* sa, uint64_t* fb,
+                         const CUtensorMap* tA0, const CUtensorMap* tA1, const CUtensorMap* tB0,
+                         const CUtensorMap* tB1) {
+  uint8_t* sb = sa + kABytes;
+  if (p.mode == MODE_KGROUP) {
+    const bool hi = ti.m_tile >= p.m_split;
+    const CUtensorMap* ma = hi ? tA1 : tA0;
+    const int mcol = (ti.m_tile - (hi ? p.m_split : 0)) * kTileM;
+    const int krow = ti.k0row + ks * kBK;
+    tma_load_2d(sa, ma, fb, mcol, krow);
+    tma_load_2d(sa + kABytes / 2, ma, fb, mcol + 64, krow);
+    for (int i = 0; i < p.BN / 64; ++i)
+      tma_load_2d(sb + i * 8192, tB0, fb, ti.n_tile * p.BN + 64 * i, krow);
+    return;
+  }
+  const bool src1 = ks >= p.k_split;
+  const int kk = (src1 ? ks - p.k_split : ks) * p.kstep;
+  const CUtensorMap* mb = src1 ? tB1 : tB0;
+  tma_load_2d(sa, src1 ? tA1 : tA0, fb, kk, ti.m_tile * kTileM);
+  if constexpr (MX) {
+    // the stage's 128x4 A scales and BNx4 B scales: 512-byte atoms
+    uint8_t* sf = sb + p.BN * 128;
+    const int brow = ti.e * p.b_group_rows + ti.n_tile * p.BN;
+    bulk_load(sf, (src1 ? p.sfa1 : p.sfa0) + ((size_t)ti.m_tile * p.sf_ka + kk / 128) * 512, 512,
+              fb);
+    for (int i = 0; i < p.BN / 128; ++i)
+      bulk_load(sf + 512 * (1 + i),
+                (src1 ? p.sfb1 : p.sfb0) + ((size_t)(brow / 128 + i) * p.sf_kb + kk / 128) * 512,
+                512, fb);
+  }
+  if (p.b_mn) {
+    const int krow = ti.e * p.b_group_rows + kk;
+    for (int i = 0; i < p.BN / 64; ++i)
+      tma_load_2d(sb + i * 8192, mb, fb, ti.n_tile * p.BN + 64 * i, krow);
+  } else if (p.b_dual) {
+    const int row = ti.e * p.b_group_rows + ti.n_tile * 128;
+    tma_load_2d(sb, tB0, fb, kk, row);
+    tma_load_2d(sb + kBBytesMax / 2, tB1, fb, kk, row);
+  } else {
+    tma_load_2d(sb, mb, fb, kk, ti.e * p.b_group_rows + ti.n_tile * p.BN);
+  }
+}
+
+template <bool MX>
 MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap* tA0,
                       const CUtensorMap* tA1, const CUtensorMap* tB0, const CUtensorMap* tB1) {
   const int nt = total_tiles(p, s.tile_off);
-  const uint32_t bytes = (uint32_t)p.stage_bytes;
+  const uint32_t bytes = (uint32_t)p.tx_bytes;
   int stage = 0;
   uint32_t phase = 0;
   long issued = 0;
@@ -150,35 +213,9 @@ MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap*
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
       uint64_t* fb = &s.full[stage];
       uint8_t* sa = ring + stage * p.stage_bytes;
-      uint8_t* sb = sa + kABytes;
       mbar_arrive_expect_tx(fb, bytes);
       ++issued;
-      if (p.mode == MODE_KGROUP) {
-        const bool hi = ti.m_tile >= p.m_split;
-        const CUtensorMap* ma = hi ? tA1 : tA0;
-        const int mcol = (ti.m_tile - (hi ? p.m_split : 0)) * kTileM;
-        const int krow = ti.k0row + ks * kBK;
-        tma_load_2d(sa, ma, fb, mcol, krow);
-        tma_load_2d(sa + kABytes / 2, ma, fb, mcol + 64, krow);
-        for (int i = 0; i < p.BN / 64; ++i)
-          tma_load_2d(sb + i * 8192, tB0, fb, ti.n_tile * p.BN + 64 * i, krow);
-      } else {
-        const bool src1 = ks >= p.k_split;
-        const int kk = (src1 ? ks - p.k_split : ks) * kBK;
-        tma_load_2d(sa, src1 ? tA1 : tA0, fb, kk, ti.m_tile * kTileM);
-        if (p.b_mn) {
-          const int krow = ti.e * p.b_group_rows + kk;
-          const CUtensorMap* mb = src1 ? tB1 : tB0;
-          for (int i = 0; i < p.BN / 64; ++i)
-            tma_load_2d(sb + i * 8192, mb, fb, ti.n_tile * p.BN + 64 * i, krow);
-        } else if (p.b_dual) {
-          const int row = ti.e * p.b_group_rows + ti.n_tile * 128;
-          tma_load_2d(sb, tB0, fb, kk, row);
-          tma_load_2d(sb + kBBytesMax / 2, tB1, fb, kk, row);
-        } else {
-          tma_load_2d(sb, src1 ? tB1 : tB0, fb, kk, ti.e * p.b_group_rows + ti.n_tile * p.BN);
-        }
-      }
+      stage_loads<MX>(p, ti, ks, sa, fb, tA0, tA1, tB0, tB1);
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
@@ -198,6 +235,7 @@ MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap*
   }
 }
 
+template <bool MX>
 MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_base) {
   const int nt = total_tiles(p, s.tile_off);
   const int n_mma = p.b_dual ? 256 : p.BN;
@@ -212,19 +250,36 @@ MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_ba
     const uint32_t use = (uint32_t)(it >> 1);
     if (!mbar_wait(&s.tempty[acc], (use & 1u) ^ 1u, &s.abort, p.err)) { ok = false; break; }
     tc_fence_after();
-    const uint32_t tmem_d = tmem_base + (uint32_t)acc * 256u;
+    const uint32_t tmem_d = tmem_base + (uint32_t)(acc * p.acc_cols);
     for (int ks = 0; ks < ti.ks; ++ks) {
       if (!mbar_wait(&s.full[stage], phase, &s.abort, p.err)) { ok = false; break; }
       tc_fence_after();
       const uint32_t a_addr = smem_u32(ring + stage * p.stage_bytes);
       const uint32_t b_addr = a_addr + kABytes;
+      if constexpr (MX) {
+        // scales of this stage -> tensor memory (columns after both accumulators)
+        const uint32_t sf_smem = b_addr + (uint32_t)p.BN * 128u;
+        const uint32_t t_sfa = tmem_base + 2u * (uint32_t)p.acc_cols + (uint32_t)stage * 8u;
+        const uint32_t t_sfb = t_sfa + 4u;
+        tc_cp_32x128b_x4(t_sfa, smem_desc_noswz(sf_smem));
+        for (int i = 0; i < p.BN / 128; ++i)
+          tc_cp_32x128b_x4(t_sfb + 4u * i, smem_desc_noswz(sf_smem + 512u * (1 + i)));
 #pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
-                                   : smem_desc_sw128(a_addr + k * 32, 16, 1024);
-        const uint64_t bd = p.b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                   : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-        tc_mma_bf16(tmem_d, ad, bd, idesc, (ks | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < 4; ++k) {   // 4 x (K = 32 fp8): 32 bytes per step, like bf16
+          const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          tc_mma_mxf8(tmem_d, ad, bd, idesc_mxf8(kTileM, n_mma, k), t_sfa, t_sfb,
+                      (ks | k) != 0 ? 1u : 0u);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = p.b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          tc_mma_bf16(tmem_d, ad, bd, idesc, (ks | k) != 0 ? 1u : 0u);
+        }
       }
       tc_commit(&s.empty[stage]);
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
@@ -256,6 +311,26 @@ MOE_DEV void store_bf16x32(__nv_bfloat16* dst, const uint32_t* v) {
                        pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
   }
+}
+
+// One MXFP8 block held by one thread: 32 values -> 32 E4M3 codes + 1 scale byte.
+MOE_DEV void mx_store32(const uint32_t* bits, uint8_t* codes, uint8_t* sf_byte) {
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(bits[i]);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const int sx = mx_scale_exp(amax);
+  const float inv = ldexpf(1.0f, -sx);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= inv;
+  uint4* c4 = reinterpret_cast<uint4*>(codes);
+  const uint2 q0 = e4m3x8(v), q1 = e4m3x8(v + 8), q2 = e4m3x8(v + 16), q3 = e4m3x8(v + 24);
+  c4[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  c4[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+  *sf_byte = (uint8_t)(sx + 127);
 }
 
 // Columns [c0, c1) of the tile, 32 at a time.
@@ -337,6 +412,65 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
       store_bf16x32(dH + c, gh);
       store_bf16x32(dU + c, gu);
     }
+  } else if (p.epi == EPI_SWIGLU_FWD_MX) {
+    // accumulator columns [0, 64) are H, [64, 128) are U for f columns n_tile*64 + [0, 64)
+    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+    const int fc = ti.n_tile * 64;
+    const int64_t off = row * p.ldo + fc;
+    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) + off;
+    __nv_bfloat16* U = static_cast<__nv_bfloat16*>(p.out1) + off;
+    uint8_t* Aq = static_cast<uint8_t*>(p.out2) + off;
+    uint32_t w[32];
+    for (int c = c0; c < c1; c += 32) {
+      tmem_ld32x2(tb + c, tb + 64 + c, v, w);
+      uint32_t a[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        a[i] = __float_as_uint(silu_f(__uint_as_float(v[i])) * __uint_as_float(w[i]));
+      store_bf16x32(H + c, v);
+      store_bf16x32(U + c, w);
+      mx_store32(a, Aq + c, p.osf0 + sf_offset(row, (fc + c) / 32, p.osf_kb));
+    }
+  } else if (p.epi == EPI_SWIGLU_BWD_MX) {
+    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+    const int fc = ti.n_tile * p.BN;
+    const int64_t off = row * p.ldo + fc;
+    const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
+    const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
+    __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(p.out0) + off;
+    __nv_bfloat16* dU = static_cast<__nv_bfloat16*>(p.out1) + off;
+    uint8_t* dHq = static_cast<uint8_t*>(p.out2) + off;
+    uint8_t* dUq = static_cast<uint8_t*>(p.out3) + off;
+    for (int c = c0; c < c1; c += 32) {
+      uint4 hc[4], uc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        hc[q] = H[c / 8 + q];
+        uc[q] = U[c / 8 + q];
+      }
+      tmem_ld32(tb + c, v);
+      uint32_t gh[32], gu[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float h[8], u[8];
+        unpack8(hc[q], h);
+        unpack8(uc[q], u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float da = __uint_as_float(v[8 * q + i]);
+          const float sg = 1.0f / (1.0f + __expf(-h[i]));
+          const float si = h[i] * sg;
+          const float ds = sg * (1.0f + h[i] * (1.0f - sg));
+          gh[8 * q + i] = __float_as_uint(da * u[i] * ds);
+          gu[8 * q + i] = __float_as_uint(da * si);
+        }
+      }
+      store_bf16x32(dH + c, gh);
+      store_bf16x32(dU + c, gu);
+      const size_t so = sf_offset(row, (fc + c) / 32, p.osf_kb);
+      mx_store32(gh, dHq + c, p.osf0 + so);
+      mx_store32(gu, dUq + c, p.osf1 + so);
+    }
   } else if (p.epi == EPI_F32) {
     const bool hi = ti.m_tile >= p.m_split;
     float* out = static_cast<float*>(hi ? p.out1 : p.out0) + (int64_t)ti.e * p.out_group_stride +
@@ -377,7 +511,7 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   const int half = (warp - 2) >> 2;        // which half of the tile's columns
   const int r = quarter * 32 + lane;
   // column range of this warp: half of the tile (of the H half for SwiGLU)
-  const int width = (p.epi == EPI_SWIGLU_FWD) ? 128 : p.BN;
+  const int width = (p.epi == EPI_SWIGLU_FWD) ? 128 : (p.epi == EPI_SWIGLU_FWD_MX ? 64 : p.BN);
   int c0, c1;
   if (width >= 64) {
     c0 = half * (width / 2);
@@ -393,13 +527,14 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     const uint32_t use = (uint32_t)(it >> 1);
     if (!mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err)) break;
     tc_fence_after();
-    const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * 256u;
+    const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
     epilogue_tile(p, ti, r, tb, c0, c1);
     tc_fence_before();
     mbar_arrive(&s.tempty[acc]);
   }
 }
 
+template <bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                         const __grid_constant__ CUtensorMap tA1,
@@ -441,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = s.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer(p, s, ring, &tA0, &tA1, &tB0, &tB1);
+    if (lane == 0) producer<MX>(p, s, ring, &tA0, &tA1, &tB0, &tB1);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(p, s, ring, tmem_base);
+    if (lane == 0) mma_issuer<MX>(p, s, ring, tmem_base);
   } else {
     epilogue(p, s, tmem_base, warp, lane);
   }
@@ -476,12 +611,13 @@ bool get_encoder() {
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
 // box of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool u8 = false) {
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * (u8 ? 1 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  return g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -491,8 +627,11 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 cudaError_t gemm_init_attributes() {
   if (!get_encoder()) return cudaErrorInitializationError;
-  return cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
@@ -509,6 +648,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   p.err = g.err;
   p.k_split = 1 << 30;
   p.m_split = 1 << 30;
+  p.kstep = kBK;
+  p.acc_cols = 256;
+  bool mx = false;
   int64_t max_tiles = 0;
   switch (g.op) {
     case OP_FWD1_SWIGLU:
@@ -575,17 +717,72 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       max_tiles = p.m_tiles;
       break;
     }
+    // ---- MXFP8: 128x128 tiles, K steps of 128 fp8 (128 bytes), scales per stage
+    case OP_MX_FWD1_SWIGLU:
+      mx = true; p.mode = MODE_MGROUP; p.epi = EPI_SWIGLU_FWD_MX; p.BN = 128;
+      p.n_tiles = 2 * f / 128; p.k_steps = d / 128; p.b_group_rows = 2 * f;
+      ok = make_map(&A0, g.a0, d, rows, 128, 128, true) &&
+           make_map(&B0, g.w0, d, (uint64_t)E * 2 * f, 128, 128, true);
+      A1 = A0; B1 = B0;
+      p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = d / 128;
+      p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.osf0 = g.osf0; p.osf_kb = f / 32;
+      p.ldo = f;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_MX_FWD2:
+      mx = true; p.mode = MODE_MGROUP; p.epi = EPI_BF16; p.BN = 128;
+      p.n_tiles = d / 128; p.k_steps = f / 128; p.b_group_rows = d;
+      ok = make_map(&A0, g.a0, f, rows, 128, 128, true) &&
+           make_map(&B0, g.w0, f, (uint64_t)E * d, 128, 128, true);
+      A1 = A0; B1 = B0;
+      p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = f / 128;
+      p.out0 = g.out0; p.ldo = d;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_MX_DGRAD2_SWIGLU:
+      mx = true; p.mode = MODE_MGROUP; p.epi = EPI_SWIGLU_BWD_MX; p.BN = 128;
+      p.n_tiles = f / 128; p.k_steps = d / 128; p.b_group_rows = f;
+      ok = make_map(&A0, g.a0, d, rows, 128, 128, true) &&
+           make_map(&B0, g.w0, d, (uint64_t)E * f, 128, 128, true);
+      A1 = A0; B1 = B0;
+      p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = d / 128;
+      p.aux0 = g.aux0; p.aux1 = g.aux1;
+      p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.out3 = g.out3;
+      p.osf0 = g.osf0; p.osf1 = g.osf1; p.osf_kb = f / 32; p.ldo = f;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
+    case OP_MX_DGRAD1:
+      mx = true; p.mode = MODE_MGROUP; p.epi = EPI_BF16; p.BN = 128;
+      p.n_tiles = d / 128; p.k_steps = 2 * f / 128; p.k_split = f / 128; p.b_group_rows = d;
+      ok = make_map(&A0, g.a0, f, rows, 128, 128, true) && make_map(&A1, g.a1, f, rows, 128, 128, true) &&
+           make_map(&B0, g.w0, f, (uint64_t)E * d, 128, 128, true) &&
+           make_map(&B1, g.w1, f, (uint64_t)E * d, 128, 128, true);
+      p.sfa0 = g.sfa0; p.sfa1 = g.sfa1; p.sfb0 = g.sfb0; p.sfb1 = g.sfb1; p.sf_ka = p.sf_kb = f / 128;
+      p.out0 = g.out0; p.ldo = d;
+      max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
+      break;
     default:
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
-  p.stage_bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
+  if (mx) {
+    p.kstep = 128;
+    p.acc_cols = 128;
+    p.tx_bytes = kABytes + p.BN * 128 + 512 * (1 + p.BN / 128);
+    p.stage_bytes = (p.tx_bytes + 1023) & ~1023;
+  } else {
+    p.tx_bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
+    p.stage_bytes = p.tx_bytes;
+  }
   p.stages = kRingBytes / p.stage_bytes;
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2 || p.stage_bytes % 1024 != 0) return cudaErrorInvalidValue;
   int grid = (int)(max_tiles < di->sm_count ? max_tiles : di->sm_count);
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);
+  if (mx)
+    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);
+  else
+    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,11 @@ enum GemmOp {
   OP_WGRAD2 = 4,
   OP_WGRAD1 = 5,
   OP_ROUTER = 6,
+  // MXFP8 (E4M3 operands with E8M0 block scales), K-major operands only
+  OP_MX_FWD1_SWIGLU = 7,   // A = Xd_q; B = [W_gate|W_up] cache, 64-row groups alternating
+  OP_MX_FWD2 = 8,          // A = A_q;  B = W_down cache
+  OP_MX_DGRAD2_SWIGLU = 9, // A = dY_q; B = W_down^T cache
+  OP_MX_DGRAD1 = 10,       // A0/A1 = dH_q/dU_q; B0/B1 = W_gate^T / W_up^T caches
 };
 
 struct GemmLaunch {
@@ -76,9 +81,28 @@ struct GemmLaunch {
   void* out0;
   void* out1;
   void* out2;
+  void* out3;
+  // MXFP8: operand scales (sf_offset layout) and scales of quantised outputs
+  const uint8_t* sfa0;
+  const uint8_t* sfa1;
+  const uint8_t* sfb0;
+  const uint8_t* sfb1;
+  uint8_t* osf0;
+  uint8_t* osf1;
   int32_t* err;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t s);
+
+// ---------------------------------------------------------------- MXFP8
+// block_axis 1 with group > 0 interleaves: output row (r/group)*2*group + offset + r%group
+cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis, const void* src,
+                                  uint8_t* q, uint8_t* sf, cudaStream_t s, int group = 0,
+                                  int offset = 0);
+cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
+                                  const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                                  int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s);
+cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t rows, int K,
+                                    void* out, cudaStream_t s);
 cudaError_t gemm_init_attributes();
 
 }  // namespace moe

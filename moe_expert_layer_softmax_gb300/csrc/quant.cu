@@ -1,0 +1,207 @@
+// MXFP8 kernels (sm_103a): E4M3 values with one E8M0 scale per 32 values along
+// the contraction axis ("Supercharging Olmo-core for Efficient and Scalable MoE
+// Training", Abstract and Section 24 Evidence 10: MXFP8 with shared block
+// scales, 33/32 byte per value; Section 24.3: the quantiser emits a layout the
+// GEMM consumes without a conversion pass).
+//   quantize_rows   K along the row: codes keep the orientation
+//   quantize_cols   K along the column: codes are written transposed (K-major),
+//                   the second weight cache of the data-gradient GEMMs
+//   dispatch_mxfp8  x[t] quantised once, then written to its k expert rows
+//   dequantize      codes + scales -> bf16 (the global dequantisation that
+//                   feeds the BF16 weight-gradient GEMMs, Section 24 Evidence 7)
+// Scales are stored at sf_offset() (common.cuh), the layout the GEMM copies
+// into tensor memory.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kQThreads = 256;
+
+// One thread per 32-value block of a [rows, cols] bf16 matrix (K = cols).
+// Output row of input row r: r, or with `group` > 0 (interleaving two matrices
+// into one of 2*rows rows): (r / group) * 2 * group + offset + r % group.
+__global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
+    const uint4* __restrict__ src, int64_t nblocks, int rows, int cols, int group, int offset,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x;
+  if (i >= nblocks) return;
+  const int kb = cols / 32;
+  const int64_t per_mat = (int64_t)rows * kb;
+  const int64_t mat = i / per_mat;
+  const int64_t rem = i - mat * per_mat;
+  const int64_t r = rem / kb;
+  const int b = (int)(rem - r * kb);
+  const int64_t out_rows = group > 0 ? 2 * (int64_t)rows : rows;
+  const int64_t ro = group > 0 ? (r / group) * 2 * group + offset + r % group : r;
+  float v[32];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) unpack8(__ldg(src + i * 4 + u), v + 8 * u);
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const int s = mx_scale_exp(amax);
+  const float inv = ldexpf(1.0f, -s);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] *= inv;
+  uint2* out = reinterpret_cast<uint2*>(q + ((size_t)mat * out_rows + ro) * cols + (size_t)b * 32);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) out[u] = e4m3x8(v + 8 * u);
+  sf[(size_t)mat * out_rows * kb + sf_offset(ro, b, kb)] = (uint8_t)(s + 127);
+}
+
+// K along the column: src [K=rows, N=cols] bf16 -> q [N, K] (K-major) with
+// scales of the [N, K] operand.  Tile: 128 K x 64 N per block.
+constexpr int kTK = 128, kTN = 64;
+__global__ void __launch_bounds__(kQThreads) quantize_cols_kernel(
+    const __nv_bfloat16* __restrict__ src, int K, int N, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sf) {
+  __shared__ __nv_bfloat16 tile[kTK][kTN];
+  const int mat = blockIdx.z;
+  const int k0 = blockIdx.y * kTK;
+  const int n0 = blockIdx.x * kTN;
+  const __nv_bfloat16* s = src + (size_t)mat * K * N;
+  // 128 rows x 128 bytes: 1024 16-byte vectors, 4 per thread
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int idx = threadIdx.x + u * kQThreads;
+    const int row = idx >> 3, col = (idx & 7) * 8;
+    *reinterpret_cast<uint4*>(&tile[row][col]) =
+        __ldg(reinterpret_cast<const uint4*>(s + (size_t)(k0 + row) * N + n0 + col));
+  }
+  __syncthreads();
+  const int n = threadIdx.x & 63;
+  const int kb = threadIdx.x >> 6;          // 4 blocks of 32 along K
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] = __bfloat162float(tile[kb * 32 + j][n]);
+    amax = fmaxf(amax, fabsf(v[j]));
+  }
+  const int e = mx_scale_exp(amax);
+  const float inv = ldexpf(1.0f, -e);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] *= inv;
+  const size_t row_out = (size_t)n0 + n;
+  uint2* out = reinterpret_cast<uint2*>(q + (size_t)mat * N * K + row_out * K + k0 + kb * 32);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) out[u] = e4m3x8(v + 8 * u);
+  sf[(size_t)mat * N * (K / 32) + sf_offset((int64_t)row_out, (k0 / 32) + kb, K / 32)] =
+      (uint8_t)(e + 127);
+}
+
+// Warp per token: a lane holds 8 values of a 256-column chunk; 4 lanes form a
+// 32-value block.  Codes and scales go to all k expert rows; padding rows get
+// zero codes and scale byte 127 (2^0).
+__global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ slot_of_route,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
+    int E, int k, int token_blocks, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int warps = kQThreads / 32;
+  const int nv = d / 8;
+  const int kb = d / 32;
+  if (blockIdx.x >= token_blocks) {
+    const int p = (blockIdx.x - token_blocks) * warps + (threadIdx.x >> 5);
+    if (p >= E * kTileM) return;
+    const int e = p / kTileM;
+    const int row = tile_offsets[e] * kTileM + counts[e] + (p % kTileM);
+    if (row >= tile_offsets[e + 1] * kTileM) return;
+    uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * d);
+    for (int c = lane; c < nv; c += 32) dst[c] = make_uint2(0, 0);
+    for (int b = lane; b < kb; b += 32) xs[sf_offset(row, b, kb)] = 127;
+    return;
+  }
+  const int t = blockIdx.x * warps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
+  for (int c0 = 0; c0 < nv; c0 += 32) {      // warp-uniform
+    const int c = c0 + lane;
+    const bool ok = c < nv;
+    float v[8];
+    if (ok) unpack8(__ldg(x + (size_t)t * nv + c), v);
+    else
+      for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int s = mx_scale_exp(amax);
+    const float inv = ldexpf(1.0f, -s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= inv;
+    const uint2 codes = e4m3x8(v);
+    for (int j = 0; j < k; ++j) {
+      const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+      if (ok) {
+        reinterpret_cast<uint2*>(xq + (size_t)slot * d)[c] = codes;
+        if ((lane & 3) == 0) xs[sf_offset(slot, c / 4, kb)] = (uint8_t)(s + 127);
+      }
+    }
+  }
+}
+
+// One thread per 16 codes of a [rows, K] MXFP8 operand -> bf16 [rows, K].
+__global__ void __launch_bounds__(kQThreads) dequantize_kernel(
+    const uint4* __restrict__ q, const uint8_t* __restrict__ sf, int64_t nvec, int K,
+    uint4* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x;
+  if (i >= nvec) return;
+  const int per_row = K / 16;
+  const int64_t r = i / per_row;
+  const int c16 = (int)(i - r * per_row);
+  const int b = c16 / 2;
+  const float scale = ldexpf(1.0f, (int)sf[sf_offset(r, b, K / 32)] - 127);
+  const uint4 v = __ldg(q + i);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[16];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    e4m3x2_to_f32(w[u] & 0xFFFFu, f[4 * u + 0], f[4 * u + 1]);
+    e4m3x2_to_f32(w[u] >> 16, f[4 * u + 2], f[4 * u + 3]);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) f[j] *= scale;
+  out[2 * i] = pack8(f);
+  out[2 * i + 1] = pack8(f + 8);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis, const void* src,
+                                  uint8_t* q, uint8_t* sf, cudaStream_t s, int group, int offset) {
+  if (block_axis == 1) {
+    const int64_t n = (int64_t)batch * rows * (cols / 32);
+    quantize_rows_kernel<<<(unsigned)((n + kQThreads - 1) / kQThreads), kQThreads, 0, s>>>(
+        static_cast<const uint4*>(src), n, rows, cols, group, offset, q, sf);
+  } else {
+    dim3 grid((unsigned)(cols / kTN), (unsigned)(rows / kTK), (unsigned)batch);
+    quantize_cols_kernel<<<grid, kQThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows,
+                                                    cols, q, sf);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
+                                  const int32_t* counts, const int32_t* tile_offsets, int T, int d,
+                                  int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s) {
+  const int warps = kQThreads / 32;
+  const int tb = (T + warps - 1) / warps;
+  const int pb = (E * kTileM + warps - 1) / warps;
+  dispatch_mxfp8_kernel<<<tb + pb, kQThreads, 0, s>>>(static_cast<const uint4*>(x), slot_of_route,
+                                                      counts, tile_offsets, T, d, E, k, tb, xq, xs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t rows, int K,
+                                    void* out, cudaStream_t s) {
+  const int64_t nvec = rows * (K / 16);
+  dequantize_kernel<<<(unsigned)((nvec + kQThreads - 1) / kQThreads), kQThreads, 0, s>>>(
+      reinterpret_cast<const uint4*>(q), sf, nvec, K, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

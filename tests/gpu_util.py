@@ -34,3 +34,25 @@ def near_tie_tokens(logits, k, gap):
     if L.shape[1] <= k:
         return np.zeros(L.shape[0], dtype=bool)
     return (L[:, k - 1] - L[:, k]) < gap
+
+
+def sf_index(rows, kblocks):
+    """Byte offset of the scale of (row r, K-block b) in the MOE_SF layout that
+    include/moe.h documents (a pure index permutation)."""
+    r = np.arange(rows)[:, None]
+    b = np.arange(kblocks)[None, :]
+    return (((r // 128) * (kblocks // 4) + b // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4
+            + (b % 4))
+
+
+def sf_pack(scales):
+    """Row-major scales [rows, K/32] -> flat MOE_SF buffer."""
+    rows, kb = scales.shape
+    buf = np.zeros(rows * kb, dtype=np.uint8)
+    buf[sf_index(rows, kb)] = scales
+    return buf
+
+
+def sf_unpack(buf, rows, kblocks):
+    """Flat MOE_SF buffer -> row-major scales [rows, K/32]."""
+    return np.asarray(buf).reshape(-1)[: rows * kblocks][sf_index(rows, kblocks)]

@@ -1,0 +1,321 @@
+"""MXFP8 parity (GPU): the quantiser is bit-exact against the oracle (codes and
+E8M0 scales, both orientations, the interleaved and transposed weight caches),
+dequantisation is exact, the MXFP8 dispatch writes the oracle's codes, every
+MXFP8 GEMM stage and the whole MXFP8 layer are within max-abs-rel 6e-2 of the
+MXFP8 oracle, and the full-size MXFP8 workload is checked on sampled outputs."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from synth import CONFIGS, bf16_bits_from_f32, make_inputs
+from gpu_util import (bf16_bits_of, f64, max_abs_rel, sf_index, sf_pack, sf_unpack,
+                      to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+TOL = 6e-2
+
+
+def u8(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to(dev)
+
+
+def bf(a, dev):
+    return to_dev_bf16(bf16_bits_from_f32(np.asarray(a, dtype=np.float32)), dev)
+
+
+def q_rows(a):
+    """oracle quantisation along the last axis -> (codes, row-major scales)"""
+    return O.quantize_mxfp8(a)
+
+
+def test_quantize_rows_bit_exact(moe_gpu):
+    m, dev = moe_gpu
+    rng = np.random.default_rng(0)
+    vals = rng.standard_normal((2, 256, 384)).astype(np.float32) * 3
+    vals[0, 0] = 0.0                                              # all-zero blocks
+    vals[0, 1] = -0.0
+    vals[0, 2, :32] = O.E4M3_VALUES[rng.integers(0, 126, 32)] * 8.0   # on the grid
+    vals[0, 2, 0] = 448.0 * 8.0
+    vals[0, 3] = rng.standard_normal(384) * 1e-30                 # tiny
+    vals[0, 4] = rng.standard_normal(384) * 1e30                  # huge
+    vals[1, 5, ::7] = -3.0e38
+    bits = bf16_bits_from_f32(vals)
+    x = to_dev_bf16(bits, dev)
+    q = torch.empty(2, 256, 384, dtype=torch.uint8, device=dev)
+    s = torch.empty(2 * 256 * 12, dtype=torch.uint8, device=dev)
+    m.quantize_mxfp8(2, 256, 384, 1, x, q, s)
+    torch.cuda.synchronize()
+    codes, scales = q_rows(O.as_f64(bits))
+    np.testing.assert_array_equal(q.cpu().numpy(), codes)
+    sb = s.cpu().numpy().reshape(2, -1)
+    for i in range(2):
+        np.testing.assert_array_equal(sf_unpack(sb[i], 256, 12), scales[i])
+
+
+def test_quantize_cols_writes_the_transpose(moe_gpu):
+    m, dev = moe_gpu
+    rng = np.random.default_rng(1)
+    vals = (rng.standard_normal((3, 256, 384)) * np.exp(rng.standard_normal((3, 256, 1)))).astype(np.float32)
+    bits = bf16_bits_from_f32(vals)
+    q = torch.empty(3, 384, 256, dtype=torch.uint8, device=dev)
+    s = torch.empty(3 * 384 * 8, dtype=torch.uint8, device=dev)
+    m.quantize_mxfp8(3, 256, 384, 0, to_dev_bf16(bits, dev), q, s)
+    torch.cuda.synchronize()
+    sb = s.cpu().numpy().reshape(3, -1)
+    for i in range(3):
+        codes, scales = q_rows(O.as_f64(bits[i]).T)
+        np.testing.assert_array_equal(q[i].cpu().numpy(), codes)
+        np.testing.assert_array_equal(sf_unpack(sb[i], 384, 8), scales)
+
+
+def oracle_caches(inp):
+    """The five MXFP8 weight caches, built from the oracle's quantiser."""
+    E, f, d = inp["E"], inp["f"], inp["d"]
+    wg, wu, wd = (O.as_f64(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+    gu_q = np.zeros((E, 2 * f, d), np.uint8)
+    gu_s = np.zeros((E, 2 * f, d // 32), np.uint8)
+    for e in range(E):
+        cg, sg = q_rows(wg[e])
+        cu, su = q_rows(wu[e])
+        for j in range(f // 64):
+            gu_q[e, 128 * j:128 * j + 64] = cg[64 * j:64 * j + 64]
+            gu_s[e, 128 * j:128 * j + 64] = sg[64 * j:64 * j + 64]
+            gu_q[e, 128 * j + 64:128 * j + 128] = cu[64 * j:64 * j + 64]
+            gu_s[e, 128 * j + 64:128 * j + 128] = su[64 * j:64 * j + 64]
+    out = {"gu": (gu_q, gu_s)}
+    out["down"] = tuple(np.stack(z) for z in zip(*[q_rows(wd[e]) for e in range(E)]))
+    out["downT"] = tuple(np.stack(z) for z in zip(*[q_rows(wd[e].T) for e in range(E)]))
+    out["gateT"] = tuple(np.stack(z) for z in zip(*[q_rows(wg[e].T) for e in range(E)]))
+    out["upT"] = tuple(np.stack(z) for z in zip(*[q_rows(wu[e].T) for e in range(E)]))
+    return out
+
+
+def pack_cache(c, dev):
+    res = {}
+    for name, (q, s) in c.items():
+        E, rows, kb = s.shape
+        res[name + "_q"] = u8(q, dev)
+        res[name + "_s"] = u8(np.concatenate([sf_pack(s[e]) for e in range(E)]), dev)
+    return res
+
+
+def test_weight_caches_bit_exact(moe_gpu):
+    m, dev = moe_gpu
+    inp = make_inputs(T=8, d=384, E=3, k=2, f=256, seed=21, with_grad=False)
+    s = m.shape(8, 384, 3, 2, 256, prec=m.MXFP8)
+    buf = m.allocate(s, with_grads=False)
+    m.build_mx_weights(s, *(to_dev_bf16(inp[n], dev) for n in ("w_gate", "w_up", "w_down")),
+                       buf.mx_weights)
+    torch.cuda.synchronize()
+    ref = oracle_caches(inp)
+    for name, (q, sc) in ref.items():
+        got_q = buf.mx_weights[name + "_q"].cpu().numpy()
+        np.testing.assert_array_equal(got_q, q, err_msg=name)
+        E, rows, kb = sc.shape
+        gs = buf.mx_weights[name + "_s"].cpu().numpy().reshape(E, -1)
+        for e in range(E):
+            np.testing.assert_array_equal(sf_unpack(gs[e], rows, kb), sc[e], err_msg=name)
+
+
+def test_dequantize_is_exact(moe_gpu):
+    m, dev = moe_gpu
+    rng = np.random.default_rng(2)
+    a = rng.standard_normal((256, 512)) * np.exp(rng.standard_normal((256, 1)) * 3)
+    codes, scales = q_rows(a)
+    out = torch.empty(256, 512, dtype=torch.bfloat16, device=dev)
+    m.dequantize_mxfp8(256, 512, u8(codes, dev), u8(sf_pack(scales), dev), out)
+    np.testing.assert_array_equal(f64(out), O.dequantize_mxfp8(codes, scales))
+
+
+# ------------------------------------------------------------------ stages
+SHAPES = [(300, 256, 6, 2, 256), (1000, 512, 8, 8, 384)]
+
+
+@pytest.fixture(scope="module", params=SHAPES, ids=lambda v: "x".join(map(str, v)))
+def mcase(request, moe_gpu):
+    m, dev = moe_gpu
+    T, d, E, k, f = request.param
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=T + 7)
+    inp["bias"][:, 2] -= 100.0                  # one empty expert
+    L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
+    fwd = O.layer_forward_mxfp8(inp["x"], None, None, inp["w_gate"], inp["w_up"], inp["w_down"],
+                                k, logits=L32)
+    bwd = O.layer_backward_mxfp8(fwd, inp["d_out"], inp["x"], None, inp["w_gate"], inp["w_up"],
+                                 inp["w_down"])
+    s = m.shape(T, d, E, k, f, prec=m.MXFP8)
+    n = m.rows_max(s)
+    used = int(fwd["row_offsets"][-1])
+
+    def rows_q(a, width):              # oracle rows -> quantised [n, width] codes + packed scales
+        full = np.zeros((n, width))
+        full[:used] = a
+        c, sc = q_rows(full)
+        return u8(c, dev), u8(sf_pack(sc), dev)
+
+    def rows_bf(a, width):
+        full = np.zeros((n, width))
+        full[:used] = a
+        return bf(full, dev)
+
+    return dict(m=m, dev=dev, T=T, d=d, E=E, k=k, f=f, s=s, n=n, used=used, inp=inp, L32=L32,
+                fwd=fwd, bwd=bwd, rows_q=rows_q, rows_bf=rows_bf,
+                ws=torch.zeros(m.workspace_size(s), dtype=torch.uint8, device=dev),
+                cache=pack_cache(oracle_caches(inp), dev),
+                tile_offsets=torch.from_numpy(fwd["tile_offsets"].astype(np.int32)).to(dev),
+                counts=torch.from_numpy(fwd["counts"].astype(np.int32)).to(dev),
+                slot=torch.from_numpy(fwd["slot_of_route"].astype(np.int32)).to(dev))
+
+
+def test_mx_dispatch_writes_the_oracle_codes(mcase):
+    c = mcase
+    m, dev, n, d = c["m"], c["dev"], c["n"], c["d"]
+    xq = torch.full((n, d), 0x55, dtype=torch.uint8, device=dev)
+    xs = torch.full((n * d // 32,), 0x66, dtype=torch.uint8, device=dev)
+    m.dispatch(c["s"], to_dev_bf16(c["inp"]["x"], dev), c["slot"], c["counts"], c["tile_offsets"],
+               xq, xs)
+    torch.cuda.synchronize()
+    codes, scales = q_rows(O.as_f64(c["inp"]["x"]))
+    used = c["used"]
+    ros = c["fwd"]["route_of_slot"]
+    want_q = np.zeros((used, d), np.uint8)
+    want_s = np.full((used, d // 32), 127, np.uint8)
+    real = ros >= 0
+    want_q[real] = codes[ros[real] // c["k"]]
+    want_s[real] = scales[ros[real] // c["k"]]
+    np.testing.assert_array_equal(xq.cpu().numpy()[:used], want_q)
+    np.testing.assert_array_equal(sf_unpack(xs.cpu().numpy(), n, d // 32)[:used], want_s)
+
+
+def test_mx_fwd1_swiglu(mcase):
+    c = mcase
+    m, dev, n, f = c["m"], c["dev"], c["n"], c["f"]
+    H, U = (torch.empty(n, f, dtype=torch.bfloat16, device=dev) for _ in range(2))
+    Aq = torch.empty(n, f, dtype=torch.uint8, device=dev)
+    As = torch.empty(n * f // 32, dtype=torch.uint8, device=dev)
+    xq, xs = c["rows_q"](c["fwd"]["Xd"], c["d"])
+    m.grouped_gemm(c["s"], m.GEMM_FWD1_SWIGLU, c["ws"], tile_offsets=c["tile_offsets"], a0=xq,
+                   sfa0=xs, w0=c["cache"]["gu_q"], sfb0=c["cache"]["gu_s"], out0=H, out1=U,
+                   out2=Aq, osf0=As)
+    u = c["used"]
+    assert m.read_error(c["ws"]) == 0
+    assert max_abs_rel(f64(H)[:u], c["fwd"]["H"]) <= TOL
+    assert max_abs_rel(f64(U)[:u], c["fwd"]["U"]) <= TOL
+    a_deq = O.dequantize_mxfp8(Aq.cpu().numpy(), sf_unpack(As.cpu().numpy(), n, f // 32))
+    assert max_abs_rel(a_deq[:u], c["fwd"]["Aq"]) <= TOL
+
+
+def test_mx_fwd2(mcase):
+    c = mcase
+    m, dev, n = c["m"], c["dev"], c["n"]
+    Y = torch.empty(n, c["d"], dtype=torch.bfloat16, device=dev)
+    aq, as_ = c["rows_q"](c["fwd"]["Aq"], c["f"])
+    m.grouped_gemm(c["s"], m.GEMM_FWD2, c["ws"], tile_offsets=c["tile_offsets"], a0=aq, sfa0=as_,
+                   w0=c["cache"]["down_q"], sfb0=c["cache"]["down_s"], out0=Y)
+    assert max_abs_rel(f64(Y)[: c["used"]], c["fwd"]["Y"]) <= TOL
+
+
+def test_mx_dgrad2_swiglu_bwd(mcase):
+    c = mcase
+    m, dev, n, f = c["m"], c["dev"], c["n"], c["f"]
+    dH, dU = (torch.empty(n, f, dtype=torch.bfloat16, device=dev) for _ in range(2))
+    dHq, dUq = (torch.empty(n, f, dtype=torch.uint8, device=dev) for _ in range(2))
+    dHs, dUs = (torch.empty(n * f // 32, dtype=torch.uint8, device=dev) for _ in range(2))
+    yq, ys = c["rows_q"](c["bwd"]["dY"], c["d"])
+    m.grouped_gemm(c["s"], m.GEMM_DGRAD2_SWIGLU, c["ws"], tile_offsets=c["tile_offsets"], a0=yq,
+                   sfa0=ys, w0=c["cache"]["downT_q"], sfb0=c["cache"]["downT_s"],
+                   aux0=c["rows_bf"](c["fwd"]["H"], f), aux1=c["rows_bf"](c["fwd"]["U"], f),
+                   out0=dH, out1=dU, out2=dHq, out3=dUq, osf0=dHs, osf1=dUs)
+    u = c["used"]
+    assert max_abs_rel(f64(dH)[:u], c["bwd"]["dH"]) <= TOL
+    assert max_abs_rel(f64(dU)[:u], c["bwd"]["dU"]) <= TOL
+    dq = O.dequantize_mxfp8(dHq.cpu().numpy(), sf_unpack(dHs.cpu().numpy(), n, f // 32))
+    assert max_abs_rel(dq[:u], c["bwd"]["dH"]) <= TOL
+
+
+def test_mx_dgrad1(mcase):
+    c = mcase
+    m, dev, n, f = c["m"], c["dev"], c["n"], c["f"]
+    dXd = torch.empty(n, c["d"], dtype=torch.bfloat16, device=dev)
+    hq, hs = c["rows_q"](c["bwd"]["dH"], f)
+    uq, us = c["rows_q"](c["bwd"]["dU"], f)
+    m.grouped_gemm(c["s"], m.GEMM_DGRAD1, c["ws"], tile_offsets=c["tile_offsets"], a0=hq, sfa0=hs,
+                   a1=uq, sfa1=us, w0=c["cache"]["gateT_q"], sfb0=c["cache"]["gateT_s"],
+                   w1=c["cache"]["upT_q"], sfb1=c["cache"]["upT_s"], out0=dXd)
+    assert max_abs_rel(f64(dXd)[: c["used"]], c["bwd"]["dXd"]) <= TOL
+
+
+def run_mx_layer(m, dev, inp, k, L32, backward=True):
+    T, d, E, f = inp["T"], inp["d"], inp["E"], inp["f"]
+    s = m.shape(T, d, E, k, f, prec=m.MXFP8)
+    buf = m.allocate(s, with_grads=backward)
+    t = {nm: to_dev_bf16(inp[nm], dev) for nm in ("x", "w_gate", "w_up", "w_down", "d_out")}
+    m.build_mx_weights(s, t["w_gate"], t["w_up"], t["w_down"], buf.mx_weights)
+    buf.saved["logits"].copy_(torch.from_numpy(L32))
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    m.clear_error(buf.ws)
+    m.forward(buf, t["x"], None, None, t["w_gate"], t["w_up"], t["w_down"], out)
+    if backward:
+        m.backward(buf, t["d_out"], t["x"], None, t["w_gate"], t["w_up"], t["w_down"])
+    return buf, out, m.read_error(buf.ws)
+
+
+def test_mx_layer_small(mcase):
+    c = mcase
+    m, dev = c["m"], c["dev"]
+    buf, out, err = run_mx_layer(m, dev, c["inp"], c["k"], c["L32"])
+    assert err == 0
+    f, b = c["fwd"], c["bwd"]
+    for nm in ("topk_idx", "counts", "offsets", "tile_offsets", "slot_of_route"):
+        np.testing.assert_array_equal(buf.saved[nm].cpu().numpy(), f[nm], err_msg=nm)
+    assert max_abs_rel(f64(out), f["out"]) <= TOL
+    g = buf.grads
+    for mine, ref in [("dx", "dx"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"),
+                      ("dw_down", "dW_down"), ("d_gates", "d_gates"), ("dlogits", "dlogits")]:
+        r = max_abs_rel(f64(g[mine]), b[ref])
+        assert r <= TOL, (mine, r)
+    empty = np.where(f["counts"] == 0)[0]
+    assert (f64(g["dw_gate"])[empty] == 0).all() and (f64(g["dw_down"])[empty] == 0).all()
+
+
+def test_mx_full_size_workload_sampled(moe_gpu):
+    """32768 tokens, d=4096, 64 experts, top-8, f=2048: routing and the dispatched
+    codes in full, two experts' forward rows and weight gradients against the
+    oracle's per-expert MXFP8 math."""
+    m, dev = moe_gpu
+    cfg = CONFIGS["mxfp8"]
+    inp = make_inputs(cfg, seed=0)
+    L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
+    buf, out, err = run_mx_layer(m, dev, inp, cfg.k, L32)
+    assert err == 0
+    idx, gates = O.softmax_topk_gates(L32, cfg.k)
+    counts = O.expert_counts(idx, cfg.E)
+    tile_offsets, row_offsets = O.tile_layout(counts, 128)
+    sor, ros = O.assign_slots(idx, row_offsets)
+    np.testing.assert_array_equal(buf.saved["topk_idx"].cpu().numpy(), idx)
+    np.testing.assert_array_equal(buf.saved["slot_of_route"].cpu().numpy(), sor)
+    n = buf.rows_max
+    xq_all = buf.mx["xd_q"].cpu().numpy()
+    xs_all = sf_unpack(buf.mx["xd_s"].cpu().numpy(), n, cfg.d // 32)
+    codes, scales = q_rows(O.as_f64(inp["x"]))
+    real = ros >= 0
+    np.testing.assert_array_equal(xq_all[: len(ros)][real], codes[ros[real] // cfg.k])
+    np.testing.assert_array_equal(xs_all[: len(ros)][real], scales[ros[real] // cfg.k])
+    assert torch.isfinite(out.float()).all()
+    Y = f64(buf.saved["y"])
+    H = f64(buf.saved["h"])
+    dO = O.as_f64(inp["d_out"])
+    for e in (int(np.argmax(counts)), int(np.argmin(counts))):
+        a, b_ = int(row_offsets[e]), int(row_offsets[e]) + int(counts[e])
+        Xe = O.dequantize_mxfp8(codes, scales)[ros[a:b_] // cfg.k]
+        He = Xe @ O._qdq(inp["w_gate"][e]).T
+        Ue = Xe @ O._qdq(inp["w_up"][e]).T
+        Aq = O._qdq(O.silu(He) * Ue)
+        Ye = Aq @ O._qdq(inp["w_down"][e]).T
+        assert max_abs_rel(H[a:b_], He) <= TOL
+        assert max_abs_rel(Y[a:b_], Ye) <= TOL
+        # weight gradient of W_down for this expert: dY_e^T Aq_e with dY = g * dOut
+        gsel = gates.reshape(-1)[ros[a:b_]]
+        dYe = gsel[:, None] * dO[ros[a:b_] // cfg.k]
+        dWd = dYe.T @ Aq
+        assert max_abs_rel(f64(buf.grads["dw_down"][e]), dWd) <= TOL
