@@ -113,6 +113,14 @@ MOE_API int moe_workspace_size(const moe_shape_t* shape, size_t* ws_bytes);
 /* Zero the device error word in `ws` (enqueued on `stream`). */
 MOE_API int moe_clear_error(void* ws, void* stream);
 
+/* Test hook for the failure path (host-side fault injection; no GPU fault is
+ * ever raised).  While `mode` is 1, the TMA producer of every following
+ * grouped-GEMM launch issues no copies, so the MMA issuer's bounded wait runs
+ * out after about one second: the kernel sets MOE_DEVERR_TIMEOUT in the error
+ * word, frees its tensor memory and returns (that launch's outputs are
+ * undefined).  mode 0 restores normal operation.  Returns the previous mode. */
+MOE_API int moe_debug_inject_stall(int32_t mode);
+
 /* Synchronise `stream`, then copy the error word to *code.  Diagnostics only:
  * the one call that waits for the GPU. */
 MOE_API int moe_read_error(const void* ws, int32_t* code, void* stream);

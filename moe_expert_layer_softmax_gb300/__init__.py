@@ -42,6 +42,7 @@ EXPORTS = (
     "moe_route", "moe_dispatch", "moe_quantize_mxfp8", "moe_grouped_gemm", "moe_combine",
     "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
     "moe_route_noalloc", "moe_dequantize_mxfp8", "moe_build_mx_weights",
+    "moe_debug_inject_stall",
 )
 
 
@@ -116,6 +117,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_workspace_size": [P(Shape), P(ctypes.c_size_t)],
         "moe_clear_error": [_vp, _vp],
         "moe_read_error": [_vp, P(i32), _vp],
+        "moe_debug_inject_stall": [i32],
         "moe_route": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_route_noalloc": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_dispatch": [P(Shape)] + [_vp] * 6 + [_vp],
@@ -192,6 +194,15 @@ def workspace_size(s: Shape) -> int:
 
 def clear_error(ws, stream=None):
     _check("moe_clear_error", load().moe_clear_error(_ptr(ws), _stream(stream)))
+
+
+def debug_inject_stall(mode: int) -> int:
+    """Test hook: 1 makes the next grouped-GEMM launches stall on purpose (their
+    bounded waits time out and report MOE_DEVERR_TIMEOUT); 0 turns it off."""
+    rc = load().moe_debug_inject_stall(int(mode))
+    if rc < 0:
+        raise MoEError("moe_debug_inject_stall", rc)
+    return rc
 
 
 def read_error(ws, stream=None) -> int:

@@ -276,6 +276,11 @@ int moe_clear_error(void* ws, void* stream) {
   return MOE_OK;
 }
 
+int moe_debug_inject_stall(int32_t mode) {
+  if (mode != 0 && mode != 1) return MOE_ERR_INVALID;
+  return gemm_set_inject_stall(mode);
+}
+
 int moe_read_error(const void* ws, int32_t* code, void* stream) {
   if (ws == nullptr || code == nullptr) return MOE_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

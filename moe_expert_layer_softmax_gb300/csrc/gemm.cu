@@ -30,6 +30,7 @@
 //                          the expert's (padded, zero-filled) rows
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -100,6 +101,7 @@ struct Params {
   uint8_t* osf0;         // scales of quantised outputs (sf_offset layout, osf_kb blocks/row)
   uint8_t* osf1;
   int osf_kb;
+  int inject_stall;      // test hook: the producer issues nothing (see moe_debug_inject_stall)
   void* out0;
   void* out1;
   void* out2;
@@ -201,6 +203,7 @@ MOE_DEV void stage_loads(const Params& p, const TileInfo& ti, int ks, uint8_t* s
 template <bool MX>
 MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap* tA0,
                       const CUtensorMap* tA1, const CUtensorMap* tB0, const CUtensorMap* tB1) {
+  if (p.inject_stall) return;   // the consumers' bounded waits must run out
   const int nt = total_tiles(p, s.tile_off);
   const uint32_t bytes = (uint32_t)p.tx_bytes;
   int stage = 0;
@@ -593,6 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
+std::atomic<int> g_inject_stall{0};
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -625,6 +630,8 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 }  // namespace
 
+int gemm_set_inject_stall(int mode) { return g_inject_stall.exchange(mode); }
+
 cudaError_t gemm_init_attributes() {
   if (!get_encoder()) return cudaErrorInitializationError;
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
@@ -650,6 +657,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   p.m_split = 1 << 30;
   p.kstep = kBK;
   p.acc_cols = 256;
+  p.inject_stall = g_inject_stall.load();
   bool mx = false;
   int64_t max_tiles = 0;
   switch (g.op) {
