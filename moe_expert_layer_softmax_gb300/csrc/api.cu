@@ -4,7 +4,7 @@
 // moe_read_error.  Declarations and documentation: include/moe.h.
 #include <cstring>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "common.cuh"
 #include "kernels.h"
 

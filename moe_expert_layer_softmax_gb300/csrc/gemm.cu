@@ -48,7 +48,8 @@ enum Epi {
 };
 
 constexpr int kMaxStages = 12;
-constexpr int kRingBytes = 224 * 1024;
+constexpr int kRingBytes = 192 * 1024;
+constexpr int kStageOutBytes = 16 * 1024;     // per column half: 128 rows x 128 bytes
 constexpr int kBK = 64;                       // bf16 elements of K per stage (128 bytes)
 constexpr int kABytes = kTileM * kBK * 2;     // 16 KB
 constexpr int kBBytesMax = 256 * kBK * 2;     // 32 KB
@@ -68,7 +69,7 @@ struct __align__(8) Ctl {
   int32_t tile_off[kMaxE + 1];
 };
 
-constexpr int kSmemBytes = 1024 + kRingBytes + (int)sizeof(Ctl);
+constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStageOutBytes + (int)sizeof(Ctl);
 
 struct Params {
   int mode;
@@ -102,6 +103,8 @@ struct Params {
   uint8_t* osf1;
   int osf_kb;
   int inject_stall;      // test hook: the producer issues nothing (see moe_debug_inject_stall)
+  int tma_store;         // epilogue writes through swizzled smem + TMA bulk stores
+  int64_t out_rows_per_group;  // KGROUP TMA store: rows of one expert's output (M)
   void* out0;
   void* out1;
   void* out2;
@@ -508,7 +511,178 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
   }
 }
 
-MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane) {
+// ---- epilogue through shared memory: each column half owns a 16 KB buffer of
+// 128 rows x 128 bytes in the 128-byte swizzled layout of the output tensor
+// maps; thread r fills row r, one elected thread issues the TMA bulk store.
+struct OutStager {
+  uint8_t* buf;
+  int bar_id;
+  bool leader;
+  int r;
+  // the buffer is free once the previous bulk store has read it
+  MOE_DEV void begin() const {
+    if (leader) bulk_wait_read_all();
+    bar_sync(bar_id, kEpiThreads / 2);
+  }
+  MOE_DEV void put16(int j, const uint4& v) const {   // 128-byte rows, 128-byte swizzle
+    *reinterpret_cast<uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+  }
+  MOE_DEV void put16_r64(int j, const uint4& v) const {   // 64-byte rows, 64-byte swizzle
+    *reinterpret_cast<uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) = v;
+  }
+  // 64 fp32 -> 64 bf16 (128 bytes)
+  MOE_DEV void row_bf16(const uint32_t* lo, const uint32_t* hi) const {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      put16(j, make_uint4(pack_bf16x2(__uint_as_float(lo[8 * j]), __uint_as_float(lo[8 * j + 1])),
+                          pack_bf16x2(__uint_as_float(lo[8 * j + 2]), __uint_as_float(lo[8 * j + 3])),
+                          pack_bf16x2(__uint_as_float(lo[8 * j + 4]), __uint_as_float(lo[8 * j + 5])),
+                          pack_bf16x2(__uint_as_float(lo[8 * j + 6]), __uint_as_float(lo[8 * j + 7]))));
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      put16(4 + j, make_uint4(pack_bf16x2(__uint_as_float(hi[8 * j]), __uint_as_float(hi[8 * j + 1])),
+                              pack_bf16x2(__uint_as_float(hi[8 * j + 2]), __uint_as_float(hi[8 * j + 3])),
+                              pack_bf16x2(__uint_as_float(hi[8 * j + 4]), __uint_as_float(hi[8 * j + 5])),
+                              pack_bf16x2(__uint_as_float(hi[8 * j + 6]), __uint_as_float(hi[8 * j + 7]))));
+  }
+  // 32 fp32 (128 bytes)
+  MOE_DEV void row_f32(const uint32_t* v) const {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) put16(j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+  }
+  MOE_DEV void row_zero() const {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) put16(j, make_uint4(0, 0, 0, 0));
+  }
+  MOE_DEV void end(const CUtensorMap* map, int x, int y) const {
+    fence_proxy_async_smem();
+    bar_sync(bar_id, kEpiThreads / 2);
+    if (leader) {
+      tma_store_2d(map, buf, x, y);
+      bulk_commit();
+    }
+  }
+};
+
+MOE_DEV void silu_mul32(const uint32_t* h, const uint32_t* u, uint32_t* a) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    a[i] = __float_as_uint(silu_f(__uint_as_float(h[i])) * __uint_as_float(u[i]));
+}
+
+// 8 columns of dH = dA * U * silu'(H) (want_dh) or dU = dA * silu(H), packed to bf16
+template <bool kDH>
+MOE_DEV uint4 swiglu_bwd8(const uint32_t* da, const uint4& hq, const uint4& uq) {
+  float h[8], u[8], g[8];
+  unpack8(hq, h);
+  unpack8(uq, u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a = __uint_as_float(da[i]);
+    const float sg = 1.0f / (1.0f + __expf(-h[i]));
+    if (kDH)
+      g[i] = a * u[i] * (sg * (1.0f + h[i] * (1.0f - sg)));
+    else
+      g[i] = a * (h[i] * sg);
+  }
+  return pack8(g);
+}
+
+// Columns [c0, c1) of the tile through the stager (bf16 outputs 64 columns per
+// store, fp32 outputs 32 columns per store).
+MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb, int c0, int c1,
+                               const OutStager& st, const CUtensorMap* tO0,
+                               const CUtensorMap* tO1, const CUtensorMap* tO2) {
+  uint32_t v0[32], v1[32];
+  const int y = ti.m_tile * kTileM;
+  if (p.epi == EPI_BF16) {
+    const int xb = ti.n_tile * p.BN;
+    for (int c = c0; c < c1; c += 64) {
+      tmem_ld32x2(tb + c, tb + c + 32, v0, v1);
+      st.begin();
+      st.row_bf16(v0, v1);
+      st.end(tO0, xb + c, y);
+    }
+  } else if (p.epi == EPI_SWIGLU_FWD) {
+    // accumulator columns [0, 128) are H, [128, 256) are U
+    const int xb = ti.n_tile * 128;
+    for (int c = c0; c < c1; c += 64) {
+      tmem_ld32x2(tb + c, tb + c + 32, v0, v1);              // H
+      st.begin();
+      st.row_bf16(v0, v1);
+      st.end(tO0, xb + c, y);
+      tmem_ld32x2(tb + 128 + c, tb + 128 + c + 32, v0, v1);  // U
+      st.begin();
+      st.row_bf16(v0, v1);
+      st.end(tO1, xb + c, y);
+      // A = silu(H) * U, H re-read from tensor memory 32 columns at a time
+      uint32_t h[32];
+      st.begin();
+      tmem_ld32(tb + c, h);
+      silu_mul32(h, v0, h);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st.put16(j, make_uint4(pack_bf16x2(__uint_as_float(h[8 * j]), __uint_as_float(h[8 * j + 1])),
+                               pack_bf16x2(__uint_as_float(h[8 * j + 2]), __uint_as_float(h[8 * j + 3])),
+                               pack_bf16x2(__uint_as_float(h[8 * j + 4]), __uint_as_float(h[8 * j + 5])),
+                               pack_bf16x2(__uint_as_float(h[8 * j + 6]), __uint_as_float(h[8 * j + 7]))));
+      tmem_ld32(tb + c + 32, h);
+      silu_mul32(h, v1, h);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st.put16(4 + j, make_uint4(pack_bf16x2(__uint_as_float(h[8 * j]), __uint_as_float(h[8 * j + 1])),
+                                   pack_bf16x2(__uint_as_float(h[8 * j + 2]), __uint_as_float(h[8 * j + 3])),
+                                   pack_bf16x2(__uint_as_float(h[8 * j + 4]), __uint_as_float(h[8 * j + 5])),
+                                   pack_bf16x2(__uint_as_float(h[8 * j + 6]), __uint_as_float(h[8 * j + 7]))));
+      st.end(tO2, xb + c, y);
+    }
+  } else if (p.epi == EPI_SWIGLU_BWD) {
+    const int xb = ti.n_tile * p.BN;
+    const int64_t off = (int64_t)(y + st.r) * p.ldo + xb;
+    const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
+    const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
+    // 32 columns per round; the output maps have 64-byte boxes (64-byte swizzle)
+    uint4 hq[4], uq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      hq[q] = H[c0 / 8 + q];
+      uq[q] = U[c0 / 8 + q];
+    }
+    for (int c = c0; c < c1; c += 32) {
+      tmem_ld32(tb + c, v0);   // dA
+      st.begin();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st.put16_r64(q, swiglu_bwd8<true>(v0 + 8 * q, hq[q], uq[q]));
+      st.end(tO0, xb + c, y);
+      st.begin();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st.put16_r64(q, swiglu_bwd8<false>(v0 + 8 * q, hq[q], uq[q]));
+      if (c + 32 < c1) {        // next columns' H and U, loaded while the store drains
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hq[q] = H[(c + 32) / 8 + q];
+          uq[q] = U[(c + 32) / 8 + q];
+        }
+      }
+      st.end(tO1, xb + c, y);
+    }
+  } else {  // EPI_F32: weight gradients, fp32 [E * M, N]
+    const bool hi = ti.m_tile >= p.m_split;
+    const int yy = (int)(ti.e * p.out_rows_per_group) + (ti.m_tile - (hi ? p.m_split : 0)) * kTileM;
+    const CUtensorMap* map = hi ? tO1 : tO0;
+    const int xb = ti.n_tile * p.BN;
+    for (int c = c0; c < c1; c += 32) {
+      if (ti.ks != 0) tmem_ld32(tb + c, v0);
+      st.begin();
+      if (ti.ks != 0) st.row_f32(v0); else st.row_zero();
+      st.end(map, xb + c, yy);
+    }
+  }
+}
+
+MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
+                      uint8_t* stage_out, const CUtensorMap* tO0, const CUtensorMap* tO1,
+                      const CUtensorMap* tO2) {
   const int nt = total_tiles(p, s.tile_off);
   const int quarter = warp & 3;            // TMEM lanes this warp may access
   const int half = (warp - 2) >> 2;        // which half of the tile's columns
@@ -523,18 +697,30 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     c0 = 0;
     c1 = (half == 0) ? width : 0;
   }
+  OutStager st;
+  st.buf = stage_out + half * kStageOutBytes;
+  st.bar_id = 1 + half;
+  st.leader = (quarter == 2) && (lane == 0);   // first warp of the half (warp 2 or 6)
+  st.r = r;
   int it = 0;
   for (int t = blockIdx.x; t < nt; t += gridDim.x, ++it) {
     const TileInfo ti = decode_tile(p, s.tile_off, t);
     const int acc = it & 1;
     const uint32_t use = (uint32_t)(it >> 1);
-    if (!mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err)) break;
+    bool ok = mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err);
+    // the half's named barriers below need all four of its warps: leave together
+    if (p.tma_store) ok = bar_and(st.bar_id, kEpiThreads / 2, ok);
+    if (!ok) break;
     tc_fence_after();
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
-    epilogue_tile(p, ti, r, tb, c0, c1);
+    if (p.tma_store)
+      epilogue_tile_tma(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
+    else
+      epilogue_tile(p, ti, r, tb, c0, c1);
     tc_fence_before();
     mbar_arrive(&s.tempty[acc]);
   }
+  if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
 }
 
 template <bool MX>
@@ -542,11 +728,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                         const __grid_constant__ CUtensorMap tA1,
                         const __grid_constant__ CUtensorMap tB0,
-                        const __grid_constant__ CUtensorMap tB1, const Params p) {
+                        const __grid_constant__ CUtensorMap tB1,
+                        const __grid_constant__ CUtensorMap tO0,
+                        const __grid_constant__ CUtensorMap tO1,
+                        const __grid_constant__ CUtensorMap tO2, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Ctl& s = *reinterpret_cast<Ctl*>(ring + kRingBytes);
+  uint8_t* stage_out = ring + kRingBytes;
+  Ctl& s = *reinterpret_cast<Ctl*>(stage_out + 2 * kStageOutBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -571,6 +761,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tA1);
     prefetch_tensormap(&tB0);
     prefetch_tensormap(&tB1);
+    if (p.tma_store) {
+      prefetch_tensormap(&tO0);
+      prefetch_tensormap(&tO1);
+      prefetch_tensormap(&tO2);
+    }
   }
   if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
   tc_fence_before();
@@ -583,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) mma_issuer<MX>(p, s, ring, tmem_base);
   } else {
-    epilogue(p, s, tmem_base, warp, lane);
+    epilogue(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2);
   }
 
   tc_fence_before();
@@ -615,15 +810,20 @@ bool get_encoder() {
 
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
 // box of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+enum MapType { MAP_BF16 = 0, MAP_U8 = 1, MAP_F32 = 2 };
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool u8 = false) {
+              uint32_t box_outer, int type = MAP_BF16, bool swizzle64 = false) {
+  const int esz = type == MAP_U8 ? 1 : (type == MAP_F32 ? 4 : 2);
+  const CUtensorMapDataType dt = type == MAP_U8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : (type == MAP_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * (u8 ? 1 : 2)};
+  cuuint64_t strides[1] = {inner * (uint64_t)esz};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                  const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -646,7 +846,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   const DeviceInfo* di = device_info();
   if (di == nullptr || !di->ready) return cudaErrorInitializationError;
   Params p = {};
-  CUtensorMap A0, A1, B0, B1;
+  CUtensorMap A0, A1, B0, B1, O0, O1, O2;
   const uint64_t rows = (uint64_t)g.rows_max;
   const int d = g.d, f = g.f, E = g.E;
   bool ok = true;
@@ -668,6 +868,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
            make_map(&B1, g.w1, d, (uint64_t)E * f, 64, 128);
       A1 = A0;
       p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.ldo = f;
+      ok = ok && make_map(&O0, g.out0, f, rows, 64, 128) && make_map(&O1, g.out1, f, rows, 64, 128) &&
+           make_map(&O2, g.out2, f, rows, 64, 128);
+      p.tma_store = 1;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
       break;
     case OP_FWD2:
@@ -677,6 +880,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
            make_map(&B0, g.w0, f, (uint64_t)E * d, 64, (uint32_t)p.BN);
       A1 = A0; B1 = B0;
       p.out0 = g.out0; p.ldo = d;
+      ok = ok && make_map(&O0, g.out0, d, rows, 64, 128);
+      O1 = O2 = O0;
+      p.tma_store = 1;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
       break;
     case OP_DGRAD2_SWIGLU:
@@ -685,6 +891,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       ok = make_map(&A0, g.a0, d, rows, 64, 128) && make_map(&B0, g.w0, f, (uint64_t)E * d, 64, 64);
       A1 = A0; B1 = B0;
       p.out0 = g.out0; p.out1 = g.out1; p.aux0 = g.aux0; p.aux1 = g.aux1; p.ldo = f;
+      ok = ok && make_map(&O0, g.out0, f, rows, 32, 128, MAP_BF16, true) &&
+           make_map(&O1, g.out1, f, rows, 32, 128, MAP_BF16, true);
+      O2 = O0;
+      p.tma_store = 1;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
       break;
     case OP_DGRAD1:
@@ -694,6 +904,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
            make_map(&B0, g.w0, d, (uint64_t)E * f, 64, 64) &&
            make_map(&B1, g.w1, d, (uint64_t)E * f, 64, 64);
       p.out0 = g.out0; p.ldo = d;
+      ok = ok && make_map(&O0, g.out0, d, rows, 64, 128);
+      O1 = O2 = O0;
+      p.tma_store = 1;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
       break;
     case OP_WGRAD2:
@@ -702,6 +915,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       ok = make_map(&A0, g.a0, d, rows, 64, 64) && make_map(&B0, g.a1, f, rows, 64, 64);
       A1 = A0; B1 = B0;
       p.out0 = g.out0; p.ldo = f; p.out_group_stride = (int64_t)d * f;
+      ok = ok && make_map(&O0, g.out0, f, (uint64_t)E * d, 32, 128, MAP_F32);
+      O1 = O2 = O0;
+      p.tma_store = 1;
+      p.out_rows_per_group = d;
       max_tiles = (int64_t)E * p.m_tiles * p.n_tiles;
       break;
     case OP_WGRAD1:
@@ -712,6 +929,11 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
            make_map(&B0, g.aux0, d, rows, 64, 64);
       B1 = B0;
       p.out0 = g.out0; p.out1 = g.out1; p.ldo = d; p.out_group_stride = (int64_t)f * d;
+      ok = ok && make_map(&O0, g.out0, d, (uint64_t)E * f, 32, 128, MAP_F32) &&
+           make_map(&O1, g.out1, d, (uint64_t)E * f, 32, 128, MAP_F32);
+      O2 = O0;
+      p.tma_store = 1;
+      p.out_rows_per_group = f;
       max_tiles = (int64_t)E * p.m_tiles * p.n_tiles;
       break;
     case OP_ROUTER: {
@@ -729,8 +951,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     case OP_MX_FWD1_SWIGLU:
       mx = true; p.mode = MODE_MGROUP; p.epi = EPI_SWIGLU_FWD_MX; p.BN = 128;
       p.n_tiles = 2 * f / 128; p.k_steps = d / 128; p.b_group_rows = 2 * f;
-      ok = make_map(&A0, g.a0, d, rows, 128, 128, true) &&
-           make_map(&B0, g.w0, d, (uint64_t)E * 2 * f, 128, 128, true);
+      ok = make_map(&A0, g.a0, d, rows, 128, 128, MAP_U8) &&
+           make_map(&B0, g.w0, d, (uint64_t)E * 2 * f, 128, 128, MAP_U8);
       A1 = A0; B1 = B0;
       p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = d / 128;
       p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.osf0 = g.osf0; p.osf_kb = f / 32;
@@ -740,8 +962,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     case OP_MX_FWD2:
       mx = true; p.mode = MODE_MGROUP; p.epi = EPI_BF16; p.BN = 128;
       p.n_tiles = d / 128; p.k_steps = f / 128; p.b_group_rows = d;
-      ok = make_map(&A0, g.a0, f, rows, 128, 128, true) &&
-           make_map(&B0, g.w0, f, (uint64_t)E * d, 128, 128, true);
+      ok = make_map(&A0, g.a0, f, rows, 128, 128, MAP_U8) &&
+           make_map(&B0, g.w0, f, (uint64_t)E * d, 128, 128, MAP_U8);
       A1 = A0; B1 = B0;
       p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = f / 128;
       p.out0 = g.out0; p.ldo = d;
@@ -750,8 +972,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     case OP_MX_DGRAD2_SWIGLU:
       mx = true; p.mode = MODE_MGROUP; p.epi = EPI_SWIGLU_BWD_MX; p.BN = 128;
       p.n_tiles = f / 128; p.k_steps = d / 128; p.b_group_rows = f;
-      ok = make_map(&A0, g.a0, d, rows, 128, 128, true) &&
-           make_map(&B0, g.w0, d, (uint64_t)E * f, 128, 128, true);
+      ok = make_map(&A0, g.a0, d, rows, 128, 128, MAP_U8) &&
+           make_map(&B0, g.w0, d, (uint64_t)E * f, 128, 128, MAP_U8);
       A1 = A0; B1 = B0;
       p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = d / 128;
       p.aux0 = g.aux0; p.aux1 = g.aux1;
@@ -762,9 +984,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     case OP_MX_DGRAD1:
       mx = true; p.mode = MODE_MGROUP; p.epi = EPI_BF16; p.BN = 128;
       p.n_tiles = d / 128; p.k_steps = 2 * f / 128; p.k_split = f / 128; p.b_group_rows = d;
-      ok = make_map(&A0, g.a0, f, rows, 128, 128, true) && make_map(&A1, g.a1, f, rows, 128, 128, true) &&
-           make_map(&B0, g.w0, f, (uint64_t)E * d, 128, 128, true) &&
-           make_map(&B1, g.w1, f, (uint64_t)E * d, 128, 128, true);
+      ok = make_map(&A0, g.a0, f, rows, 128, 128, MAP_U8) && make_map(&A1, g.a1, f, rows, 128, 128, MAP_U8) &&
+           make_map(&B0, g.w0, f, (uint64_t)E * d, 128, 128, MAP_U8) &&
+           make_map(&B1, g.w1, f, (uint64_t)E * d, 128, 128, MAP_U8);
       p.sfa0 = g.sfa0; p.sfa1 = g.sfa1; p.sfb0 = g.sfb0; p.sfb1 = g.sfb1; p.sf_ka = p.sf_kb = f / 128;
       p.out0 = g.out0; p.ldo = d;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
@@ -773,6 +995,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if (!p.tma_store) O0 = O1 = O2 = A0;   // unused by the direct-store epilogues
   if (mx) {
     p.kstep = 128;
     p.acc_cols = 128;
@@ -788,9 +1011,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   int grid = (int)(max_tiles < di->sm_count ? max_tiles : di->sm_count);
   if (grid < 1) grid = 1;
   if (mx)
-    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);
+    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0, O1, O2, p);
   else
-    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, p);
+    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0, O1, O2,
+                                                                        p);
   return cudaGetLastError();
 }
 

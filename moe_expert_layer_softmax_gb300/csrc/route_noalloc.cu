@@ -23,7 +23,7 @@
 //     two streams at once) race on the array: serialise them.
 #include <mutex>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "common.cuh"
 #include "kernels.h"
 
