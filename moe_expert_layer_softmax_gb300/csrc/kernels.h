@@ -10,7 +10,7 @@ namespace moe {
 
 // Tokens handled by one block of the top-k kernel; the per-block expert
 // histograms and route ranks are taken over these tokens.
-constexpr int kRouteTokensPerBlock = 64;
+constexpr int kRouteTokensPerBlock = 16;
 
 struct DeviceInfo {
   int sm_count = 0;

@@ -18,7 +18,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kTopkThreads = 256;  // 8 warps; each warp handles 8 of the block's 64 tokens
+constexpr int kTopkThreads = 256;  // 8 warps; each warp handles 2 of the block's 16 tokens
 
 // Order used for the selection: larger key first, lower expert id on ties.
 // NaN is treated as -inf so that the selection stays a valid set of k distinct
