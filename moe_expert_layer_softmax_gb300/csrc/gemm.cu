@@ -67,9 +67,13 @@ struct __align__(8) Ctl {
   uint32_t tmem_base;
   int abort;
   int32_t tile_off[kMaxE + 1];
+  int32_t pair_off[kMaxE + 1];   // CTA pairs: exclusive scan of ceil(m-tiles / 2) per expert
 };
 
-constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStageOutBytes + (int)sizeof(Ctl);
+// the dynamic shared memory is declared 1024-byte aligned (the swizzled tiles
+// need it), so no alignment slack is requested
+constexpr int kSmemBytes = kRingBytes + 2 * kStageOutBytes + (int)sizeof(Ctl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Params {
   int mode;
@@ -105,6 +109,9 @@ struct Params {
   int inject_stall;      // test hook: the producer issues nothing (see moe_debug_inject_stall)
   int tma_store;         // epilogue writes through swizzled smem + TMA bulk stores
   int64_t out_rows_per_group;  // KGROUP TMA store: rows of one expert's output (M)
+  int num_acc;           // TMEM accumulators (2: the epilogue overlaps the next tile)
+  int tmem_cols;         // TMEM columns allocated
+  int pair_half_bytes;   // CTA pairs: bytes one CTA's copies deliver per stage
   void* out0;
   void* out1;
   void* out2;
@@ -295,6 +302,169 @@ MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_ba
   }
   // everything this thread issued must be finished before TMEM is freed
   tc_commit(&s.fin);
+  const uint32_t a = smem_u32(&s.fin);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, 0)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      raise_error(p.err, MOE_DEVERR_TIMEOUT);
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ CTA pairs
+// A pair of CTAs (a cluster of two) runs one 256 x BN tile with one
+// tcgen05.mma.cta_group::2 (M = 256): CTA r holds rows [128 r, 128 r + 128)
+// of A and columns [r BN/2, (r + 1) BN/2) of B in its shared memory, and rows
+// [128 r, 128 r + 128) of the accumulator in its tensor memory.  The even CTA
+// issues the MMAs; the odd CTA's copies complete on the even CTA's `full`
+// barriers, the MMA commits arrive on both CTAs' barriers (multicast), and the
+// odd CTA's epilogue arrives on the even CTA's `tempty` barrier.
+
+// Tile `t` of the pair schedule, seen from CTA `rank`.  M-grouped: the pair
+// covers m-tiles (2j, 2j + 1) of one expert; when the expert has an odd number
+// of m-tiles the odd CTA of its last pair reloads the even CTA's rows and
+// stores nothing (`valid` false).  K-grouped: m-tiles (2i, 2i + 1).
+MOE_DEV int total_tiles_pair(const Params& p, const Ctl& s) {
+  if (p.mode == MODE_MGROUP) return s.pair_off[p.E] * p.n_tiles;
+  return p.E * (p.m_tiles / 2) * p.n_tiles;
+}
+MOE_DEV TileInfo decode_pair(const Params& p, const Ctl& s, int t, int rank, bool& valid) {
+  TileInfo ti;
+  valid = true;
+  if (p.mode == MODE_KGROUP) {
+    const int per = (p.m_tiles / 2) * p.n_tiles;
+    ti.e = t / per;
+    const int r = t - ti.e * per;
+    const int pm = r / p.n_tiles;
+    ti.n_tile = r - pm * p.n_tiles;
+    ti.m_tile = 2 * pm + rank;
+    ti.k0row = s.tile_off[ti.e] * kTileM;
+    ti.ks = (s.tile_off[ti.e + 1] - s.tile_off[ti.e]) * (kTileM / kBK);
+  } else {
+    const int pt = t / p.n_tiles;
+    ti.n_tile = t - pt * p.n_tiles;
+    ti.e = find_group(s.pair_off, p.E, pt);
+    const int m = s.tile_off[ti.e] + 2 * (pt - s.pair_off[ti.e]) + rank;
+    valid = m < s.tile_off[ti.e + 1];
+    ti.m_tile = valid ? m : m - 1;
+    ti.k0row = 0;
+    ti.ks = p.k_steps;
+  }
+  return ti;
+}
+
+// One stage's copies of this CTA (its A rows and its half of B), counted on
+// the even CTA's full barrier (cluster address `fb`).
+MOE_DEV void stage_loads_pair(const Params& p, const TileInfo& ti, int ks, int rank, uint8_t* sa,
+                              uint32_t fb, const CUtensorMap* tA0, const CUtensorMap* tA1,
+                              const CUtensorMap* tB0, const CUtensorMap* tB1) {
+  uint8_t* sb = sa + kABytes;
+  const int nh = p.BN / 2;                        // this CTA's columns of B
+  const int n0 = ti.n_tile * p.BN + rank * nh;
+  if (p.mode == MODE_KGROUP) {
+    const bool hi = ti.m_tile >= p.m_split;
+    const CUtensorMap* ma = hi ? tA1 : tA0;
+    const int mcol = (ti.m_tile - (hi ? p.m_split : 0)) * kTileM;
+    const int krow = ti.k0row + ks * kBK;
+    tma_load_2d_pair(sa, ma, fb, mcol, krow);
+    tma_load_2d_pair(sa + kABytes / 2, ma, fb, mcol + 64, krow);
+    for (int i = 0; i < nh / 64; ++i) tma_load_2d_pair(sb + i * 8192, tB0, fb, n0 + 64 * i, krow);
+    return;
+  }
+  const bool src1 = ks >= p.k_split;
+  const int kk = (src1 ? ks - p.k_split : ks) * kBK;
+  const CUtensorMap* mb = src1 ? tB1 : tB0;
+  tma_load_2d_pair(sa, src1 ? tA1 : tA0, fb, kk, ti.m_tile * kTileM);
+  if (p.b_mn) {
+    const int krow = ti.e * p.b_group_rows + kk;
+    for (int i = 0; i < nh / 64; ++i) tma_load_2d_pair(sb + i * 8192, mb, fb, n0 + 64 * i, krow);
+  } else if (p.b_dual) {   // the even CTA holds the gate rows, the odd CTA the up rows
+    tma_load_2d_pair(sb, rank == 0 ? tB0 : tB1, fb, kk, ti.e * p.b_group_rows + ti.n_tile * 128);
+  } else {
+    tma_load_2d_pair(sb, mb, fb, kk, ti.e * p.b_group_rows + n0);
+  }
+}
+
+MOE_DEV void producer_pair(const Params& p, Ctl& s, uint8_t* ring, int rank,
+                           const CUtensorMap* tA0, const CUtensorMap* tA1, const CUtensorMap* tB0,
+                           const CUtensorMap* tB1) {
+  if (p.inject_stall) return;
+  const int nt = total_tiles_pair(p, s);
+  const int nclusters = (int)gridDim.x / 2;
+  const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);   // even CTA's full[0]
+  int stage = 0;
+  uint32_t phase = 0;
+  long issued = 0;
+  bool ok = true;
+  for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters) {
+    bool valid;
+    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    for (int ks = 0; ks < ti.ks; ++ks) {
+      if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
+      if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)p.pair_half_bytes);
+      ++issued;
+      stage_loads_pair(p, ti, ks, rank, ring + stage * p.stage_bytes, full0 + 8u * (uint32_t)stage,
+                       tA0, tA1, tB0, tB1);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+  if (!ok) {
+    // copies in flight land on the even CTA's barriers: the even CTA waits for
+    // the stages it armed; both give their copies time to land before leaving
+    if (rank == 0) {
+      for (long i = (issued > p.stages ? issued - p.stages : 0); i < issued; ++i) {
+        const uint32_t a = smem_u32(&s.full[(int)(i % p.stages)]);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(a, (uint32_t)((i / p.stages) & 1))) {
+          if (globaltimer() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 100000ull) {}   // 100 us
+  }
+}
+
+MOE_DEV void mma_issuer_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_base, int rank) {
+  if (rank == 0) {
+    const int nt = total_tiles_pair(p, s);
+    const int nclusters = (int)gridDim.x / 2;
+    const int n_mma = p.b_dual ? 256 : p.BN;
+    const uint32_t idesc = idesc_bf16_f32(2 * kTileM, n_mma, p.a_mn, p.b_mn);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters, ++it) {
+      bool valid;
+      const TileInfo ti = decode_pair(p, s, t, 0, valid);
+      const int acc = it % p.num_acc;
+      const uint32_t use = (uint32_t)(it / p.num_acc);
+      if (!mbar_wait(&s.tempty[acc], (use & 1u) ^ 1u, &s.abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tmem_d = tmem_base + (uint32_t)(acc * p.acc_cols);
+      for (int ks = 0; ks < ti.ks; ++ks) {
+        if (!mbar_wait(&s.full[stage], phase, &s.abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(ring + stage * p.stage_bytes);
+        const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = p.b_mn ? smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                     : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          tc_mma_bf16_pair(tmem_d, ad, bd, idesc, (ks | k) != 0 ? 1u : 0u);
+        }
+        tc_commit_pair(&s.empty[stage]);
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit_pair(&s.tfull[acc]);
+    }
+    tc_commit_pair(&s.fin);      // both CTAs learn when the pair's MMAs are done
+  }
   const uint32_t a = smem_u32(&s.fin);
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(a, 0)) {
@@ -680,10 +850,15 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
   }
 }
 
+template <bool PAIR>
 MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                       uint8_t* stage_out, const CUtensorMap* tO0, const CUtensorMap* tO1,
-                      const CUtensorMap* tO2) {
-  const int nt = total_tiles(p, s.tile_off);
+                      const CUtensorMap* tO2, int rank) {
+  const int nt = PAIR ? total_tiles_pair(p, s) : total_tiles(p, s.tile_off);
+  const int t_first = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int t_step = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+  // the pair's accumulator-empty barriers live in the even CTA
+  const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&s.tempty[0]), 0) : 0u;
   const int quarter = warp & 3;            // TMEM lanes this warp may access
   const int half = (warp - 2) >> 2;        // which half of the tile's columns
   const int r = quarter * 32 + lane;
@@ -703,27 +878,33 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   st.leader = (quarter == 2) && (lane == 0);   // first warp of the half (warp 2 or 6)
   st.r = r;
   int it = 0;
-  for (int t = blockIdx.x; t < nt; t += gridDim.x, ++it) {
-    const TileInfo ti = decode_tile(p, s.tile_off, t);
-    const int acc = it & 1;
-    const uint32_t use = (uint32_t)(it >> 1);
+  for (int t = t_first; t < nt; t += t_step, ++it) {
+    bool valid = true;
+    const TileInfo ti = PAIR ? decode_pair(p, s, t, rank, valid) : decode_tile(p, s.tile_off, t);
+    const int acc = it % p.num_acc;
+    const uint32_t use = (uint32_t)(it / p.num_acc);
     bool ok = mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err);
     // the half's named barriers below need all four of its warps: leave together
     if (p.tma_store) ok = bar_and(st.bar_id, kEpiThreads / 2, ok);
     if (!ok) break;
     tc_fence_after();
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
-    if (p.tma_store)
-      epilogue_tile_tma(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
-    else
-      epilogue_tile(p, ti, r, tb, c0, c1);
+    if (valid) {
+      if (p.tma_store)
+        epilogue_tile_tma(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
+      else
+        epilogue_tile(p, ti, r, tb, c0, c1);
+    }
     tc_fence_before();
-    mbar_arrive(&s.tempty[acc]);
+    if (PAIR)
+      mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+    else
+      mbar_arrive(&s.tempty[acc]);
   }
   if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
 }
 
-template <bool MX>
+template <bool MX, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                         const __grid_constant__ CUtensorMap tA1,
@@ -732,13 +913,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tO0,
                         const __grid_constant__ CUtensorMap tO1,
                         const __grid_constant__ CUtensorMap tO2, const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {   // uniform over the grid: report and leave
+    if (threadIdx.x == 0) raise_error(p.err, MOE_DEVERR_BOUNDS);
+    return;
+  }
+  uint8_t* ring = smem_raw;
   uint8_t* stage_out = ring + kRingBytes;
   Ctl& s = *reinterpret_cast<Ctl*>(stage_out + 2 * kStageOutBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages; ++i) {
@@ -747,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], kEpiThreads);
+      mbar_init(&s.tempty[i], PAIR ? 2 * kEpiThreads : kEpiThreads);
     }
     mbar_init(&s.fin, 1);
     s.abort = 0;
@@ -755,6 +940,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (p.mode != MODE_DENSE) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.tile_off[i] = p.tile_offsets[i];
+  }
+  if (PAIR) {
+    __syncthreads();
+    if (threadIdx.x == 0 && p.mode == MODE_MGROUP) {
+      int run = 0;
+      for (int e = 0; e < p.E; ++e) {
+        s.pair_off[e] = run;
+        run += (s.tile_off[e + 1] - s.tile_off[e] + 1) / 2;
+      }
+      s.pair_off[p.E] = run;
+    }
+    cluster_sync();   // both CTAs' barriers are initialised before any remote arrive
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tA0);
@@ -767,31 +964,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tO2);
     }
   }
-  if (warp == 1) tmem_alloc(&s.tmem_base, kTmemCols);
+  if (warp == 1) {
+    if (PAIR)
+      tmem_alloc_pair(&s.tmem_base, (uint32_t)p.tmem_cols);
+    else
+      tmem_alloc(&s.tmem_base, kTmemCols);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer<MX>(p, s, ring, &tA0, &tA1, &tB0, &tB1);
+    if (lane == 0) {
+      if (PAIR)
+        producer_pair(p, s, ring, rank, &tA0, &tA1, &tB0, &tB1);
+      else
+        producer<MX>(p, s, ring, &tA0, &tA1, &tB0, &tB1);
+    }
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<MX>(p, s, ring, tmem_base);
+    if (lane == 0) {
+      if (PAIR)
+        mma_issuer_pair(p, s, ring, tmem_base, rank);
+      else
+        mma_issuer<MX>(p, s, ring, tmem_base);
+    }
   } else {
-    epilogue(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2);
+    epilogue<PAIR>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();   // the partner no longer reads this CTA's memory
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // ------------------------------------------------------------------ host side
 std::atomic<int> g_inject_stall{0};
+
+// GEMMs that run on CTA pairs (measured on the 8192-token, 32-expert layer:
+// fwd2 -6%, dgrad1 -8%, wgrad2 -11%, wgrad1 -13% against single CTAs; fwd1
+// and dgrad2, whose epilogues are the heaviest, gain nothing and stay single).
+bool op_uses_pairs(int op) {
+  return op == OP_FWD2 || op == OP_DGRAD1 || op == OP_WGRAD1 || op == OP_WGRAD2;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -834,10 +1059,13 @@ int gemm_set_inject_stall(int mode) { return g_inject_stall.exchange(mode); }
 
 cudaError_t gemm_init_attributes() {
   if (!get_encoder()) return cudaErrorInitializationError;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<true, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
@@ -858,6 +1086,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   p.kstep = kBK;
   p.acc_cols = 256;
   p.inject_stall = g_inject_stall.load();
+  p.num_acc = 2;
+  p.tmem_cols = (int)kTmemCols;
   bool mx = false;
   int64_t max_tiles = 0;
   switch (g.op) {
@@ -996,11 +1226,29 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   }
   if (!ok) return cudaErrorInvalidValue;
   if (!p.tma_store) O0 = O1 = O2 = A0;   // unused by the direct-store epilogues
+  // CTA pairs: bf16 M-grouped GEMMs, and K-grouped ones with an even number of M tiles
+  const bool pair = op_uses_pairs(g.op) && !mx && p.tma_store &&
+                    (p.mode == MODE_MGROUP || (p.mode == MODE_KGROUP && p.m_tiles % 2 == 0));
+  if (pair && p.mode == MODE_MGROUP && !p.b_mn && !p.b_dual) {
+    // K-major B: each CTA of the pair loads BN/2 rows
+    const void* wb = (g.op == OP_FWD2) ? g.w0 : nullptr;
+    if (wb == nullptr || !make_map(&B0, wb, f, (uint64_t)E * d, 64, (uint32_t)(p.BN / 2)))
+      return cudaErrorInvalidValue;
+    B1 = B0;
+  }
   if (mx) {
     p.kstep = 128;
     p.acc_cols = 128;
     p.tx_bytes = kABytes + p.BN * 128 + 512 * (1 + p.BN / 128);
     p.stage_bytes = (p.tx_bytes + 1023) & ~1023;
+  } else if (pair) {
+    p.pair_half_bytes = kABytes + (p.BN / 2) * kBK * 2;
+    p.tx_bytes = 2 * p.pair_half_bytes;
+    p.stage_bytes = p.pair_half_bytes;
+    // two 256-column accumulators per CTA: the pair's allocation is collective
+    // (both CTAs receive the same columns)
+    p.num_acc = 2;
+    p.tmem_cols = 512;
   } else {
     p.tx_bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
     p.stage_bytes = p.tx_bytes;
@@ -1010,11 +1258,45 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   if (p.stages < 2 || p.stage_bytes % 1024 != 0) return cudaErrorInvalidValue;
   int grid = (int)(max_tiles < di->sm_count ? max_tiles : di->sm_count);
   if (grid < 1) grid = 1;
+  if (pair) {
+    const int64_t pairs = (p.mode == MODE_MGROUP) ? (max_tiles / 2 + (int64_t)E * p.n_tiles)
+                                                  : max_tiles / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many pairs as can be resident at once (persistent tile loop)
+    static int resident[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && resident[dev] == 0) {
+      cfg.gridDim = dim3((unsigned)di->sm_count);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<false, true>, &cfg) != cudaSuccess ||
+          n < 1)
+        n = di->sm_count / 2;
+      resident[dev] = n;
+    }
+    int64_t np = (dev >= 0 && dev < 64) ? resident[dev] : di->sm_count / 2;
+    if (pairs < np) np = pairs;
+    if (np < 1) np = 1;
+    cfg.gridDim = dim3((unsigned)(2 * np));
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true>, A0, A1, B0, B1, O0, O1, O2,
+                              p);
+  }
   if (mx)
-    grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0, O1, O2, p);
+    grouped_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0, O1,
+                                                                             O2, p);
   else
-    grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0, O1, O2,
-                                                                        p);
+    grouped_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0,
+                                                                              O1, O2, p);
   return cudaGetLastError();
 }
 
