@@ -158,9 +158,10 @@ MOE_API int moe_route(const moe_shape_t* shape, const void* x, const void* w_rou
 
 /* Allocation-free variant of moe_route.  The pages have no counterpart to this
  * call: it exists for callers that cannot hand the library a workspace buffer
- * (code running inside a CUDA graph capture, where cudaMalloc is not allowed;
- * code that must stay out of the allocator because cudaMalloc can synchronise
- * the device; hosts working inside a fixed, pre-assigned memory budget).
+ * (plugins hosted by a framework that owns all device memory and exposes no
+ * allocator to them; hosts working inside a fixed, pre-assigned memory budget;
+ * latency-critical loops that must stay out of cudaMalloc because it can
+ * synchronise the whole device and stall work on other streams).
  *
  * Same arguments and results as moe_route, without `ws`.  Its scratch (error
  * word, per-block histograms, per-route ranks) lives in one static device

@@ -2,11 +2,11 @@
 // workspace buffer.
 //
 // moe_route needs `ws` (error word, per-block expert histograms, per-route
-// ranks).  Some callers have no way to obtain that device memory: code that
-// runs while a CUDA graph is being captured (cudaMalloc is not allowed there),
-// code that must not enter the allocator because cudaMalloc can synchronise
-// the whole device and stall other streams, and hosts that work inside a fixed
-// device-memory budget handed out up front.  This variant keeps its scratch in
+// ranks).  Some callers have no way to obtain that device memory: plugins
+// hosted by a framework that owns all device memory and offers them no
+// allocator, hosts that work inside a fixed device-memory budget handed out up
+// front, and latency-critical loops that must not enter cudaMalloc because it
+// can synchronise the whole device and stall other streams.  This variant keeps its scratch in
 // one file-scope device array instead, so the caller passes only inputs and
 // outputs and nothing is ever allocated.
 //

@@ -1,8 +1,9 @@
 """moe_route_noalloc against moe_route (GPU).
 
-moe_route_noalloc serves callers that cannot allocate device memory (inside a
-CUDA graph capture, or code that must stay out of the allocator): it takes no
-workspace and keeps its scratch in a static device array of the library.  Its
+moe_route_noalloc serves callers that cannot allocate device memory (plugins
+whose host owns all device memory, fixed memory budgets, loops that must stay
+out of cudaMalloc because it can synchronise the device): it takes no workspace
+and keeps its scratch in a static device array of the library.  Its
 results must equal those of moe_route, the call it stands in for, on two calls
 in a row (the array keeps the previous call's contents, so the second call
 checks that nothing stale leaks through).  This file is collected last on
