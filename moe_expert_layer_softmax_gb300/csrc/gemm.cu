@@ -162,7 +162,9 @@ MOE_DEV TileInfo decode_tile(const Params& p, const int32_t* off, int t) {
   return ti;
 }
 
-MOE_DEV float silu_f(float h) { return h / (1.0f + __expf(-h)); }
+// logistic sigmoid with the fast reciprocal (the results are stored in bf16)
+MOE_DEV float sigmoid_f(float h) { return __fdividef(1.0f, 1.0f + __expf(-h)); }
+MOE_DEV float silu_f(float h) { return h * sigmoid_f(h); }
 
 // ------------------------------------------------------------------ roles
 // One stage's TMA loads (and, for MXFP8, the stage's scale atoms).
@@ -578,7 +580,7 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float da = __uint_as_float(v[8 * q + i]);
-          const float sg = 1.0f / (1.0f + __expf(-h[i]));
+          const float sg = sigmoid_f(h[i]);
           const float si = h[i] * sg;
           const float ds = sg * (1.0f + h[i] * (1.0f - sg));
           gh[8 * q + i] = __float_as_uint(da * u[i] * ds);
@@ -634,7 +636,7 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float da = __uint_as_float(v[8 * q + i]);
-          const float sg = 1.0f / (1.0f + __expf(-h[i]));
+          const float sg = sigmoid_f(h[i]);
           const float si = h[i] * sg;
           const float ds = sg * (1.0f + h[i] * (1.0f - sg));
           gh[8 * q + i] = __float_as_uint(da * u[i] * ds);
@@ -697,8 +699,9 @@ struct OutStager {
   MOE_DEV void put16(int j, const uint4& v) const {   // 128-byte rows, 128-byte swizzle
     *reinterpret_cast<uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4)) = v;
   }
-  MOE_DEV void put16_r64(int j, const uint4& v) const {   // 64-byte rows, 64-byte swizzle
-    *reinterpret_cast<uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) = v;
+  // 64-byte rows, 64-byte swizzle; `part` selects one of two 8 KB boxes
+  MOE_DEV void put16_r64(int j, const uint4& v, int part) const {
+    *reinterpret_cast<uint4*>(buf + part * 8192 + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) = v;
   }
   // 64 fp32 -> 64 bf16 (128 bytes)
   MOE_DEV void row_bf16(const uint32_t* lo, const uint32_t* hi) const {
@@ -732,6 +735,16 @@ struct OutStager {
       bulk_commit();
     }
   }
+  // both 8 KB boxes: box 0 to map0, box 1 to map1, at the same coordinates
+  MOE_DEV void end2(const CUtensorMap* map0, const CUtensorMap* map1, int x, int y) const {
+    fence_proxy_async_smem();
+    bar_sync(bar_id, kEpiThreads / 2);
+    if (leader) {
+      tma_store_2d(map0, buf, x, y);
+      tma_store_2d(map1, buf + 8192, x, y);
+      bulk_commit();
+    }
+  }
 };
 
 MOE_DEV void silu_mul32(const uint32_t* h, const uint32_t* u, uint32_t* a) {
@@ -740,22 +753,31 @@ MOE_DEV void silu_mul32(const uint32_t* h, const uint32_t* u, uint32_t* a) {
     a[i] = __float_as_uint(silu_f(__uint_as_float(h[i])) * __uint_as_float(u[i]));
 }
 
-// 8 columns of dH = dA * U * silu'(H) (want_dh) or dU = dA * silu(H), packed to bf16
-template <bool kDH>
-MOE_DEV uint4 swiglu_bwd8(const uint32_t* da, const uint4& hq, const uint4& uq) {
-  float h[8], u[8], g[8];
+// 8 columns of dH = dA * U * silu'(H) and dU = dA * silu(H), packed to bf16
+MOE_DEV void swiglu_bwd8(const uint32_t* da, const uint4& hq, const uint4& uq, uint4& dh,
+                         uint4& du) {
+  float h[8], u[8], gh[8], gu[8];
   unpack8(hq, h);
   unpack8(uq, u);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float a = __uint_as_float(da[i]);
-    const float sg = 1.0f / (1.0f + __expf(-h[i]));
-    if (kDH)
-      g[i] = a * u[i] * (sg * (1.0f + h[i] * (1.0f - sg)));
-    else
-      g[i] = a * (h[i] * sg);
+    const float sg = sigmoid_f(h[i]);
+    gh[i] = a * u[i] * (sg * (1.0f + h[i] * (1.0f - sg)));
+    gu[i] = a * (h[i] * sg);
   }
-  return pack8(g);
+  dh = pack8(gh);
+  du = pack8(gu);
+}
+
+// L2 prefetch of the H and U columns [c0, c1) of row r of a tile (SwiGLU
+// backward reads them in its epilogue; issued one tile ahead)
+MOE_DEV void prefetch_aux_row(const Params& p, const TileInfo& ti, int r, int c0, int c1) {
+  if (c1 <= c0) return;
+  const int64_t off = ((int64_t)ti.m_tile * kTileM + r) * p.ldo + (int64_t)ti.n_tile * p.BN + c0;
+  const uint32_t bytes = (uint32_t)(c1 - c0) * 2u;
+  bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(p.aux0) + off, bytes);
+  bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(p.aux1) + off, bytes);
 }
 
 // Columns [c0, c1) of the tile through the stager (bf16 outputs 64 columns per
@@ -818,23 +840,25 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
       hq[q] = H[c0 / 8 + q];
       uq[q] = U[c0 / 8 + q];
     }
+    // one round per 32 columns: dH into box 0, dU into box 1 of the half's buffer
     for (int c = c0; c < c1; c += 32) {
       tmem_ld32(tb + c, v0);   // dA
       st.begin();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) st.put16_r64(q, swiglu_bwd8<true>(v0 + 8 * q, hq[q], uq[q]));
-      st.end(tO0, xb + c, y);
-      st.begin();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) st.put16_r64(q, swiglu_bwd8<false>(v0 + 8 * q, hq[q], uq[q]));
-      if (c + 32 < c1) {        // next columns' H and U, loaded while the store drains
+      for (int q = 0; q < 4; ++q) {
+        uint4 gh, gu;
+        swiglu_bwd8(v0 + 8 * q, hq[q], uq[q], gh, gu);
+        st.put16_r64(q, gh, 0);
+        st.put16_r64(q, gu, 1);
+      }
+      if (c + 32 < c1) {        // next columns' H and U, loaded while the stores drain
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           hq[q] = H[(c + 32) / 8 + q];
           uq[q] = U[(c + 32) / 8 + q];
         }
       }
-      st.end(tO1, xb + c, y);
+      st.end2(tO0, tO1, xb + c, y);
     }
   } else {  // EPI_F32: weight gradients, fp32 [E * M, N]
     const bool hi = ti.m_tile >= p.m_split;
@@ -877,10 +901,22 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   st.bar_id = 1 + half;
   st.leader = (quarter == 2) && (lane == 0);   // first warp of the half (warp 2 or 6)
   st.r = r;
+  const bool pf = (p.epi == EPI_SWIGLU_BWD) && p.tma_store;
+  if (pf && t_first < nt) {
+    bool v;
+    const TileInfo t0 = PAIR ? decode_pair(p, s, t_first, rank, v) : decode_tile(p, s.tile_off, t_first);
+    prefetch_aux_row(p, t0, r, c0, c1);
+  }
   int it = 0;
   for (int t = t_first; t < nt; t += t_step, ++it) {
     bool valid = true;
     const TileInfo ti = PAIR ? decode_pair(p, s, t, rank, valid) : decode_tile(p, s.tile_off, t);
+    if (pf && t + t_step < nt) {   // this thread's rows of the next tile's H and U
+      bool v;
+      const TileInfo tn = PAIR ? decode_pair(p, s, t + t_step, rank, v)
+                               : decode_tile(p, s.tile_off, t + t_step);
+      prefetch_aux_row(p, tn, r, c0, c1);
+    }
     const int acc = it % p.num_acc;
     const uint32_t use = (uint32_t)(it / p.num_acc);
     bool ok = mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err);
