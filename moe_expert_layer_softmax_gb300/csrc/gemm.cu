@@ -1048,10 +1048,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 std::atomic<int> g_inject_stall{0};
 
 // GEMMs that run on CTA pairs (measured on the 8192-token, 32-expert layer:
-// fwd2 -6%, dgrad1 -8%, wgrad2 -11%, wgrad1 -13% against single CTAs; fwd1
-// and dgrad2, whose epilogues are the heaviest, gain nothing and stay single).
+// fwd2 -6%, dgrad1 -8%, wgrad2 -11%, wgrad1 -13%, fwd1 -3% against single
+// CTAs; dgrad2, whose epilogue is the heaviest, gains nothing and stays single).
 bool op_uses_pairs(int op) {
-  return op == OP_FWD2 || op == OP_DGRAD1 || op == OP_WGRAD1 || op == OP_WGRAD2;
+  return op == OP_FWD1_SWIGLU || op == OP_FWD2 || op == OP_DGRAD1 || op == OP_WGRAD1 ||
+         op == OP_WGRAD2;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

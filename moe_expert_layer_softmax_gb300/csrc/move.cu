@@ -268,14 +268,18 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_kernel(
 }
 
 // Pass 1: partial[m][col] = sum over the real rows s of tile m of
-// dlogits[t(s), e(m)] * x[t(s)][col], for a 1024-column chunk (128 threads x 8).
-constexpr int kRbThreads = 128;
+// dlogits[t(s), e(m)] * x[t(s)][col], for a 1024-column chunk: 128 column
+// threads x 8 columns, and two row groups (even and odd rows) whose sums are
+// added in a fixed order at the end.  Eight row loads are in flight per thread.
+constexpr int kRbCols = 128;
+constexpr int kRbThreads = 2 * kRbCols;
 __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
     const uint4* __restrict__ x, const float* __restrict__ dlogits,
     const int32_t* __restrict__ route_of_slot, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ tile_offsets, int d, int E, int k, float* __restrict__ partial) {
   __shared__ int32_t s_tok[kTileM];
   __shared__ float s_dl[kTileM];
+  __shared__ float4 s_odd[2][kRbCols];
   const int m = blockIdx.x;
   if (m >= tile_offsets[E]) return;
   // expert owning tile m: the largest e with tile_offsets[e] <= m
@@ -295,35 +299,47 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
     s_dl[threadIdx.x] = dlogits[(size_t)t * E + e];
   }
   __syncthreads();
-  const int c = blockIdx.y * kRbThreads + threadIdx.x;
-  if (c >= nv) return;
+  const int ct = threadIdx.x % kRbCols;
+  const int grp = threadIdx.x / kRbCols;        // rows grp, grp + 2, grp + 4, ...
+  const int c = blockIdx.y * kRbCols + ct;
+  const bool ok = c < nv;
   float acc[kVec];
 #pragma unroll
   for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
-  int r = 0;
-  for (; r + 4 <= nrows; r += 4) {
-    uint4 v[4];
+  if (ok) {
+    int r = grp;
+    for (; r + 14 < nrows; r += 16) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldg(x + (size_t)s_tok[r + u] * nv + c);
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(x + (size_t)s_tok[r + 2 * u] * nv + c);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
+        float f[kVec];
+        unpack8(v[u], f);
+        const float dl = s_dl[r + 2 * u];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
+      }
+    }
+    for (; r < nrows; r += 2) {
       float f[kVec];
-      unpack8(v[u], f);
-      const float dl = s_dl[r + u];
+      unpack8(__ldg(x + (size_t)s_tok[r] * nv + c), f);
+      const float dl = s_dl[r];
 #pragma unroll
       for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
     }
   }
-  for (; r < nrows; ++r) {
-    float f[kVec];
-    unpack8(__ldg(x + (size_t)s_tok[r] * nv + c), f);
-    const float dl = s_dl[r];
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
+  if (grp == 1) {
+    s_odd[0][ct] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    s_odd[1][ct] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
-  float4* dst = reinterpret_cast<float4*>(partial + (size_t)m * d + (size_t)c * kVec);
-  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  if (grp == 0 && ok) {
+    const float4 a = s_odd[0][ct], b = s_odd[1][ct];
+    float4* dst = reinterpret_cast<float4*>(partial + (size_t)m * d + (size_t)c * kVec);
+    dst[0] = make_float4(acc[0] + a.x, acc[1] + a.y, acc[2] + a.z, acc[3] + a.w);
+    dst[1] = make_float4(acc[4] + b.x, acc[5] + b.y, acc[6] + b.z, acc[7] + b.w);
+  }
 }
 
 // Pass 2: dW_r[e][col] = sum over e's tiles in order (zero for empty experts).
@@ -401,7 +417,7 @@ cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t
                               cudaStream_t s) {
   (void)T;
   const int nv = d / kVec;
-  dim3 g1((unsigned)tiles_max, (unsigned)((nv + kRbThreads - 1) / kRbThreads));
+  dim3 g1((unsigned)tiles_max, (unsigned)((nv + kRbCols - 1) / kRbCols));
   router_bwd_partial_kernel<<<g1, kRbThreads, 0, s>>>(static_cast<const uint4*>(x), dlogits,
                                                       route_of_slot, counts, tile_offsets, d, E, k,
                                                       partial);
