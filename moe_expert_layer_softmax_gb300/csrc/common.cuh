@@ -113,6 +113,19 @@ MOE_DEV void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation (launch_pdl): it may be scheduled
+// while the previous kernel of the stream is still finishing.  Each kernel
+// first allows its own successor to be scheduled, then calls pdl_wait()
+// before its first global-memory access: pdl_wait() returns once the
+// previous kernel has completed and its writes are visible.
+MOE_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void pdl_begin() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
 MOE_DEV void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

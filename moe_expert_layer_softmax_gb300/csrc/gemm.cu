@@ -951,6 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tO2, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0) {   // uniform over the grid: report and leave
+    pdl_wait();
     if (threadIdx.x == 0) raise_error(p.err, MOE_DEVERR_BOUNDS);
     return;
   }
@@ -960,6 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages; ++i) {
@@ -974,6 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.abort = 0;
     fence_barrier_init();
   }
+  pdl_wait();   // the previous kernel's outputs (operands, tile_offsets) are visible from here
   if (p.mode != MODE_DENSE) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.tile_off[i] = p.tile_offsets[i];
   }
@@ -1325,16 +1328,19 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (pairs < np) np = pairs;
     if (np < 1) np = 1;
     cfg.gridDim = dim3((unsigned)(2 * np));
+    cudaLaunchAttribute attr2[2] = {attr[0], {}};
+    attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr2[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr2;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true>, A0, A1, B0, B1, O0, O1, O2,
                               p);
   }
   if (mx)
-    grouped_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0, O1,
-                                                                             O2, p);
-  else
-    grouped_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(A0, A1, B0, B1, O0,
-                                                                              O1, O2, p);
-  return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<true, false>, dim3(grid), dim3(kThreads), kSmemBytes,
+                      stream, A0, A1, B0, B1, O0, O1, O2, p);
+  return launch_pdl(grouped_gemm_kernel<false, false>, dim3(grid), dim3(kThreads), kSmemBytes,
+                    stream, A0, A1, B0, B1, O0, O1, O2, p);
 }
 
 }  // namespace moe

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bf16_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
     int E, int k, int token_blocks, uint4* __restrict__ xd) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int nv = d / kVec;
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bf16_kernel(
 __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ gates,
     const int32_t* __restrict__ slot_of_route, int T, int d, int k, uint4* __restrict__ out) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
     int E, int k, int token_blocks, uint4* __restrict__ dy, float* __restrict__ d_gates,
     float* __restrict__ dlogits) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nv = d / kVec;
   if (blockIdx.x >= token_blocks) {
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_kernel(
     const uint4* __restrict__ dxd, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ dlogits,
     const uint4* __restrict__ w_router, int T, int d, int E, int k, uint4* __restrict__ dx) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -277,6 +281,7 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
     const uint4* __restrict__ x, const float* __restrict__ dlogits,
     const int32_t* __restrict__ route_of_slot, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ tile_offsets, int d, int E, int k, float* __restrict__ partial) {
+  pdl_begin();
   __shared__ int32_t s_tok[kTileM];
   __shared__ float s_dl[kTileM];
   __shared__ float4 s_odd[2][kRbCols];
@@ -346,6 +351,7 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
 __global__ void __launch_bounds__(256) router_bwd_reduce_kernel(
     const float* __restrict__ partial, const int32_t* __restrict__ tile_offsets, int d,
     float* __restrict__ dw) {
+  pdl_begin();
   const int e = blockIdx.y;
   const int col = blockIdx.x * 256 + threadIdx.x;
   if (col >= d) return;
@@ -362,7 +368,7 @@ cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
                                  const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                  int E, int k, void* xd, cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  dispatch_bf16_kernel<<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+  launch_pdl(dispatch_bf16_kernel, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
       static_cast<const uint4*>(x), slot_of_route, counts, tile_offsets, T, d, E, k, tb,
       static_cast<uint4*>(xd));
   return cudaGetLastError();
@@ -371,7 +377,7 @@ cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
 cudaError_t launch_combine(const void* y, const float* gates, const int32_t* slot_of_route, int T,
                            int d, int k, void* out, cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  combine_kernel<<<tb, kMoveThreads, 0, s>>>(static_cast<const uint4*>(y), gates, slot_of_route, T,
+  launch_pdl(combine_kernel, dim3(tb), dim3(kMoveThreads), 0, s, static_cast<const uint4*>(y), gates, slot_of_route, T,
                                              d, k, static_cast<uint4*>(out));
   return cudaGetLastError();
 }
@@ -383,12 +389,12 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (k <= 8)
-    combine_bwd_kernel<8><<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+    launch_pdl(combine_bwd_kernel<8>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
         slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
         dlogits);
   else
-    combine_bwd_kernel<32><<<tb + pad_blocks(E), kMoveThreads, 0, s>>>(
+    launch_pdl(combine_bwd_kernel<32>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
         slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
         dlogits);
@@ -401,11 +407,11 @@ cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
                                 cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (k <= 8)
-    dispatch_bwd_kernel<8><<<tb, kMoveThreads, 0, s>>>(
+    launch_pdl(dispatch_bwd_kernel<8>, dim3(tb), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
         static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
   else
-    dispatch_bwd_kernel<32><<<tb, kMoveThreads, 0, s>>>(
+    launch_pdl(dispatch_bwd_kernel<32>, dim3(tb), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
         static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
   return cudaGetLastError();
@@ -418,13 +424,13 @@ cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t
   (void)T;
   const int nv = d / kVec;
   dim3 g1((unsigned)tiles_max, (unsigned)((nv + kRbCols - 1) / kRbCols));
-  router_bwd_partial_kernel<<<g1, kRbThreads, 0, s>>>(static_cast<const uint4*>(x), dlogits,
+  launch_pdl(router_bwd_partial_kernel, dim3(g1), dim3(kRbThreads), 0, s, static_cast<const uint4*>(x), dlogits,
                                                       route_of_slot, counts, tile_offsets, d, E, k,
                                                       partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2((unsigned)((d + 255) / 256), (unsigned)E);
-  router_bwd_reduce_kernel<<<g2, 256, 0, s>>>(partial, tile_offsets, d, dw_router);
+  launch_pdl(router_bwd_reduce_kernel, dim3(g2), dim3(256), 0, s, partial, tile_offsets, d, dw_router);
   return cudaGetLastError();
 }
 

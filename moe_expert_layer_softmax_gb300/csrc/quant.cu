@@ -25,6 +25,7 @@ constexpr int kQThreads = 256;
 __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     const uint4* __restrict__ src, int64_t nblocks, int rows, int cols, int group, int offset,
     uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  pdl_begin();
   const int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x;
   if (i >= nblocks) return;
   const int kb = cols / 32;
@@ -57,6 +58,7 @@ constexpr int kTK = 128, kTN = 64;
 __global__ void __launch_bounds__(kQThreads) quantize_cols_kernel(
     const __nv_bfloat16* __restrict__ src, int K, int N, uint8_t* __restrict__ q,
     uint8_t* __restrict__ sf) {
+  pdl_begin();
   __shared__ __nv_bfloat16 tile[kTK][kTN];
   const int mat = blockIdx.z;
   const int k0 = blockIdx.y * kTK;
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
     int E, int k, int token_blocks, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = kQThreads / 32;
   const int nv = d / 8;
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
 __global__ void __launch_bounds__(kQThreads) dequantize_kernel(
     const uint4* __restrict__ q, const uint8_t* __restrict__ sf, int64_t nvec, int K,
     uint4* __restrict__ out) {
+  pdl_begin();
   const int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x;
   if (i >= nvec) return;
   const int per_row = K / 16;
@@ -175,11 +179,11 @@ cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis,
                                   uint8_t* q, uint8_t* sf, cudaStream_t s, int group, int offset) {
   if (block_axis == 1) {
     const int64_t n = (int64_t)batch * rows * (cols / 32);
-    quantize_rows_kernel<<<(unsigned)((n + kQThreads - 1) / kQThreads), kQThreads, 0, s>>>(
+    launch_pdl(quantize_rows_kernel, dim3((unsigned)((n + kQThreads - 1) / kQThreads)), dim3(kQThreads), 0, s, 
         static_cast<const uint4*>(src), n, rows, cols, group, offset, q, sf);
   } else {
     dim3 grid((unsigned)(cols / kTN), (unsigned)(rows / kTK), (unsigned)batch);
-    quantize_cols_kernel<<<grid, kQThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows,
+    launch_pdl(quantize_cols_kernel, dim3(grid), dim3(kQThreads), 0, s, static_cast<const __nv_bfloat16*>(src), rows,
                                                     cols, q, sf);
   }
   return cudaGetLastError();
@@ -191,7 +195,7 @@ cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
   const int warps = kQThreads / 32;
   const int tb = (T + warps - 1) / warps;
   const int pb = (E * kTileM + warps - 1) / warps;
-  dispatch_mxfp8_kernel<<<tb + pb, kQThreads, 0, s>>>(static_cast<const uint4*>(x), slot_of_route,
+  launch_pdl(dispatch_mxfp8_kernel, dim3(tb + pb), dim3(kQThreads), 0, s, static_cast<const uint4*>(x), slot_of_route,
                                                       counts, tile_offsets, T, d, E, k, tb, xq, xs);
   return cudaGetLastError();
 }
@@ -199,7 +203,7 @@ cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
 cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t rows, int K,
                                     void* out, cudaStream_t s) {
   const int64_t nvec = rows * (K / 16);
-  dequantize_kernel<<<(unsigned)((nvec + kQThreads - 1) / kQThreads), kQThreads, 0, s>>>(
+  launch_pdl(dequantize_kernel, dim3((unsigned)((nvec + kQThreads - 1) / kQThreads)), dim3(kQThreads), 0, s, 
       reinterpret_cast<const uint4*>(q), sf, nvec, K, static_cast<uint4*>(out));
   return cudaGetLastError();
 }

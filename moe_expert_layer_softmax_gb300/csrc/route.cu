@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ gates, int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
     int32_t* __restrict__ err) {
+  pdl_begin();
   __shared__ int32_t s_sel[kRouteTokensPerBlock * 32];  // expert of each route of the block
   __shared__ int32_t s_cnt[256];
   const int lane = threadIdx.x & 31;
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
     int32_t* __restrict__ block_hist, int n_blocks, int E, int e_pad,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ tile_offsets) {
+  pdl_begin();
   __shared__ int32_t s_part[kScanThreads];  // [p][e] chunk sums
   __shared__ int32_t s_c[256];
   __shared__ int32_t s_t[256];
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(256) route_slots_kernel(
     const int32_t* __restrict__ tile_offsets, int T, int E, int k, int64_t rows_max,
     int32_t* __restrict__ slot_of_route, int32_t* __restrict__ route_of_slot,
     int32_t* __restrict__ err) {
+  pdl_begin();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t R = (int64_t)T * k;
   if (i < R) {
@@ -234,16 +237,16 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
   const int nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   const int epl = (E + 31) / 32;
   if (epl <= 1)
-    route_topk_kernel<1><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+    launch_pdl(route_topk_kernel<1>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
                                                     block_hist, err);
   else if (epl <= 2)
-    route_topk_kernel<2><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+    launch_pdl(route_topk_kernel<2>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
                                                     block_hist, err);
   else if (epl <= 4)
-    route_topk_kernel<4><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+    launch_pdl(route_topk_kernel<4>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
                                                     block_hist, err);
   else
-    route_topk_kernel<8><<<nb, kTopkThreads, 0, s>>>(logits, T, E, k, topk_idx, gates, local_rank,
+    launch_pdl(route_topk_kernel<8>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
                                                     block_hist, err);
   return cudaGetLastError();
 }
@@ -252,7 +255,7 @@ cudaError_t launch_route_scan(int32_t* block_hist, int n_blocks, int E, int32_t*
                               int32_t* offsets, int32_t* tile_offsets, cudaStream_t s) {
   int e_pad = 4;
   while (e_pad < E) e_pad <<= 1;   // E <= 256 -> at least 4 chunks per expert
-  route_scan_kernel<<<1, kScanThreads, 0, s>>>(block_hist, n_blocks, E, e_pad, counts, offsets,
+  launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, block_hist, n_blocks, E, e_pad, counts, offsets,
                                                tile_offsets);
   return cudaGetLastError();
 }
@@ -264,7 +267,7 @@ cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_ran
                                cudaStream_t s) {
   const int64_t n = (int64_t)T * k + (int64_t)E * kTileM;
   const int nb = (int)((n + 255) / 256);
-  route_slots_kernel<<<nb, 256, 0, s>>>(topk_idx, local_rank, block_base, counts, tile_offsets, T,
+  launch_pdl(route_slots_kernel, dim3(nb), dim3(256), 0, s, topk_idx, local_rank, block_base, counts, tile_offsets, T,
                                         E, k, rows_max, slot_of_route, route_of_slot, err);
   return cudaGetLastError();
 }
