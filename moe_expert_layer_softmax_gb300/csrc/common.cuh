@@ -108,11 +108,6 @@ MOE_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
-// Asynchronous prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
-MOE_DEV void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialisation (launch_pdl): it may be scheduled
 // while the previous kernel of the stream is still finishing.  Each kernel

@@ -770,16 +770,6 @@ MOE_DEV void swiglu_bwd8(const uint32_t* da, const uint4& hq, const uint4& uq, u
   du = pack8(gu);
 }
 
-// L2 prefetch of the H and U columns [c0, c1) of row r of a tile (SwiGLU
-// backward reads them in its epilogue; issued one tile ahead)
-MOE_DEV void prefetch_aux_row(const Params& p, const TileInfo& ti, int r, int c0, int c1) {
-  if (c1 <= c0) return;
-  const int64_t off = ((int64_t)ti.m_tile * kTileM + r) * p.ldo + (int64_t)ti.n_tile * p.BN + c0;
-  const uint32_t bytes = (uint32_t)(c1 - c0) * 2u;
-  bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(p.aux0) + off, bytes);
-  bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(p.aux1) + off, bytes);
-}
-
 // Columns [c0, c1) of the tile through the stager (bf16 outputs 64 columns per
 // store, fp32 outputs 32 columns per store).
 MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb, int c0, int c1,
@@ -901,22 +891,10 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   st.bar_id = 1 + half;
   st.leader = (quarter == 2) && (lane == 0);   // first warp of the half (warp 2 or 6)
   st.r = r;
-  const bool pf = (p.epi == EPI_SWIGLU_BWD) && p.tma_store;
-  if (pf && t_first < nt) {
-    bool v;
-    const TileInfo t0 = PAIR ? decode_pair(p, s, t_first, rank, v) : decode_tile(p, s.tile_off, t_first);
-    prefetch_aux_row(p, t0, r, c0, c1);
-  }
   int it = 0;
   for (int t = t_first; t < nt; t += t_step, ++it) {
     bool valid = true;
     const TileInfo ti = PAIR ? decode_pair(p, s, t, rank, valid) : decode_tile(p, s.tile_off, t);
-    if (pf && t + t_step < nt) {   // this thread's rows of the next tile's H and U
-      bool v;
-      const TileInfo tn = PAIR ? decode_pair(p, s, t + t_step, rank, v)
-                               : decode_tile(p, s.tile_off, t + t_step);
-      prefetch_aux_row(p, tn, r, c0, c1);
-    }
     const int acc = it % p.num_acc;
     const uint32_t use = (uint32_t)(it / p.num_acc);
     bool ok = mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err);

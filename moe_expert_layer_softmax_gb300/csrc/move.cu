@@ -123,11 +123,11 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
   }
 }
 
-// KM = compile-time bound on k (8 covers every workload; 32 is the generic
+// KM = compile-time bound on k (4 and 8 cover the workloads; 32 is the generic
 // fallback).  Per 256-column chunk a lane loads dOut once and the k rows of y
 // together, so k + 1 16-byte loads are in flight per lane.
 template <int KM>
-__global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
+__global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1)) combine_bwd_kernel(
     const uint4* __restrict__ d_out, const uint4* __restrict__ y, const float* __restrict__ gates,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kMoveThreads) combine_bwd_kernel(
 }
 
 template <int KM>
-__global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_kernel(
+__global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1)) dispatch_bwd_kernel(
     const uint4* __restrict__ dxd, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ dlogits,
     const uint4* __restrict__ w_router, int T, int d, int E, int k, uint4* __restrict__ dx) {
@@ -388,7 +388,12 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                int E, int k, void* dy, float* d_gates, float* dlogits,
                                cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  if (k <= 8)
+  if (k <= 4)
+    launch_pdl(combine_bwd_kernel<4>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s,
+        static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
+        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
+        dlogits);
+  else if (k <= 8)
     launch_pdl(combine_bwd_kernel<8>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
         slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
@@ -406,7 +411,11 @@ cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
                                 const void* w_router, int T, int d, int E, int k, void* dx,
                                 cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  if (k <= 8)
+  if (k <= 4)
+    launch_pdl(dispatch_bwd_kernel<4>, dim3(tb), dim3(kMoveThreads), 0, s,
+        static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
+        static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
+  else if (k <= 8)
     launch_pdl(dispatch_bwd_kernel<8>, dim3(tb), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
         static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
