@@ -88,6 +88,7 @@ struct Params {
   int BN;                // MMA N (256 when b_dual)
   int n_valid;           // ROUTER: valid columns (E)
   int k_steps;           // DENSE/MGROUP: K / 64
+  int k_parts;           // DENSE: K split into this many parts (1 or 2), summed atomically
   int k_split;           // DENSE/MGROUP: steps >= k_split read maps A1/B1
   int m_split;           // KGROUP: M tiles >= m_split read A1 and write out1
   int b_group_rows;      // expert stride in the rows of B's 2-D view
@@ -125,6 +126,7 @@ struct Params {
 
 struct TileInfo {
   int e, m_tile, n_tile, k0row, ks;
+  int kb;   // DENSE split-K: first K step of this part
 };
 
 MOE_DEV int find_group(const int32_t* off, int E, int m_tile) {
@@ -137,13 +139,25 @@ MOE_DEV int find_group(const int32_t* off, int E, int m_tile) {
 }
 
 MOE_DEV int total_tiles(const Params& p, const int32_t* off) {
-  if (p.mode == MODE_DENSE) return p.m_tiles * p.n_tiles;
+  if (p.mode == MODE_DENSE) return p.m_tiles * p.n_tiles * p.k_parts;
   if (p.mode == MODE_MGROUP) return off[p.E] * p.n_tiles;
   return p.E * p.m_tiles * p.n_tiles;
 }
 
 MOE_DEV TileInfo decode_tile(const Params& p, const int32_t* off, int t) {
   TileInfo ti;
+  ti.kb = 0;
+  if (p.mode == MODE_DENSE) {
+    const int part = t % p.k_parts;
+    const int mt = t / p.k_parts;
+    ti.m_tile = mt / p.n_tiles;
+    ti.n_tile = mt - ti.m_tile * p.n_tiles;
+    ti.e = 0;
+    ti.k0row = 0;
+    ti.ks = p.k_steps / p.k_parts;
+    ti.kb = part * ti.ks;
+    return ti;
+  }
   if (p.mode == MODE_KGROUP) {
     const int per = p.m_tiles * p.n_tiles;
     ti.e = t / per;
@@ -230,7 +244,7 @@ MOE_DEV void producer(const Params& p, Ctl& s, uint8_t* ring, const CUtensorMap*
       uint8_t* sa = ring + stage * p.stage_bytes;
       mbar_arrive_expect_tx(fb, bytes);
       ++issued;
-      stage_loads<MX>(p, ti, ks, sa, fb, tA0, tA1, tB0, tB1);
+      stage_loads<MX>(p, ti, ti.kb + ks, sa, fb, tA0, tA1, tB0, tB1);
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
@@ -334,6 +348,7 @@ MOE_DEV int total_tiles_pair(const Params& p, const Ctl& s) {
 MOE_DEV TileInfo decode_pair(const Params& p, const Ctl& s, int t, int rank, bool& valid) {
   TileInfo ti;
   valid = true;
+  ti.kb = 0;
   if (p.mode == MODE_KGROUP) {
     const int per = (p.m_tiles / 2) * p.n_tiles;
     ti.e = t / per;
@@ -668,15 +683,22 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
       }
     }
   } else {  // EPI_ROUTER: fp32 logits (+ bias), rows < T and columns < E only
+    // With the K loop split in two, each part adds its sum into the zeroed
+    // logits (the first part with the bias): (0 + a) + b == (0 + b) + a, so the
+    // result does not depend on which part lands first.
     const int64_t row = (int64_t)ti.m_tile * kTileM + r;
     float* out = static_cast<float*>(p.out0);
+    const bool add_bias = p.bias != nullptr && ti.kb == 0;
     for (int c = c0; c < c1; c += 32) {
       tmem_ld32(tb + c, v);      // warp-collective: executed by every lane
       if (row < p.m_valid) {
         for (int i = 0; i < 32 && c + i < p.n_valid; ++i) {
           float val = __uint_as_float(v[i]);
-          if (p.bias != nullptr) val += p.bias[row * p.n_valid + c + i];
-          out[row * p.n_valid + c + i] = val;
+          if (add_bias) val += p.bias[row * p.n_valid + c + i];
+          if (p.k_parts > 1)
+            atomicAdd(out + row * p.n_valid + c + i, val);
+          else
+            out[row * p.n_valid + c + i] = val;
         }
       }
     }
@@ -1028,12 +1050,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host side
 std::atomic<int> g_inject_stall{0};
 
-// GEMMs that run on CTA pairs (measured on the 8192-token, 32-expert layer:
-// fwd2 -6%, dgrad1 -8%, wgrad2 -11%, wgrad1 -13%, fwd1 -3% against single
-// CTAs; dgrad2, whose epilogue is the heaviest, gains nothing and stays single).
+// The bf16 data GEMMs run on CTA pairs (measured on the 8192-token, 32-expert
+// layer against single CTAs: fwd2 -6%, dgrad1 -8%, wgrad2 -11%, wgrad1 -13%,
+// fwd1 -3%, dgrad2 -4%); the narrow router GEMM stays on single CTAs.
 bool op_uses_pairs(int op) {
-  return op == OP_FWD1_SWIGLU || op == OP_FWD2 || op == OP_DGRAD1 || op == OP_WGRAD1 ||
-         op == OP_WGRAD2;
+  return op == OP_FWD1_SWIGLU || op == OP_FWD2 || op == OP_DGRAD2_SWIGLU || op == OP_DGRAD1 ||
+         op == OP_WGRAD1 || op == OP_WGRAD2;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1101,6 +1123,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   p.err = g.err;
   p.k_split = 1 << 30;
   p.m_split = 1 << 30;
+  p.k_parts = 1;
   p.kstep = kBK;
   p.acc_cols = 256;
   p.inject_stall = g_inject_stall.load();
@@ -1192,7 +1215,14 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
            make_map(&B0, g.w0, d, (uint64_t)E, 64, (uint32_t)p.BN);
       A1 = A0; B1 = B0;
       p.out0 = g.out0; p.bias = g.bias;
-      max_tiles = p.m_tiles;
+      // few row tiles: two CTAs per tile, each over half of K (the logits are
+      // zeroed first and both halves are added atomically)
+      if (2 * p.m_tiles <= di->sm_count && p.k_steps % 2 == 0) {
+        p.k_parts = 2;
+        if (cudaMemsetAsync(g.out0, 0, (size_t)g.T * E * sizeof(float), stream) != cudaSuccess)
+          return cudaErrorInvalidValue;
+      }
+      max_tiles = (int64_t)p.m_tiles * p.k_parts;
       break;
     }
     // ---- MXFP8: 128x128 tiles, K steps of 128 fp8 (128 bytes), scales per stage
