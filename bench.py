@@ -98,7 +98,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -134,8 +134,9 @@ class ClockSampler:
 _INPUT_CACHE = {}
 
 
-def oracle_sample(cfg, seed: int, budget_s: float = 12.0) -> dict:
-    """Time the CPU oracle's forward+backward on a bounded token sample."""
+def oracle_sample(cfg, seed: int, budget_s: float = 12.0, n_tok: int = 1024) -> dict:
+    """Time the CPU oracle's forward+backward on a bounded token sample (at
+    least one pass over `n_tok` tokens, repeated until `budget_s` has passed)."""
     from oracle import moe_oracle as O
     from synth import make_inputs
 
@@ -143,7 +144,6 @@ def oracle_sample(cfg, seed: int, budget_s: float = 12.0) -> dict:
     if key not in _INPUT_CACHE:
         _INPUT_CACHE[key] = make_inputs(cfg, seed=seed)
     inp = _INPUT_CACHE[key]
-    n_tok = 1024
     sl = slice(0, n_tok)
     x, dO = inp["x"][sl], inp["d_out"][sl]
     bias = inp["bias"][sl] if inp["bias"] is not None else None
@@ -170,11 +170,17 @@ def run_reference(args, cfg):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    # each step is one bounded sample; the whole run stays near two minutes:
+    # 1024-token passes (about 1 s each on 16 cores) for up to ~100 steps,
+    # smaller samples beyond that
+    steps = max(args.steps, 1)
+    budget = min(2.0, 100.0 / steps)
+    n_tok = 1024 if budget >= 1.0 else max(128, 64 * int(16 * budget))
     per = []
     for _ in range(args.warmup):
-        oracle_sample(cfg, 0, budget_s=1.0)
+        oracle_sample(cfg, 0, budget_s=0.0, n_tok=128)
     for _ in range(args.steps):
-        per.append(oracle_sample(cfg, 0, budget_s=max(2.0, 20.0 / max(args.steps, 1))))
+        per.append(oracle_sample(cfg, 0, budget_s=budget, n_tok=n_tok))
     v = sum(p["value"] for p in per) / len(per)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
@@ -263,16 +269,25 @@ def run_ours(args, cfg):
     gemm_fl = sum(fl[k] for k in ("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"))
     peaks = load_peaks()
     dom = max(("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"), key=lambda k: stages[k])
-    achieved = fl[dom] / (stages[dom] / 1000.0) / 1e12
+    # the dominant GEMM's own launch time: CUDA events recorded by the library
+    # around each of its launches during another `steps` whole layer steps
+    m.profile_start(GEMM_OP[dom])
+    for _ in range(args.steps):
+        step()
+    kernel_ms_total, kernel_launches = m.profile_stop()
+    kernel_ms = kernel_ms_total / max(kernel_launches, 1)
+    achieved = fl[dom] / (kernel_ms / 1000.0) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     peak_note = f"{peaks['source']} sustained bf16 (kernel timed inside the step)"
     if mx and dom in ("fwd1", "fwd2", "dgrad2", "dgrad1"):
         # dense fp8 is twice the dense bf16 rate on this part (2.25 -> 4.5 PFLOP/s nominal)
         peak = 2.0 * peaks["bf16_tflops_sustained"]
         peak_note = f"{peaks['source']} sustained bf16 x 2 (nominal fp8/bf16 ratio)"
+    traffic, traffic_note = gemm_traffic(cfg.name, dom)
     roofline = {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({dom})", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                "peak_source": peak_note,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "traffic_source": traffic_note, "kernel_ms": kernel_ms,
+                "kernel_launches_timed": kernel_launches, "peak_source": peak_note,
                 "algorithmic": f"{fl[dom] / 1e9:.1f} GFLOP per launch (useful flops, no tile padding)"}
 
     # ---- end to end through the public API with host buffers
@@ -305,6 +320,43 @@ def run_ours(args, cfg):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+GEMM_OP = {"fwd1": 0, "fwd2": 1, "dgrad2": 2, "dgrad1": 3, "wgrad2": 4, "wgrad1": 5}
+GEMM_SOURCES = ("moe_expert_layer_softmax_gb300/csrc/gemm.cu",
+                "moe_expert_layer_softmax_gb300/csrc/common.cuh",
+                "moe_expert_layer_softmax_gb300/csrc/kernels.h")
+
+
+def gemm_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def gemm_traffic(workload: str, op: str):
+    """DRAM bytes (read + write) of one launch of GEMM `op`, from the committed
+    ncu summary of this workload; None when the GEMM sources changed since."""
+    import re
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_dram_{workload}.md")
+    if not os.path.exists(path):
+        return None, "no ncu capture for this workload"
+    with open(path) as fh:
+        text = fh.read()
+    mt = re.search(r"<!-- dram: (\{.*?\}) -->", text, re.S)
+    if mt is None:
+        return None, "no dram record in " + os.path.relpath(path, ROOT)
+    rec = json.loads(mt.group(1))
+    if rec.get("source_sha256") != gemm_source_hash():
+        return None, "GEMM sources changed since the ncu capture"
+    ops = rec.get("ops", {})
+    if op not in ops:
+        return None, f"{op} not in the ncu capture"
+    return (int(ops[op]["read"]) + int(ops[op]["write"]),
+            "dram__bytes_read.sum + dram__bytes_write.sum, " + os.path.relpath(path, ROOT))
 
 
 def load_peaks():
@@ -498,8 +550,8 @@ def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="fine_grained")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -121,6 +121,17 @@ MOE_API int moe_clear_error(void* ws, void* stream);
  * undefined).  mode 0 restores normal operation.  Returns the previous mode. */
 MOE_API int moe_debug_inject_stall(int32_t mode);
 
+/* Kernel timing hook (the pages have no counterpart: it serves the benchmark's
+ * roofline figure).  moe_profile_start(op) makes every following grouped-GEMM
+ * launch of `op` (a moe_gemm_op_t, through moe_grouped_gemm or the layer
+ * calls) record a pair of CUDA events around itself on its stream, for up to
+ * 1024 launches; the events are created by the library on the first call.
+ * moe_profile_stop() waits for those events, writes the summed milliseconds
+ * and the number of timed launches, and ends the timing.  Host-side only: no
+ * kernel changes.  Not thread-safe against concurrent layer calls. */
+MOE_API int moe_profile_start(int32_t op);
+MOE_API int moe_profile_stop(float* total_ms, int32_t* launches);
+
 /* Synchronise `stream`, then copy the error word to *code.  Diagnostics only:
  * the one call that waits for the GPU. */
 MOE_API int moe_read_error(const void* ws, int32_t* code, void* stream);

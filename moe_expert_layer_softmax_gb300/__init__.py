@@ -42,7 +42,7 @@ EXPORTS = (
     "moe_route", "moe_dispatch", "moe_quantize_mxfp8", "moe_grouped_gemm", "moe_combine",
     "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
     "moe_route_noalloc", "moe_dequantize_mxfp8", "moe_build_mx_weights",
-    "moe_debug_inject_stall",
+    "moe_debug_inject_stall", "moe_profile_start", "moe_profile_stop",
 )
 
 
@@ -118,6 +118,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_clear_error": [_vp, _vp],
         "moe_read_error": [_vp, P(i32), _vp],
         "moe_debug_inject_stall": [i32],
+        "moe_profile_start": [i32],
+        "moe_profile_stop": [_vp, _vp],
         "moe_route": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_route_noalloc": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_dispatch": [P(Shape)] + [_vp] * 6 + [_vp],
@@ -203,6 +205,19 @@ def debug_inject_stall(mode: int) -> int:
     if rc < 0:
         raise MoEError("moe_debug_inject_stall", rc)
     return rc
+
+
+def profile_start(op: int):
+    """moe_profile_start: time every following launch of grouped-GEMM `op`."""
+    _check("moe_profile_start", load().moe_profile_start(int(op)))
+
+
+def profile_stop():
+    """moe_profile_stop: (summed milliseconds, number of timed launches)."""
+    ms = ctypes.c_float(0.0)
+    n = ctypes.c_int32(0)
+    _check("moe_profile_stop", load().moe_profile_stop(ctypes.byref(ms), ctypes.byref(n)))
+    return float(ms.value), int(n.value)
 
 
 def read_error(ws, stream=None) -> int:

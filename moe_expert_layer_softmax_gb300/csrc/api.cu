@@ -3,6 +3,7 @@
 // enqueues kernels on the caller's stream; none waits for the GPU except
 // moe_read_error.  Declarations and documentation: include/moe.h.
 #include <cstring>
+#include <mutex>
 
 #include "moe.h"
 #include "common.cuh"
@@ -123,6 +124,17 @@ int route_impl(const moe_shape_t* s, const void* x, const void* w_router, const 
   return MOE_OK;
 }
 
+// ---- kernel timing hook (moe_profile_start / moe_profile_stop)
+constexpr int kProfMax = 1024;
+struct Profile {
+  std::mutex mu;
+  int op = -1;
+  int used = 0;
+  cudaEvent_t ev[2 * kProfMax] = {};
+  bool created = false;
+};
+Profile g_prof;
+
 int gemm_impl(const moe_shape_t* s, int op, const moe_gemm_args_t* a, void* ws, cudaStream_t st) {
   GemmLaunch g = {};
   g.op = op;
@@ -144,7 +156,14 @@ int gemm_impl(const moe_shape_t* s, int op, const moe_gemm_args_t* a, void* ws, 
   g.aux0 = a->aux0; g.aux1 = a->aux1;
   g.out0 = a->out0; g.out1 = a->out1; g.out2 = a->out2;
   g.err = at<int32_t>(ws, 0);
+  cudaEvent_t* ev = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (g_prof.op == op && g_prof.used < kProfMax) ev = &g_prof.ev[2 * g_prof.used++];
+  }
+  if (ev != nullptr) MOE_CUDA(cudaEventRecord(ev[0], st));
   MOE_CUDA(launch_grouped_gemm(g, st));
+  if (ev != nullptr) MOE_CUDA(cudaEventRecord(ev[1], st));
   return MOE_OK;
 }
 
@@ -279,6 +298,36 @@ int moe_clear_error(void* ws, void* stream) {
 int moe_debug_inject_stall(int32_t mode) {
   if (mode != 0 && mode != 1) return MOE_ERR_INVALID;
   return gemm_set_inject_stall(mode);
+}
+
+int moe_profile_start(int32_t op) {
+  if (op < MOE_GEMM_FWD1_SWIGLU || op > MOE_GEMM_WGRAD1) return MOE_ERR_INVALID;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  if (!g_prof.created) {
+    for (int i = 0; i < 2 * kProfMax; ++i)
+      if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
+    g_prof.created = true;
+  }
+  g_prof.used = 0;
+  g_prof.op = op;
+  return MOE_OK;
+}
+
+int moe_profile_stop(float* total_ms, int32_t* launches) {
+  if (total_ms == nullptr || launches == nullptr) return MOE_ERR_INVALID;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.op = -1;
+  float sum = 0.0f;
+  for (int i = 0; i < g_prof.used; ++i) {
+    MOE_CUDA(cudaEventSynchronize(g_prof.ev[2 * i + 1]));
+    float ms = 0.0f;
+    MOE_CUDA(cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]));
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = g_prof.used;
+  g_prof.used = 0;
+  return MOE_OK;
 }
 
 int moe_read_error(const void* ws, int32_t* code, void* stream) {
