@@ -54,7 +54,11 @@ def compare_grads(g, b, use_router, rows=None):
 
 
 SMALL = [(256, 128, 8, 2, 256), (300, 256, 6, 2, 384), (1000, 512, 16, 4, 256), (77, 384, 4, 4, 128),
-         (1, 128, 4, 2, 128)]
+         (1, 128, 4, 2, 128),
+         # k in 5..8 and k > 8 take the wider gather kernels; 256 experts and
+         # top-32 are the envelope's maxima; T = 513 is not a multiple of the
+         # 16-token routing block
+         (513, 256, 64, 8, 256), (200, 128, 256, 32, 128), (129, 128, 3, 3, 128)]
 
 
 @pytest.mark.parametrize("T,d,E,k,f", SMALL, ids=lambda v: str(v))
@@ -98,7 +102,7 @@ def check_full_path(m, dev, inp, k, backward=True):
     return g
 
 
-@pytest.mark.parametrize("T,d,E,k,f", SMALL[:3], ids=lambda v: str(v))
+@pytest.mark.parametrize("T,d,E,k,f", SMALL[:3] + SMALL[5:7], ids=lambda v: str(v))
 def test_layer_with_router_projection(moe_gpu, T, d, E, k, f):
     m, dev = moe_gpu
     inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=5 * T + d)

@@ -19,6 +19,7 @@ SHAPES = [
     (300, 256, 6, 2, 384),
     (1000, 512, 8, 4, 256),
     (129, 128, 3, 1, 128),
+    (500, 256, 16, 8, 256),    # k = 8: the wider gather kernels
 ]
 
 
