@@ -273,10 +273,12 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
 
 // Pass 1: partial[m][col] = sum over the real rows s of tile m of
 // dlogits[t(s), e(m)] * x[t(s)][col], for a 1024-column chunk: 128 column
-// threads x 8 columns, and two row groups (even and odd rows) whose sums are
-// added in a fixed order at the end.  Eight row loads are in flight per thread.
+// threads x 8 columns, and four row groups (rows g, g + 4, g + 8, ...) whose
+// sums are added in a fixed order at the end.  Eight row loads are in flight
+// per thread.
 constexpr int kRbCols = 128;
-constexpr int kRbThreads = 2 * kRbCols;
+constexpr int kRbGroups = 4;
+constexpr int kRbThreads = kRbGroups * kRbCols;
 __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
     const uint4* __restrict__ x, const float* __restrict__ dlogits,
     const int32_t* __restrict__ route_of_slot, const int32_t* __restrict__ counts,
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
   pdl_begin();
   __shared__ int32_t s_tok[kTileM];
   __shared__ float s_dl[kTileM];
-  __shared__ float4 s_odd[2][kRbCols];
+  __shared__ float4 s_odd[kRbGroups - 1][2][kRbCols];
   const int m = blockIdx.x;
   if (m >= tile_offsets[E]) return;
   // expert owning tile m: the largest e with tile_offsets[e] <= m
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
   }
   __syncthreads();
   const int ct = threadIdx.x % kRbCols;
-  const int grp = threadIdx.x / kRbCols;        // rows grp, grp + 2, grp + 4, ...
+  const int grp = threadIdx.x / kRbCols;        // rows grp, grp + G, grp + 2G, ...
   const int c = blockIdx.y * kRbCols + ct;
   const bool ok = c < nv;
   float acc[kVec];
@@ -313,20 +315,20 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
   for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
   if (ok) {
     int r = grp;
-    for (; r + 14 < nrows; r += 16) {
+    for (; r + 7 * kRbGroups < nrows; r += 8 * kRbGroups) {
       uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldg(x + (size_t)s_tok[r + 2 * u] * nv + c);
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(x + (size_t)s_tok[r + kRbGroups * u] * nv + c);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         float f[kVec];
         unpack8(v[u], f);
-        const float dl = s_dl[r + 2 * u];
+        const float dl = s_dl[r + kRbGroups * u];
 #pragma unroll
         for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
       }
     }
-    for (; r < nrows; r += 2) {
+    for (; r < nrows; r += kRbGroups) {
       float f[kVec];
       unpack8(__ldg(x + (size_t)s_tok[r] * nv + c), f);
       const float dl = s_dl[r];
@@ -334,16 +336,21 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
       for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl, f[i], acc[i]);
     }
   }
-  if (grp == 1) {
-    s_odd[0][ct] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    s_odd[1][ct] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  if (grp > 0) {
+    s_odd[grp - 1][0][ct] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    s_odd[grp - 1][1][ct] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
   __syncthreads();
   if (grp == 0 && ok) {
-    const float4 a = s_odd[0][ct], b = s_odd[1][ct];
+#pragma unroll
+    for (int g2 = 0; g2 < kRbGroups - 1; ++g2) {
+      const float4 a = s_odd[g2][0][ct], b = s_odd[g2][1][ct];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
     float4* dst = reinterpret_cast<float4*>(partial + (size_t)m * d + (size_t)c * kVec);
-    dst[0] = make_float4(acc[0] + a.x, acc[1] + a.y, acc[2] + a.z, acc[3] + a.w);
-    dst[1] = make_float4(acc[4] + b.x, acc[5] + b.y, acc[6] + b.z, acc[7] + b.w);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
