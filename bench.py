@@ -328,12 +328,18 @@ GEMM_SOURCES = ("moe_expert_layer_softmax_gb300/csrc/gemm.cu",
                 "moe_expert_layer_softmax_gb300/csrc/kernels.h")
 
 
-def gemm_source_hash() -> str:
+def gemm_source_hash(root: str = ROOT) -> str:
+    """sha256 of the GEMM sources with comments and whitespace removed (so that
+    only a change of the code itself invalidates a recorded ncu capture)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in GEMM_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(root, rel)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -2,28 +2,35 @@
 //
 // "Supercharging Olmo-core for Efficient and Scalable MoE Training", Abstract:
 // the expert GEMMs are grouped GEMMs scheduled on the device from routing
-// metadata that never leaves the GPU; the blog "Olmo-core 3: an open training
-// stack for trillion-parameter MoE" (section "Olmo-core 3's answer") adds that
+// metadata that never leaves the GPU; the article "Olmo-core 3: an open training
+// stack for trillion-parameter MoE" (section "Olmo-core 3's answer: experts
+// resident, data routed") adds that
 // they run the uneven per-expert shapes without padding to a common capacity.
 // Here each expert's rows are padded only to the 128-row tile, and the tile
 // schedule is read from the device-resident tile_offsets.
 //
-// Kernel structure (one persistent CTA per SM, 320 threads):
-//   warp 0     TMA producer: 128-byte-swizzled A/B tiles into a ring of as many
-//              stages as fit in 224 KB (4 for 128x256 bf16 tiles, up to 12 for
-//              the narrow router tile)
-//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
-//              (128 x N x 16 bf16 MMAs, fp32 accumulators in tensor memory,
-//              two 256-column accumulators so the epilogue of one tile
-//              overlaps the main loop of the next)
+// Kernel structure (persistent, one CTA per SM, 320 threads):
+//   warp 0     TMA producer: 128-byte-swizzled A/B tiles into a 192 KB ring
+//              (6 stages of 32 KB on CTA pairs, 4 of 48 KB on single CTAs,
+//              up to 12 for the narrow router tile, 6 of 33 KB for MXFP8)
+//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer (bf16 or
+//              block-scaled fp8 in, fp32 accumulators in tensor memory, two
+//              accumulators so the epilogue of one tile overlaps the main loop
+//              of the next)
 //   warps 2-9  epilogue, two warps per TMEM lane quarter (each takes half of
 //              the tile's columns): tcgen05.ld -> fused SwiGLU /
-//              SwiGLU-backward / bias / fp32 -> global stores
+//              SwiGLU-backward / fp32 / router math -> swizzled shared-memory
+//              staging -> TMA bulk stores (direct stores for the router and
+//              the MXFP8 epilogues)
+// CTA pairs (clusters of 2, the bf16 data GEMMs): one 256-row tile per pair
+// with tcgen05.mma.cta_group::2; each CTA stages its 128 A rows and half of B,
+// the even CTA issues the MMAs (see "CTA pairs" below).
 // Every wait is bounded (error word + abort flag); an aborted CTA waits for
 // its own copies in flight and frees its tensor memory before returning.
 //
 // Schedules:
-//   DENSE   (router)       tiles = ceil(T/128) x n_tiles, K = d
+//   DENSE   (router)       tiles = ceil(T/128) x n_tiles (x 2 K halves when the
+//                          row tiles fill at most half the SMs), K = d
 //   MGROUP  (fwd / dgrad)  tiles = tile_offsets[E] x n_tiles; a tile's expert is
 //                          found by binary search in tile_offsets
 //   KGROUP  (wgrad)        tiles = E x (M/128) x n_tiles, the K loop runs over
