@@ -425,14 +425,15 @@ int moe_build_mx_weights(const moe_shape_t* s, const void* w_gate, const void* w
   for (const void* p : ptrs) MOE_NONNULL_ALIGNED(p);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int E = s->n_experts, d = s->d_model, f = s->d_ff;
-  // forward cache: gate/up along d, interleaved in 64-row groups; down along f
-  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 1, w_gate, c->gu_q, c->gu_s, st, 64, 0));
-  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 1, w_up, c->gu_q, c->gu_s, st, 64, 64));
-  MOE_CUDA(launch_quantize_mxfp8(E, d, f, 1, w_down, c->down_q, c->down_s, st));
-  // data-gradient cache: the transposes, blocked along the other axis
-  MOE_CUDA(launch_quantize_mxfp8(E, d, f, 0, w_down, c->downT_q, c->downT_s, st));
-  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 0, w_gate, c->gateT_q, c->gateT_s, st));
-  MOE_CUDA(launch_quantize_mxfp8(E, f, d, 0, w_up, c->upT_q, c->upT_s, st));
+  // one pass per weight writes both caches: the forward cache (gate/up along d,
+  // interleaved in 64-row groups; down along f) and the data-gradient cache
+  // (the transposes, blocked along the other axis)
+  MOE_CUDA(launch_quantize_mxfp8_both(E, f, d, w_gate, 64, 0, c->gu_q, c->gu_s, c->gateT_q,
+                                      c->gateT_s, st));
+  MOE_CUDA(launch_quantize_mxfp8_both(E, f, d, w_up, 64, 64, c->gu_q, c->gu_s, c->upT_q,
+                                      c->upT_s, st));
+  MOE_CUDA(launch_quantize_mxfp8_both(E, d, f, w_down, 0, 0, c->down_q, c->down_s, c->downT_q,
+                                      c->downT_s, st));
   return MOE_OK;
 }
 

@@ -118,6 +118,11 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis, const void* src,
                                   uint8_t* q, uint8_t* sf, cudaStream_t s, int group = 0,
                                   int offset = 0);
+// Both orientations of [batch][rows, cols] bf16 in one pass: blocked along cols
+// (row interleave as above) and the transpose [cols, rows] blocked along rows.
+cudaError_t launch_quantize_mxfp8_both(int batch, int rows, int cols, const void* src, int group,
+                                       int offset, uint8_t* q_rows, uint8_t* sf_rows,
+                                       uint8_t* q_cols, uint8_t* sf_cols, cudaStream_t s);
 cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
                                   const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                   int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s);

@@ -94,6 +94,75 @@ __global__ void __launch_bounds__(kQThreads) quantize_cols_kernel(
       (uint8_t)(e + 127);
 }
 
+// Both orientations of a weight from one read: src [R, C] bf16 per matrix ->
+// (1) q_r [R, C] blocked along C (rows interleaved by `group`/`offset` as in
+// quantize_rows_kernel) and (2) q_c [C, R] blocked along R (the transpose, as
+// in quantize_cols_kernel).  Tile: 128 rows x 64 columns; for (1) a thread
+// holds 8 values of a row and 4 neighbouring lanes form one 32-value block.
+__global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
+    const __nv_bfloat16* __restrict__ src, int R, int C, int group, int offset,
+    uint8_t* __restrict__ q_r, uint8_t* __restrict__ s_r, uint8_t* __restrict__ q_c,
+    uint8_t* __restrict__ s_c) {
+  pdl_begin();
+  __shared__ __nv_bfloat16 tile[kTK][kTN];
+  const int mat = blockIdx.z;
+  const int k0 = blockIdx.y * kTK;
+  const int n0 = blockIdx.x * kTN;
+  const __nv_bfloat16* sm = src + (size_t)mat * R * C;
+  const int64_t out_rows = group > 0 ? 2 * (int64_t)R : R;
+  const int cb = C / 32;
+  uint4 raw[4];   // all four loads in flight before any is used
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int idx = threadIdx.x + u * kQThreads;
+    raw[u] = __ldg(reinterpret_cast<const uint4*>(sm + (size_t)(k0 + (idx >> 3)) * C + n0 +
+                                                   (idx & 7) * 8));
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int idx = threadIdx.x + u * kQThreads;
+    const int row = idx >> 3, col = (idx & 7) * 8;
+    *reinterpret_cast<uint4*>(&tile[row][col]) = raw[u];
+    float v[8];
+    unpack8(raw[u], v);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int sx = mx_scale_exp(amax);
+    const float inv = ldexpf(1.0f, -sx);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= inv;
+    const int64_t r = k0 + row;
+    const int64_t ro = group > 0 ? (r / group) * 2 * group + offset + r % group : r;
+    *reinterpret_cast<uint2*>(q_r + ((size_t)mat * out_rows + ro) * C + n0 + col) = e4m3x8(v);
+    if ((idx & 3) == 0)
+      s_r[(size_t)mat * out_rows * cb + sf_offset(ro, (n0 + col) / 32, cb)] = (uint8_t)(sx + 127);
+  }
+  __syncthreads();
+  // the transpose, blocked along R (as quantize_cols_kernel)
+  const int n = threadIdx.x & 63;
+  const int kb = threadIdx.x >> 6;
+  float v[32];
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] = __bfloat162float(tile[kb * 32 + j][n]);
+    amax = fmaxf(amax, fabsf(v[j]));
+  }
+  const int e = mx_scale_exp(amax);
+  const float inv = ldexpf(1.0f, -e);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] *= inv;
+  const size_t row_out = (size_t)n0 + n;
+  uint2* out = reinterpret_cast<uint2*>(q_c + (size_t)mat * C * R + row_out * R + k0 + kb * 32);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) out[u] = e4m3x8(v + 8 * u);
+  s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)row_out, (k0 / 32) + kb, R / 32)] =
+      (uint8_t)(e + 127);
+}
+
 // Warp per token: a lane holds 8 values of a 256-column chunk; 4 lanes form a
 // 32-value block.  Codes and scales go to all k expert rows; padding rows get
 // zero codes and scale byte 127 (2^0).
@@ -186,6 +255,16 @@ cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis,
     launch_pdl(quantize_cols_kernel, dim3(grid), dim3(kQThreads), 0, s, static_cast<const __nv_bfloat16*>(src), rows,
                                                     cols, q, sf);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp8_both(int batch, int rows, int cols, const void* src, int group,
+                                       int offset, uint8_t* q_rows, uint8_t* sf_rows,
+                                       uint8_t* q_cols, uint8_t* sf_cols, cudaStream_t s) {
+  dim3 grid((unsigned)(cols / kTN), (unsigned)(rows / kTK), (unsigned)batch);
+  launch_pdl(quantize_both_kernel, grid, dim3(kQThreads), 0, s,
+             static_cast<const __nv_bfloat16*>(src), rows, cols, group, offset, q_rows, sf_rows,
+             q_cols, sf_cols);
   return cudaGetLastError();
 }
 
