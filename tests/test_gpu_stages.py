@@ -190,3 +190,25 @@ def test_router_bwd(case):
     assert max_abs_rel(got, c["bwd"]["dW_router"]) <= 1e-4
     empty = np.where(c["fwd"]["counts"] == 0)[0]
     assert (got[empty] == 0).all()
+
+
+def test_profile_hook_times_each_launch(case):
+    """moe_profile_start/stop record one event pair per launch of the chosen GEMM only."""
+    c = case
+    m, dev, n = c["m"], c["dev"], c["n"]
+    Y = torch.empty(n, c["d"], dtype=torch.bfloat16, device=dev)
+    a0 = c["rows"](c["fwd"]["A"], c["f"])
+    w0 = c["to"]("w_down")
+    m.profile_start(m.GEMM_FWD2)
+    for _ in range(3):
+        m.grouped_gemm(c["s"], m.GEMM_FWD2, c["ws"], tile_offsets=c["tile_offsets"], a0=a0, w0=w0,
+                       out0=Y)
+    dXd = torch.empty(n, c["d"], dtype=torch.bfloat16, device=dev)   # another op: not timed
+    m.grouped_gemm(c["s"], m.GEMM_DGRAD1, c["ws"], tile_offsets=c["tile_offsets"],
+                   a0=c["rows"](c["bwd"]["dH"], c["f"]), a1=c["rows"](c["bwd"]["dU"], c["f"]),
+                   w0=c["to"]("w_gate"), w1=c["to"]("w_up"), out0=dXd)
+    ms, launches = m.profile_stop()
+    assert launches == 3 and ms > 0.0
+    ms2, launches2 = m.profile_stop()          # stopped: nothing more recorded
+    assert launches2 == 0 and ms2 == 0.0
+    assert max_abs_rel(f64(Y)[: c["used"]], c["fwd"]["Y"]) <= TOL
