@@ -290,6 +290,35 @@ def run_ours(args, cfg):
                 "kernel_launches_timed": kernel_launches, "peak_source": peak_note,
                 "algorithmic": f"{fl[dom] / 1e9:.1f} GFLOP per launch (useful flops, no tile padding)"}
 
+    # ---- per-layer recompute: the backward re-runs dispatch and both expert
+    # GEMMs, so the expert activations need not be kept from the forward
+    def step_recompute():
+        if mx:
+            m.build_mx_weights(s, wg, wu, wd, buf.mx_weights)
+        m.forward(buf, x, wr, bias, wg, wu, wd, out)
+        m.backward(buf, dO, x, wr, wg, wu, wd, recompute=True)
+
+    for _ in range(3):
+        step_recompute()
+    torch.cuda.synchronize()
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(args.steps):
+        step_recompute()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    rc_ms = max_over_ranks(r0.elapsed_time(r1) / args.steps, world)
+    rows = m.rows_max(s)
+    if mx:   # xd_q, a_q (+ 1/32 scales), H, U, Y
+        act_bytes = rows * ((cfg.d + cfg.f) * 33 // 32 + (2 * cfg.f + cfg.d) * 2)
+    else:    # Xd, H, U, A, Y in bf16
+        act_bytes = rows * (2 * cfg.d + 3 * cfg.f) * 2
+    recompute = {"value": job_value(world, cfg.T, rc_ms), "unit": UNIT, "ms_per_step": rc_ms,
+                 "activation_bytes_not_kept": int(act_bytes),
+                 "what": "backward re-runs dispatch, GEMM1 and GEMM2 from x and the routing "
+                         "metadata (per-layer recompute)"}
+
     # ---- end to end through the public API with host buffers
     e2e = end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, args.steps, world)
 
@@ -312,6 +341,7 @@ def run_ours(args, cfg):
                  "bf16_peak_tflops": peaks["bf16_tflops_sustained"]},
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
+        "recompute": recompute,
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:
@@ -324,8 +354,7 @@ def run_ours(args, cfg):
 
 GEMM_OP = {"fwd1": 0, "fwd2": 1, "dgrad2": 2, "dgrad1": 3, "wgrad2": 4, "wgrad1": 5}
 GEMM_SOURCES = ("moe_expert_layer_softmax_gb300/csrc/gemm.cu",
-                "moe_expert_layer_softmax_gb300/csrc/common.cuh",
-                "moe_expert_layer_softmax_gb300/csrc/kernels.h")
+                "moe_expert_layer_softmax_gb300/csrc/common.cuh")
 
 
 def gemm_source_hash(root: str = ROOT) -> str:

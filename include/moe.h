@@ -420,6 +420,12 @@ typedef struct {
   /* MXFP8 only (else NULL) */
   const moe_mx_weights_t* mx_weights;
   const moe_mx_buffers_t* mx;
+  /* 0: read the expert activations the forward saved.  1: recompute them
+   * first (dispatch -> FWD1_SWIGLU -> FWD2 from x and the saved routing
+   * metadata), so that saved->xd, h, u, a, y (MXFP8: mx->xd_q/xd_s, a_q/a_s)
+   * need not survive from the forward: the caller may reuse that memory in
+   * between.  Only x and the routing metadata must be kept. */
+  int32_t recompute;
 } moe_bwd_args_t;
 
 /* route -> dispatch -> FWD1_SWIGLU -> FWD2 -> combine, all on `stream`.
@@ -428,8 +434,12 @@ typedef struct {
 MOE_API int moe_layer_fwd(const moe_shape_t* shape, const moe_fwd_args_t* args, const moe_saved_t* saved,
                   void* ws, void* stream);
 
-/* combine_bwd -> DGRAD2_SWIGLU -> WGRAD2 -> DGRAD1 -> WGRAD1 -> dispatch_bwd
- * -> router_bwd, all on `stream`, reading what moe_layer_fwd saved.
+/* [recompute: dispatch -> FWD1_SWIGLU -> FWD2] -> combine_bwd -> DGRAD2_SWIGLU
+ * -> WGRAD2 -> DGRAD1 -> WGRAD1 -> dispatch_bwd -> router_bwd, all on `stream`,
+ * reading what moe_layer_fwd saved (per-layer recompute: the report's
+ * "Section 24: Conclusion", Evidence 11, trades repeated dispatch and expert
+ * compute for activation memory).  Recomputed values equal the saved ones bit
+ * for bit (the same deterministic kernels on the same inputs).
  * MXFP8 mode: dY is quantised after the combine backward, DGRAD2/DGRAD1 run on
  * MXFP8 (the second weight cache), and the weight gradients run in BF16 on
  * dequantised Xd and A. */

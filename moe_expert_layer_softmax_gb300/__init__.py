@@ -94,7 +94,8 @@ class FwdArgs(ctypes.Structure):
 class BwdArgs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("d_out", "x", "w_router", "w_gate", "w_up", "w_down", "dx",
                                    "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates",
-                                   "dlogits", "dy", "dh", "du", "dxd", "mx_weights", "mx")]
+                                   "dlogits", "dy", "dh", "du", "dxd", "mx_weights", "mx")] + \
+        [("recompute", ctypes.c_int32)]
 
 
 _lib = None
@@ -392,10 +393,15 @@ def forward(buf: LayerBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, ou
     layer_fwd(buf.shape, fa, buf.saved_struct(), buf.ws, stream)
 
 
-def backward(buf: LayerBuffers, d_out, x, w_router, w_gate, w_up, w_down, stream=None):
+def backward(buf: LayerBuffers, d_out, x, w_router, w_gate, w_up, w_down, stream=None,
+             recompute: bool = False):
+    """moe_layer_bwd.  recompute=True re-runs dispatch and both expert GEMMs
+    from x and the saved routing metadata instead of reading the saved
+    activations."""
     g = buf.grads
     mw, mb = buf.mx_structs()
     ba = BwdArgs(d_out=_ptr(d_out), x=_ptr(x), w_router=_ptr(w_router), w_gate=_ptr(w_gate),
                  w_up=_ptr(w_up), w_down=_ptr(w_down), mx_weights=mw, mx=mb,
+                 recompute=1 if recompute else 0,
                  **{k: _ptr(v) for k, v in g.items()})
     layer_bwd(buf.shape, ba, buf.saved_struct(), buf.ws, stream)

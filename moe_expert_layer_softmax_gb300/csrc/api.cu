@@ -257,6 +257,38 @@ const DeviceInfo* device_info() {
   return &g_dev[dev];
 }
 
+
+// dispatch -> FWD1_SWIGLU -> FWD2: the expert part of the forward, from x and
+// the routing metadata in `sv` (writes xd, h, u, a, y; in MXFP8 mode xd_q/xd_s
+// and a_q/a_s instead of xd and a).  The backward's recompute mode re-runs it.
+int expert_forward(const moe_shape_t* s, const void* x, const void* w_gate, const void* w_up,
+                   const void* w_down, const moe_mx_weights_t* w, const moe_mx_buffers_t* b,
+                   const moe_saved_t* sv, void* ws, cudaStream_t st) {
+  moe_gemm_args_t g = {};
+  if (s->prec == MOE_MXFP8) {
+    MOE_CUDA(launch_dispatch_mxfp8(x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
+                                   s->d_model, s->n_experts, s->top_k, b->xd_q, b->xd_s, st));
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = b->xd_q; g.sfa0 = b->xd_s; g.w0 = w->gu_q; g.sfb0 = w->gu_s;
+    g.out0 = sv->h; g.out1 = sv->u; g.out2 = b->a_q; g.osf0 = b->a_s;
+    MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
+    g = moe_gemm_args_t{};
+    g.tile_offsets = sv->tile_offsets;
+    g.a0 = b->a_q; g.sfa0 = b->a_s; g.w0 = w->down_q; g.sfb0 = w->down_s; g.out0 = sv->y;
+    return gemm_impl(s, MOE_GEMM_FWD2, &g, ws, st);
+  }
+  MOE_CUDA(launch_dispatch_bf16(x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
+                                s->d_model, s->n_experts, s->top_k, sv->xd, st));
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = sv->xd; g.w0 = w_gate; g.w1 = w_up;
+  g.out0 = sv->h; g.out1 = sv->u; g.out2 = sv->a;
+  MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
+  g = moe_gemm_args_t{};
+  g.tile_offsets = sv->tile_offsets;
+  g.a0 = sv->a; g.w0 = w_down; g.out0 = sv->y;
+  return gemm_impl(s, MOE_GEMM_FWD2, &g, ws, st);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -554,35 +586,7 @@ int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved
   MOE_TRY(route_impl(s, a->x, a->w_router, a->logit_bias, sv->logits, sv->topk_idx, sv->gates,
                      sv->counts, sv->offsets, sv->tile_offsets, sv->slot_of_route,
                      sv->route_of_slot, ws, st));
-  if (mx) {
-    const moe_mx_weights_t* w = a->mx_weights;
-    const moe_mx_buffers_t* b = a->mx;
-    MOE_CUDA(launch_dispatch_mxfp8(a->x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
-                                   s->d_model, s->n_experts, s->top_k, b->xd_q, b->xd_s, st));
-    moe_gemm_args_t g = {};
-    g.tile_offsets = sv->tile_offsets;
-    g.a0 = b->xd_q; g.sfa0 = b->xd_s; g.w0 = w->gu_q; g.sfb0 = w->gu_s;
-    g.out0 = sv->h; g.out1 = sv->u; g.out2 = b->a_q; g.osf0 = b->a_s;
-    MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
-    g = moe_gemm_args_t{};
-    g.tile_offsets = sv->tile_offsets;
-    g.a0 = b->a_q; g.sfa0 = b->a_s; g.w0 = w->down_q; g.sfb0 = w->down_s; g.out0 = sv->y;
-    MOE_TRY(gemm_impl(s, MOE_GEMM_FWD2, &g, ws, st));
-    MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->top_k,
-                            a->out, st));
-    return MOE_OK;
-  }
-  MOE_CUDA(launch_dispatch_bf16(a->x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
-                                s->d_model, s->n_experts, s->top_k, sv->xd, st));
-  moe_gemm_args_t g = {};
-  g.tile_offsets = sv->tile_offsets;
-  g.a0 = sv->xd; g.w0 = a->w_gate; g.w1 = a->w_up;
-  g.out0 = sv->h; g.out1 = sv->u; g.out2 = sv->a;
-  MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
-  g = moe_gemm_args_t{};
-  g.tile_offsets = sv->tile_offsets;
-  g.a0 = sv->a; g.w0 = a->w_down; g.out0 = sv->y;
-  MOE_TRY(gemm_impl(s, MOE_GEMM_FWD2, &g, ws, st));
+  MOE_TRY(expert_forward(s, a->x, a->w_gate, a->w_up, a->w_down, a->mx_weights, a->mx, sv, ws, st));
   MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->top_k, a->out,
                           st));
   return MOE_OK;
@@ -614,6 +618,10 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   MOE_NONNULL_ALIGNED(a->dxd);
   MOE_NONNULL_ALIGNED(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (a->recompute != 0 && a->recompute != 1) return MOE_ERR_INVALID;
+  if (a->recompute)
+    MOE_TRY(expert_forward(s, a->x, a->w_gate, a->w_up, a->w_down, a->mx_weights, a->mx, sv, ws,
+                           st));
   MOE_CUDA(launch_combine_bwd(a->d_out, sv->y, sv->gates, sv->topk_idx, sv->slot_of_route,
                               sv->counts, sv->tile_offsets, s->T, s->d_model, s->n_experts,
                               s->top_k, a->dy, a->d_gates, a->dlogits, st));

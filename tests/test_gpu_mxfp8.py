@@ -319,3 +319,28 @@ def test_mx_full_size_workload_sampled(moe_gpu):
         dYe = gsel[:, None] * dO[ros[a:b_] // cfg.k]
         dWd = dYe.T @ Aq
         assert max_abs_rel(f64(buf.grads["dw_down"][e]), dWd) <= TOL
+
+
+def test_mx_recompute_backward_is_bitwise_the_saved_one(mcase):
+    """MXFP8 recompute: the quantised Xd and A and the bf16 H, U, Y are rebuilt
+    from x; with them overwritten in between, the gradients are bit for bit
+    those of the saving backward."""
+    c = mcase
+    m, dev = c["m"], c["dev"]
+    buf, out, err = run_mx_layer(m, dev, c["inp"], c["k"], c["L32"])
+    assert err == 0
+    names = ("dx", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits")
+    saved_grads = {n: buf.grads[n].clone() for n in names}
+    for n in ("h", "u", "y"):
+        buf.saved[n].fill_(float("nan"))
+    for n in ("xd_q", "a_q"):
+        buf.mx[n].fill_(0x7F)          # E4M3 NaN codes
+    for n in ("xd_s", "a_s"):
+        buf.mx[n].fill_(0xFF)          # E8M0 NaN scale
+    for n in names:
+        buf.grads[n].fill_(float("nan"))
+    t = {nm: to_dev_bf16(c["inp"][nm], dev) for nm in ("x", "w_gate", "w_up", "w_down", "d_out")}
+    m.backward(buf, t["d_out"], t["x"], None, t["w_gate"], t["w_up"], t["w_down"], recompute=True)
+    assert m.read_error(buf.ws) == 0
+    for n in names:
+        assert torch.equal(buf.grads[n], saved_grads[n]), n
