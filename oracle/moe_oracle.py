@@ -34,6 +34,9 @@ plainest ones the pages support) are:
   row_offsets[e] = BM * (number of BM-row tiles of the experts before e); with
   BM = 1 this is the plain exclusive scan of the counts.  Within an expert,
   rows are in ascending route order (token t, then choice j);
+* load balancing (optional): the Switch-style scalar LBL = E * sum_e f_e P_e,
+  f_e = fraction of routes of expert e (hard counts, not differentiated),
+  P_e = mean full-softmax probability of expert e (Section 24.2, Evidence 9);
 * backward: the exact gradient for a fixed top-k selection (the selection
   itself is piecewise constant);
 * MXFP8: E4M3 values with one E8M0 (power-of-two) scale per 32 consecutive
@@ -326,13 +329,47 @@ def dispatch_backward(dXd, slot_of_route, T: int, k: int) -> np.ndarray:
     return dx
 
 
-def router_backward(d_gates, gates, topk_idx, E: int, x=None, w_router=None):
+def load_balance(logits, topk_idx, E: int):
+    """Switch-style load-balancing scalar of a top-k router.
+
+    "Section 24: Conclusion" of the report (Section 24.2, Evidence 9) describes
+    the Switch-style scalar as a cross-term between soft router scores and hard
+    expert counts.  Reading: the hard part is the fraction of routes each expert
+    receives, f_e = count_e / (T k); the soft part is the mean router
+    probability, P_e = mean over tokens of the softmax over all E experts; the
+    scalar is LBL = E * sum_e f_e P_e (1 when the scores are uniform).
+    Returns (LBL, P [E], f [E]).
+    """
+    L = as_f64(logits)
+    idx = np.asarray(topk_idx)
+    T, k = idx.shape
+    p = np.exp(L - L.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    f = np.bincount(idx.ravel(), minlength=E).astype(np.float64) / (T * k)
+    P = p.mean(axis=0)
+    return float(E * np.dot(f, P)), P, f
+
+
+def load_balance_dlogits(logits, topk_idx, E: int, coef: float) -> np.ndarray:
+    """d(coef * LBL)/dlogits, the counts held fixed (they are not differentiable):
+    coef * E / T * p[t, e] * (f_e - sum_e' f_e' p[t, e'])."""
+    L = as_f64(logits)
+    T = L.shape[0]
+    _, _, f = load_balance(L, topk_idx, E)
+    p = np.exp(L - L.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    s = p @ f
+    return coef * E / T * p * (f[None, :] - s[:, None])
+
+
+def router_backward(d_gates, gates, topk_idx, E: int, x=None, w_router=None, dlogits_extra=None):
     """Gradient through the renormalised softmax and the router projection.
 
     For the selected experts g_j = exp(l_j) / sum_sel exp(l_i), so
     dl_j = g_j * (dg_j - sum_i g_i dg_i); unselected logits get zero (the full
     softmax denominator cancels in the renormalisation).  With a router weight,
-    dx_router = dlogits W_r and dW_r = dlogits^T x.
+    dx_router = dlogits W_r and dW_r = dlogits^T x.  `dlogits_extra` (a dense
+    [T, E] term, e.g. the load-balancing loss's) is added to dlogits first.
     Returns dlogits [T, E] and, when W_r is given, (dx_router [T, d], dW_r [E, d]).
     """
     dg = as_f64(d_gates)
@@ -344,6 +381,8 @@ def router_backward(d_gates, gates, topk_idx, E: int, x=None, w_router=None):
     dlogits = np.zeros((T, E))
     for j in range(k):
         dlogits[np.arange(T), idx[:, j]] += dl_sel[:, j]
+    if dlogits_extra is not None:
+        dlogits = dlogits + as_f64(dlogits_extra)
     out = {"dlogits": dlogits}
     if w_router is not None:
         out["dx_router"] = dlogits @ as_f64(w_router)
@@ -381,8 +420,9 @@ def layer_forward(x, w_router, bias, w_gate, w_up, w_down, k: int, bm: int = 128
     }
 
 
-def layer_backward(fwd, d_out, x, w_router, w_gate, w_up, w_down):
-    """Backward of the layer for upstream gradient dOut [T, d]."""
+def layer_backward(fwd, d_out, x, w_router, w_gate, w_up, w_down, lb_coef: float = 0.0):
+    """Backward of the layer for upstream gradient dOut [T, d], plus lb_coef
+    times the load-balancing scalar's gradient when lb_coef is not 0."""
     T, k = fwd["topk_idx"].shape
     E = fwd["logits"].shape[1]
     n_rows = fwd["Xd"].shape[0]
@@ -390,8 +430,10 @@ def layer_backward(fwd, d_out, x, w_router, w_gate, w_up, w_down):
     g = expert_ffn_backward(dY, fwd["Xd"], fwd["H"], fwd["U"], fwd["A"], w_gate, w_up, w_down,
                             fwd["row_offsets"])
     dx = dispatch_backward(g["dXd"], fwd["slot_of_route"], T, k)
+    extra = (load_balance_dlogits(fwd["logits"], fwd["topk_idx"], E, lb_coef)
+             if lb_coef != 0.0 else None)
     rb = router_backward(d_gates, fwd["gates"], fwd["topk_idx"], E,
-                         x if w_router is not None else None, w_router)
+                         x if w_router is not None else None, w_router, extra)
     if w_router is not None:
         dx = dx + rb["dx_router"]
     out = {"d_gates": d_gates, "dY": dY, "dx": dx, "dlogits": rb["dlogits"]}
@@ -559,7 +601,7 @@ def layer_forward_mxfp8(x, w_router, bias, w_gate, w_up, w_down, k: int, bm: int
     }
 
 
-def layer_backward_mxfp8(fwd, d_out, x, w_router, w_gate, w_up, w_down):
+def layer_backward_mxfp8(fwd, d_out, x, w_router, w_gate, w_up, w_down, lb_coef: float = 0.0):
     """Backward with MXFP8 data-gradient GEMMs and BF16 weight-gradient GEMMs.
 
     The data-gradient GEMMs quantise their gradient operand along the
@@ -597,8 +639,10 @@ def layer_backward_mxfp8(fwd, d_out, x, w_router, w_gate, w_up, w_down):
         dWg[e] = dH[a:b].T @ Xd[a:b]
         dWu[e] = dU[a:b].T @ Xd[a:b]
     dx = dispatch_backward(dXd, fwd["slot_of_route"], T, k)
+    extra = (load_balance_dlogits(fwd["logits"], fwd["topk_idx"], E, lb_coef)
+             if lb_coef != 0.0 else None)
     rb = router_backward(d_gates, fwd["gates"], fwd["topk_idx"], E,
-                         x if w_router is not None else None, w_router)
+                         x if w_router is not None else None, w_router, extra)
     if w_router is not None:
         dx = dx + rb["dx_router"]
     out = {"d_gates": d_gates, "dY": dY, "dH": dH, "dU": dU, "dXd": dXd, "dx": dx,
