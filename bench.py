@@ -319,6 +319,33 @@ def run_ours(args, cfg):
                  "what": "backward re-runs dispatch, GEMM1 and GEMM2 from x and the routing "
                          "metadata (per-layer recompute)"}
 
+    # ---- with the load-balancing term: statistics in the forward, coef * LBL's
+    # gradient in the backward (dense router backward)
+    buf.saved["lb_stats"] = torch.empty(cfg.E + 1, dtype=torch.float32, device=dev)
+
+    def step_lb():
+        if mx:
+            m.build_mx_weights(s, wg, wu, wd, buf.mx_weights)
+        m.forward(buf, x, wr, bias, wg, wu, wd, out)
+        m.backward(buf, dO, x, wr, wg, wu, wd, lb_coef=0.01)
+
+    for _ in range(3):
+        step_lb()
+    torch.cuda.synchronize()
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(args.steps):
+        step_lb()
+    l1.record(stream)
+    torch.cuda.synchronize()
+    lb_ms = max_over_ranks(l0.elapsed_time(l1) / args.steps, world)
+    lb_line = {"value": job_value(world, cfg.T, lb_ms), "unit": UNIT, "ms_per_step": lb_ms,
+               "lbl": float(buf.saved["lb_stats"][0].item()), "coef": 0.01,
+               "what": "Switch-style load-balancing scalar in the forward and coef * its "
+                       "gradient in the backward (the router backward becomes dense)"}
+    buf.saved["lb_stats"] = None
+
     # ---- end to end through the public API with host buffers
     e2e = end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, args.steps, world)
 
@@ -341,7 +368,7 @@ def run_ours(args, cfg):
                  "bf16_peak_tflops": peaks["bf16_tflops_sustained"]},
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
-        "recompute": recompute,
+        "recompute": recompute, "load_balance": lb_line,
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:

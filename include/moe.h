@@ -347,6 +347,20 @@ MOE_API int moe_router_bwd(const moe_shape_t* shape, const void* x, const float*
                    const int32_t* route_of_slot, const int32_t* counts,
                    const int32_t* tile_offsets, float* dw_router, void* ws, void* stream);
 
+/* ------------------------------------------------------------ load balancing
+ * Switch-style load-balancing scalar of the router ("Supercharging Olmo-core
+ * for Efficient and Scalable MoE Training", Section 24.2, Evidence 9: a
+ * cross-term between soft router scores and hard expert counts):
+ *   f_e = counts[e] / (T k)                      hard, not differentiated
+ *   P_e = mean over tokens of softmax(logits[t])_e over all E experts
+ *   LBL = E * sum_e f_e P_e                      (1 for uniform scores)
+ *   lb_stats  fp32 [1 + E]: lb_stats[0] = LBL, lb_stats[1 + e] = P_e.
+ * Tokens with a non-finite logit add nothing to P.  Uses `ws` (sized by
+ * moe_workspace_size); deterministic (fixed-order sums, no atomics).  The
+ * gradient of coef * LBL enters through moe_bwd_args_t.lb_coef. */
+MOE_API int moe_load_balance(const moe_shape_t* shape, const float* logits, const int32_t* counts,
+                             float* lb_stats, void* ws, void* stream);
+
 /* ------------------------------------------------------------ whole layer
  * Buffers saved by the forward for the backward (all caller-owned, device).
  * Row buffers have rows_max rows (moe_rows_max). */
@@ -364,6 +378,8 @@ typedef struct {
   void* u;                /* bf16 [rows_max, f]                          */
   void* a;                /* bf16 [rows_max, f]                          */
   void* y;                /* bf16 [rows_max, d]                          */
+  float* lb_stats;        /* fp32 [1 + E] or NULL: the forward writes the
+                             load-balancing statistics here (moe_load_balance) */
 } moe_saved_t;
 
 /* MXFP8 activation buffers (rows_max rows; scales in the MOE_SF layout).
@@ -426,9 +442,14 @@ typedef struct {
    * need not survive from the forward: the caller may reuse that memory in
    * between.  Only x and the routing metadata must be kept. */
   int32_t recompute;
+  /* Coefficient of the load-balancing scalar in the loss (0: no such term).
+   * When not 0, coef * dLBL/dlogits is added to dlogits for every token and
+   * expert, and (with w_router) dx and dW_r take the dense router backward. */
+  float lb_coef;
 } moe_bwd_args_t;
 
-/* route -> dispatch -> FWD1_SWIGLU -> FWD2 -> combine, all on `stream`.
+/* route -> [load-balancing statistics into saved->lb_stats when it is not
+ * NULL] -> dispatch -> FWD1_SWIGLU -> FWD2 -> combine, all on `stream`.
  * MXFP8 mode: the dispatch quantises each token once (Xd_q), GEMM1/GEMM2 run
  * on the MXFP8 weight cache, saved->xd and saved->a are not used. */
 MOE_API int moe_layer_fwd(const moe_shape_t* shape, const moe_fwd_args_t* args, const moe_saved_t* saved,

@@ -42,7 +42,7 @@ EXPORTS = (
     "moe_route", "moe_dispatch", "moe_quantize_mxfp8", "moe_grouped_gemm", "moe_combine",
     "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
     "moe_route_noalloc", "moe_dequantize_mxfp8", "moe_build_mx_weights",
-    "moe_debug_inject_stall", "moe_profile_start", "moe_profile_stop",
+    "moe_debug_inject_stall", "moe_profile_start", "moe_profile_stop", "moe_load_balance",
 )
 
 
@@ -83,7 +83,7 @@ class MxBuffers(ctypes.Structure):
 class Saved(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("logits", "topk_idx", "gates", "counts", "offsets",
                                    "tile_offsets", "slot_of_route", "route_of_slot", "xd", "h",
-                                   "u", "a", "y")]
+                                   "u", "a", "y", "lb_stats")]
 
 
 class FwdArgs(ctypes.Structure):
@@ -95,7 +95,7 @@ class BwdArgs(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("d_out", "x", "w_router", "w_gate", "w_up", "w_down", "dx",
                                    "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates",
                                    "dlogits", "dy", "dh", "du", "dxd", "mx_weights", "mx")] + \
-        [("recompute", ctypes.c_int32)]
+        [("recompute", ctypes.c_int32), ("lb_coef", ctypes.c_float)]
 
 
 _lib = None
@@ -120,6 +120,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_read_error": [_vp, P(i32), _vp],
         "moe_debug_inject_stall": [i32],
         "moe_profile_start": [i32],
+        "moe_load_balance": [P(Shape), _vp, _vp, _vp, _vp, _vp],
         "moe_profile_stop": [_vp, _vp],
         "moe_route": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_route_noalloc": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
@@ -206,6 +207,12 @@ def debug_inject_stall(mode: int) -> int:
     if rc < 0:
         raise MoEError("moe_debug_inject_stall", rc)
     return rc
+
+
+def load_balance(s: Shape, logits, counts, lb_stats, ws, stream=None):
+    """moe_load_balance: lb_stats[0] = LBL, lb_stats[1 + e] = P_e."""
+    _check("moe_load_balance", load().moe_load_balance(ctypes.byref(s), _ptr(logits), _ptr(counts),
+                                                       _ptr(lb_stats), _ptr(ws), _stream(stream)))
 
 
 def profile_start(op: int):
@@ -335,8 +342,11 @@ class LayerBuffers:
         return ctypes.addressof(self._mxw), ctypes.addressof(self._mxb)
 
 
-def allocate(s: Shape, device=None, with_grads: bool = True) -> LayerBuffers:
-    """Allocate every buffer moe_layer_fwd / moe_layer_bwd need for shape `s`."""
+def allocate(s: Shape, device=None, with_grads: bool = True,
+             load_balance: bool = False) -> LayerBuffers:
+    """Allocate every buffer moe_layer_fwd / moe_layer_bwd need for shape `s`
+    (with load_balance, saved["lb_stats"] receives the forward's
+    load-balancing statistics)."""
     import torch
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     T, d, E, k, f = s.T, s.d_model, s.n_experts, s.top_k, s.d_ff
@@ -355,6 +365,7 @@ def allocate(s: Shape, device=None, with_grads: bool = True) -> LayerBuffers:
         "xd": None if mx else torch.empty(n, d, **bf), "h": torch.empty(n, f, **bf),
         "u": torch.empty(n, f, **bf), "a": None if mx else torch.empty(n, f, **bf),
         "y": torch.empty(n, d, **bf),
+        "lb_stats": torch.empty(E + 1, **f32) if load_balance else None,
     }
     grads = {}
     if with_grads:
@@ -394,14 +405,15 @@ def forward(buf: LayerBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, ou
 
 
 def backward(buf: LayerBuffers, d_out, x, w_router, w_gate, w_up, w_down, stream=None,
-             recompute: bool = False):
+             recompute: bool = False, lb_coef: float = 0.0):
     """moe_layer_bwd.  recompute=True re-runs dispatch and both expert GEMMs
     from x and the saved routing metadata instead of reading the saved
-    activations."""
+    activations; lb_coef adds lb_coef * LBL (the load-balancing scalar) to the
+    loss."""
     g = buf.grads
     mw, mb = buf.mx_structs()
     ba = BwdArgs(d_out=_ptr(d_out), x=_ptr(x), w_router=_ptr(w_router), w_gate=_ptr(w_gate),
                  w_up=_ptr(w_up), w_down=_ptr(w_down), mx_weights=mw, mx=mb,
-                 recompute=1 if recompute else 0,
+                 recompute=1 if recompute else 0, lb_coef=float(lb_coef),
                  **{k: _ptr(v) for k, v in g.items()})
     layer_bwd(buf.shape, ba, buf.saved_struct(), buf.ws, stream)

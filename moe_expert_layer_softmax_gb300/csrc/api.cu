@@ -2,6 +2,7 @@
 // layout, the stage calls and the whole-layer orchestration.  Every call only
 // enqueues kernels on the caller's stream; none waits for the GPU except
 // moe_read_error.  Declarations and documentation: include/moe.h.
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -51,7 +52,7 @@ int n_route_blocks(const moe_shape_t* s) {
 
 // Workspace: [error word | block histograms | route ranks | router-grad partials]
 struct WsLayout {
-  size_t hist, rank, partial, total;
+  size_t hist, rank, partial, lb, total;
 };
 WsLayout ws_layout(const moe_shape_t* s) {
   WsLayout w;
@@ -60,8 +61,12 @@ WsLayout ws_layout(const moe_shape_t* s) {
   off += align256((size_t)n_route_blocks(s) * s->n_experts * 4);
   w.rank = off;
   off += align256((size_t)s->T * s->top_k * 4);
-  w.partial = off;
-  off += align256((size_t)(rows_max_of(s) / kTileM) * s->d_model * 4);
+  w.partial = off;   // router-gradient partial sums: per row tile, or per token split (dense)
+  const size_t tiles = (size_t)(rows_max_of(s) / kTileM);
+  const size_t dense = (size_t)kRouterDenseSplits * s->n_experts;
+  off += align256((tiles > dense ? tiles : dense) * s->d_model * 4);
+  w.lb = off;        // load-balancing partial sums
+  off += align256((size_t)lb_partial_blocks(s->T) * s->n_experts * 4);
   w.total = off;
   return w;
 }
@@ -552,6 +557,20 @@ int moe_router_bwd(const moe_shape_t* s, const void* x, const float* dlogits,
   return MOE_OK;
 }
 
+int moe_load_balance(const moe_shape_t* s, const float* logits, const int32_t* counts,
+                     float* lb_stats, void* ws, void* stream) {
+  MOE_TRY(check_shape(s));
+  MOE_TRY(ready_or_error());
+  MOE_NONNULL_ALIGNED(logits);
+  MOE_NONNULL_ALIGNED(counts);
+  MOE_NONNULL_ALIGNED(lb_stats);
+  MOE_NONNULL_ALIGNED(ws);
+  const WsLayout w = ws_layout(s);
+  MOE_CUDA(launch_load_balance(logits, counts, s->T, s->n_experts, s->top_k, at<float>(ws, w.lb),
+                               lb_stats, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
 int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved_t* sv, void* ws,
                   void* stream) {
   MOE_TRY(check_shape(s));
@@ -586,6 +605,12 @@ int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved
   MOE_TRY(route_impl(s, a->x, a->w_router, a->logit_bias, sv->logits, sv->topk_idx, sv->gates,
                      sv->counts, sv->offsets, sv->tile_offsets, sv->slot_of_route,
                      sv->route_of_slot, ws, st));
+  if (sv->lb_stats != nullptr) {
+    MOE_ALIGNED_OR_NULL(sv->lb_stats);
+    const WsLayout w = ws_layout(s);
+    MOE_CUDA(launch_load_balance(sv->logits, sv->counts, s->T, s->n_experts, s->top_k,
+                                 at<float>(ws, w.lb), sv->lb_stats, st));
+  }
   MOE_TRY(expert_forward(s, a->x, a->w_gate, a->w_up, a->w_down, a->mx_weights, a->mx, sv, ws, st));
   MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->top_k, a->out,
                           st));
@@ -622,9 +647,13 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   if (a->recompute)
     MOE_TRY(expert_forward(s, a->x, a->w_gate, a->w_up, a->w_down, a->mx_weights, a->mx, sv, ws,
                            st));
+  // load-balancing term: coef * LBL's gradient joins dlogits (all experts)
+  if (!isfinite(a->lb_coef)) return MOE_ERR_INVALID;
+  const bool lb = a->lb_coef != 0.0f;
+  const float lb_scale = lb ? a->lb_coef * (float)s->n_experts / (float)s->T : 0.0f;
   MOE_CUDA(launch_combine_bwd(a->d_out, sv->y, sv->gates, sv->topk_idx, sv->slot_of_route,
                               sv->counts, sv->tile_offsets, s->T, s->d_model, s->n_experts,
-                              s->top_k, a->dy, a->d_gates, a->dlogits, st));
+                              s->top_k, a->dy, a->d_gates, a->dlogits, st, sv->logits, lb_scale));
   if (mx) {
     const moe_mx_weights_t* w = a->mx_weights;
     const moe_mx_buffers_t* b = a->mx;
@@ -672,10 +701,18 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   g.a0 = a->dh; g.a1 = a->du; g.aux0 = sv->xd; g.out0 = a->dw_gate; g.out1 = a->dw_up;
   MOE_TRY(gemm_impl(s, MOE_GEMM_WGRAD1, &g, ws, st));
   }
+  const WsLayout w = ws_layout(s);
+  if (lb && a->w_router != nullptr) {
+    // every logit carries gradient: the router backward is dense
+    MOE_CUDA(launch_dispatch_bwd_dense(a->dxd, sv->slot_of_route, a->dlogits, a->w_router, s->T,
+                                       s->d_model, s->n_experts, s->top_k, a->dx, st));
+    MOE_CUDA(launch_router_bwd_dense(a->x, a->dlogits, s->T, s->d_model, s->n_experts,
+                                     at<float>(ws, w.partial), a->dw_router, st));
+    return MOE_OK;
+  }
   MOE_CUDA(launch_dispatch_bwd(a->dxd, sv->slot_of_route, sv->topk_idx, a->dlogits, a->w_router,
                                s->T, s->d_model, s->n_experts, s->top_k, a->dx, st));
   if (a->w_router != nullptr) {
-    const WsLayout w = ws_layout(s);
     MOE_CUDA(launch_router_bwd(a->x, a->dlogits, sv->route_of_slot, sv->counts, sv->tile_offsets,
                                s->T, s->d_model, s->n_experts, s->top_k,
                                rows_max_of(s) / kTileM, at<float>(ws, w.partial), a->dw_router,

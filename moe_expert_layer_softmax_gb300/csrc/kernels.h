@@ -60,11 +60,27 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                const int32_t* topk_idx, const int32_t* slot_of_route,
                                const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                int E, int k, void* dy, float* d_gates, float* dlogits,
-                               cudaStream_t s);
+                               cudaStream_t s,
+                               const float* lb_logits = nullptr, float lb_scale = 0.0f);
 cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
                                 const int32_t* topk_idx, const float* dlogits,
                                 const void* w_router, int T, int d, int E, int k, void* dx,
                                 cudaStream_t s);
+// ---------------------------------------------------------------- load balancing
+// LBL = E * sum_e f_e P_e; lb_stats = [LBL, P_0 .. P_{E-1}]; `partial` holds
+// lb_partial_blocks(T) * E floats.
+int lb_partial_blocks(int T);
+cudaError_t launch_load_balance(const float* logits, const int32_t* counts, int T, int E, int k,
+                                float* partial, float* lb_stats, cudaStream_t s);
+// Dense router backward (every logit may carry gradient): dx = sum_j dXd[slot]
+// + dlogits . W_r, and dW_r = dlogits^T . x over kRouterDenseSplits token splits
+// (`partial` holds kRouterDenseSplits * E * d floats).
+constexpr int kRouterDenseSplits = 8;
+cudaError_t launch_dispatch_bwd_dense(const void* dxd, const int32_t* slot_of_route,
+                                      const float* dlogits, const void* w_router, int T, int d,
+                                      int E, int k, void* dx, cudaStream_t s);
+cudaError_t launch_router_bwd_dense(const void* x, const float* dlogits, int T, int d, int E,
+                                    float* partial, float* dw_router, cudaStream_t s);
 cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t* route_of_slot,
                               const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                               int E, int k, int64_t tiles_max, float* partial, float* dw_router,

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
     int E, int k, int token_blocks, uint4* __restrict__ dy, float* __restrict__ d_gates,
-    float* __restrict__ dlogits) {
+    float* __restrict__ dlogits, const float* __restrict__ lb_logits, float lb_scale) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nv = d / kVec;
@@ -198,6 +198,31 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
   const float my_dl = my_g * (my_dg - inner);
   if (lane < k) d_gates[(size_t)t * k + lane] = my_dg;
   if (dlogits != nullptr) {
+    // load-balancing term (lb_scale = coef * E / T): every logit gets
+    // lb_scale * p_e (f_e - sum_e' f_e' p_e'), f_e = counts[e] / (T k)
+    float lb_max = -INFINITY, lb_z = 0.0f, lb_s = 0.0f;
+    const float inv_rk = 1.0f / ((float)T * (float)k);
+    if (lb_scale != 0.0f) {
+      const float* row = lb_logits + (size_t)t * E;
+      for (int e0 = 0; e0 < E; e0 += 32)
+        if (e0 + lane < E) lb_max = fmaxf(lb_max, __ldg(row + e0 + lane));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        lb_max = fmaxf(lb_max, __shfl_xor_sync(0xffffffffu, lb_max, off));
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        if (e0 + lane < E) {
+          const float pe = expf(__ldg(row + e0 + lane) - lb_max);
+          lb_z += pe;
+          lb_s += pe * ((float)counts[e0 + lane] * inv_rk);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        lb_z += __shfl_xor_sync(0xffffffffu, lb_z, off);
+        lb_s += __shfl_xor_sync(0xffffffffu, lb_s, off);
+      }
+      lb_s /= lb_z;
+    }
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       float v = 0.0f;
@@ -205,6 +230,10 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
         const int id = __shfl_sync(0xffffffffu, my_id, j);
         const float dl = __shfl_sync(0xffffffffu, my_dl, j);
         if (id == e) v = dl;
+      }
+      if (lb_scale != 0.0f && e < E) {
+        const float pe = expf(__ldg(lb_logits + (size_t)t * E + e) - lb_max) / lb_z;
+        v += lb_scale * pe * ((float)counts[e] * inv_rk - lb_s);
       }
       if (e < E) dlogits[(size_t)t * E + e] = v;
     }
@@ -393,23 +422,23 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                const int32_t* topk_idx, const int32_t* slot_of_route,
                                const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                int E, int k, void* dy, float* d_gates, float* dlogits,
-                               cudaStream_t s) {
+                               cudaStream_t s, const float* lb_logits, float lb_scale) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (k <= 4)
     launch_pdl(combine_bwd_kernel<4>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s,
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
         slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-        dlogits);
+        dlogits, lb_logits, lb_scale);
   else if (k <= 8)
     launch_pdl(combine_bwd_kernel<8>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
         slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-        dlogits);
+        dlogits, lb_logits, lb_scale);
   else
     launch_pdl(combine_bwd_kernel<32>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
         slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-        dlogits);
+        dlogits, lb_logits, lb_scale);
   return cudaGetLastError();
 }
 
