@@ -63,7 +63,7 @@ WsLayout ws_layout(const moe_shape_t* s) {
   off += align256((size_t)s->T * s->top_k * 4);
   w.partial = off;   // router-gradient partial sums: per row tile, or per token split (dense)
   const size_t tiles = (size_t)(rows_max_of(s) / kTileM);
-  const size_t dense = (size_t)kRouterDenseSplits * s->n_experts;
+  const size_t dense = (size_t)kRouterDenseRows;
   off += align256((tiles > dense ? tiles : dense) * s->d_model * 4);
   w.lb = off;        // load-balancing partial sums
   off += align256((size_t)lb_partial_blocks(s->T) * s->n_experts * 4);

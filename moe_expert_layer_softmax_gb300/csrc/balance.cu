@@ -252,7 +252,7 @@ cudaError_t launch_dispatch_bwd_dense(const void* dxd, const int32_t* slot_of_ro
 
 cudaError_t launch_router_bwd_dense(const void* x, const float* dlogits, int T, int d, int E,
                                     float* partial, float* dw_router, cudaStream_t s) {
-  const int splits = kRouterDenseSplits;
+  const int splits = router_dense_splits(E);
   dim3 grid((unsigned)(d / kDenseCols), (unsigned)splits);
   launch_pdl(router_bwd_dense_partial_kernel, grid, dim3(256), 0, s,
              static_cast<const __nv_bfloat16*>(x), dlogits, T, d, E, splits, partial);

@@ -73,9 +73,13 @@ int lb_partial_blocks(int T);
 cudaError_t launch_load_balance(const float* logits, const int32_t* counts, int T, int E, int k,
                                 float* partial, float* lb_stats, cudaStream_t s);
 // Dense router backward (every logit may carry gradient): dx = sum_j dXd[slot]
-// + dlogits . W_r, and dW_r = dlogits^T . x over kRouterDenseSplits token splits
-// (`partial` holds kRouterDenseSplits * E * d floats).
-constexpr int kRouterDenseSplits = 8;
+// + dlogits . W_r, and dW_r = dlogits^T . x over router_dense_splits(E) token
+// splits (`partial` holds kRouterDenseRows * d floats: splits * E <= 1024).
+constexpr int kRouterDenseRows = 1024;
+inline int router_dense_splits(int E) {
+  const int s = kRouterDenseRows / E;
+  return s < 1 ? 1 : (s > 32 ? 32 : s);
+}
 cudaError_t launch_dispatch_bwd_dense(const void* dxd, const int32_t* slot_of_route,
                                       const float* dlogits, const void* w_router, int T, int d,
                                       int E, int k, void* dx, cudaStream_t s);
