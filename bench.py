@@ -346,6 +346,13 @@ def run_ours(args, cfg):
                        "gradient in the backward (the router backward becomes dense)"}
     buf.saved["lb_stats"] = None
 
+    # ---- two-batch overlap on one GPU: the batch split in halves whose fwd+bwd
+    # run on two streams, against the same halves one after the other
+    tbo = None
+    if not mx and cfg.T % 2 == 0:
+        tbo = two_batch_overlap(m, cfg, x, wr, bias, wg, wu, wd, dO, dev, stream, args.steps,
+                                world)
+
     # ---- end to end through the public API with host buffers
     e2e = end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, args.steps, world)
 
@@ -368,7 +375,7 @@ def run_ours(args, cfg):
                  "bf16_peak_tflops": peaks["bf16_tflops_sustained"]},
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
-        "recompute": recompute, "load_balance": lb_line,
+        "recompute": recompute, "load_balance": lb_line, "two_batch_overlap": tbo,
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:
@@ -535,6 +542,59 @@ def stage_times_mx(m, buf, s, x, wr, bias, wg, wu, wd, dO, out, stream, reps):
     torch.cuda.synchronize()
     return {name: sum(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps)) / reps
             for i, (name, _) in enumerate(calls)}
+
+
+def two_batch_overlap(m, cfg, x, wr, bias, wg, wu, wd, dO, dev, stream, steps, world):
+    """The step's tokens in two halves, each a whole layer fwd+bwd with its own
+    buffers: (a) on two streams at once, (b) one after the other on one stream."""
+    import torch
+    h = cfg.T // 2
+    s2 = m.shape(h, cfg.d, cfg.E, cfg.k, cfg.f)
+    bufs = [m.allocate(s2) for _ in range(2)]
+    outs = [torch.empty(h, cfg.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    xs = [x[:h], x[h:]]
+    ds = [dO[:h], dO[h:]]
+    bs = [bias[:h], bias[h:]] if bias is not None else [None, None]
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    fork = torch.cuda.Event()
+    joins = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def half(i, st):
+        m.forward(bufs[i], xs[i], wr, bs[i], wg, wu, wd, outs[i], stream=st)
+        m.backward(bufs[i], ds[i], xs[i], wr, wg, wu, wd, stream=st)
+
+    def step_overlap():
+        fork.record(stream)
+        for i in range(2):
+            streams[i].wait_event(fork)
+            with torch.cuda.stream(streams[i]):
+                half(i, streams[i])
+            joins[i].record(streams[i])
+        for i in range(2):
+            stream.wait_event(joins[i])
+
+    def step_serial():
+        for i in range(2):
+            half(i, stream)
+
+    res = {}
+    for name, fn in (("overlapped", step_overlap), ("serial", step_serial)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+        res[name] = {"value": job_value(world, cfg.T, ms), "ms_per_step": ms}
+    res["unit"] = UNIT
+    res["what"] = (f"two halves of {h} tokens per step, each a whole layer fwd+bwd: on two "
+                   "streams at once vs one after the other")
+    return res
 
 
 def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world):
