@@ -27,19 +27,23 @@
  * without conversion); the blog "Olmo-core 3: an open training stack for
  * trillion-parameter MoE", section "Olmo-core 3's answer: experts resident,
  * data routed" (grouped GEMM over uneven per-expert shapes without padding to a
- * common capacity).  The pages do not write the layer's arithmetic out; the
- * readings taken (softmax/top-k/renormalisation, bias-free SwiGLU experts, gate
- * applied in the combine) are listed with each call.
+ * common capacity); Section 24.2 / Evidence 9 (the Switch-style load-balancing
+ * scalar) and Section 24.3 / Evidence 11 (per-layer recompute).  The pages do
+ * not write the layer's arithmetic out; the readings taken (softmax/top-k/
+ * renormalisation, bias-free SwiGLU experts, gate applied in the combine) are
+ * listed with each call.
  *
  * Conventions for every call
  *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
  *     The library never allocates or frees device memory on these paths and
- *     keeps no state between calls except what moe_init() caches per device.
+ *     keeps no state between calls except what moe_init() caches per device
+ *     (and the CUDA events of the timing hook, created on its first use).
  *   - bf16 tensors are raw 16-bit patterns; all matrices are row-major and
  *     contiguous.  Every device pointer must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void*; all work is enqueued on it and
- *     no call waits for the GPU (except moe_read_error).  The calls can be
- *     captured into a CUDA graph.
+ *     no call waits for the GPU (except moe_read_error and moe_profile_stop).
+ *     moe_layer_fwd / moe_layer_bwd (and the stage calls they are built from)
+ *     can be captured into a CUDA graph.
  *   - Return value: MOE_OK (0), or a negative MOE_ERR_* code from host-side
  *     argument validation (nothing is enqueued then) or from a failed launch.
  *   - Conditions found on the device (a non-finite logit, a bounded wait that
@@ -107,7 +111,8 @@ MOE_API int moe_init(int device);
 MOE_API int moe_rows_max(const moe_shape_t* shape, int64_t* rows_max);
 
 /* Bytes of scratch workspace `ws` that the calls below need (error word,
- * per-block histograms, per-route ranks).  Pure host arithmetic. */
+ * per-block histograms, per-route ranks, router-gradient and load-balancing
+ * partial sums).  Pure host arithmetic. */
 MOE_API int moe_workspace_size(const moe_shape_t* shape, size_t* ws_bytes);
 
 /* Zero the device error word in `ws` (enqueued on `stream`). */
@@ -133,7 +138,7 @@ MOE_API int moe_profile_start(int32_t op);
 MOE_API int moe_profile_stop(float* total_ms, int32_t* launches);
 
 /* Synchronise `stream`, then copy the error word to *code.  Diagnostics only:
- * the one call that waits for the GPU. */
+ * with moe_profile_stop, the only call that waits for the GPU. */
 MOE_API int moe_read_error(const void* ws, int32_t* code, void* stream);
 
 /* ------------------------------------------------------------ routing (a1-a3)
