@@ -534,83 +534,46 @@ MOE_DEV void mx_store32(const uint32_t* bits, uint8_t* codes, uint8_t* sf_byte) 
 }
 
 // Columns [c0, c1) of the tile, 32 at a time.
+MOE_DEV void epilogue_router(const Params& p, const TileInfo& ti, int r, uint32_t tb, int c0,
+                             int c1, uint32_t* v) {
+  // EPI_ROUTER: fp32 logits (+ bias), rows < T and columns < E only
+  // With the K loop split in two, each part adds its sum into the zeroed
+  // logits (the first part with the bias): (0 + a) + b == (0 + b) + a, so the
+  // result does not depend on which part lands first.
+  const int64_t row = (int64_t)ti.m_tile * kTileM + r;
+  float* out = static_cast<float*>(p.out0);
+  const bool add_bias = p.bias != nullptr && ti.kb == 0;
+  for (int c = c0; c < c1; c += 32) {
+    tmem_ld32(tb + c, v);      // warp-collective: executed by every lane
+    if (row < p.m_valid) {
+      for (int i = 0; i < 32 && c + i < p.n_valid; ++i) {
+        float val = __uint_as_float(v[i]);
+        if (add_bias) val += p.bias[row * p.n_valid + c + i];
+        if (p.k_parts > 1)
+          atomicAdd(out + row * p.n_valid + c + i, val);
+        else
+          out[row * p.n_valid + c + i] = val;
+      }
+    }
+  }
+}
+
+// Direct-store epilogues: the router (bf16 kernels) and every MXFP8 epilogue;
+// each instantiation compiles only the branches it can reach (register
+// pressure at the 168-register cap).
+template <bool MX>
 MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t tb, int c0, int c1) {
   uint32_t v[32];
+  if (!MX) {
+    epilogue_router(p, ti, r, tb, c0, c1, v);
+    return;
+  }
   if (p.epi == EPI_BF16) {
     const int64_t row = (int64_t)ti.m_tile * kTileM + r;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) + row * p.ldo + (int64_t)ti.n_tile * p.BN;
     for (int c = c0; c < c1; c += 32) {
       tmem_ld32(tb + c, v);
       store_bf16x32(out + c, v);
-    }
-  } else if (p.epi == EPI_SWIGLU_FWD) {
-    // accumulator columns [0, 128) are H, [128, 256) are U for the same f range
-    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
-    const int64_t off = row * p.ldo + (int64_t)ti.n_tile * 128;
-    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) + off;
-    __nv_bfloat16* U = static_cast<__nv_bfloat16*>(p.out1) + off;
-    __nv_bfloat16* A = static_cast<__nv_bfloat16*>(p.out2) + off;
-    uint32_t w[32];
-    for (int c = c0; c < c1; c += 32) {
-      tmem_ld32x2(tb + c, tb + 128 + c, v, w);
-      uint32_t a[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float h = __uint_as_float(v[i]);
-        const float u = __uint_as_float(w[i]);
-        a[i] = __float_as_uint(silu_f(h) * u);
-      }
-      store_bf16x32(H + c, v);
-      store_bf16x32(U + c, w);
-      store_bf16x32(A + c, a);
-    }
-  } else if (p.epi == EPI_SWIGLU_BWD) {
-    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
-    const int64_t off = row * p.ldo + (int64_t)ti.n_tile * p.BN;
-    const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
-    const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
-    __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(p.out0) + off;
-    __nv_bfloat16* dU = static_cast<__nv_bfloat16*>(p.out1) + off;
-    // the H/U loads of the next 32 columns are issued before this chunk's math
-    uint4 hn[4], un[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      hn[q] = H[c0 / 8 + q];
-      un[q] = U[c0 / 8 + q];
-    }
-    for (int c = c0; c < c1; c += 32) {
-      uint4 hc[4], uc[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        hc[q] = hn[q];
-        uc[q] = un[q];
-      }
-      if (c + 32 < c1) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          hn[q] = H[(c + 32) / 8 + q];
-          un[q] = U[(c + 32) / 8 + q];
-        }
-      }
-      tmem_ld32(tb + c, v);
-      uint32_t gh[32], gu[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float h[8], u[8];
-        unpack8(hc[q], h);
-        unpack8(uc[q], u);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float da = __uint_as_float(v[8 * q + i]);
-          const float sg = sigmoid_f(h[i]);
-          const float si = h[i] * sg;
-          const float ds = sg * (1.0f + h[i] * (1.0f - sg));
-          gh[8 * q + i] = __float_as_uint(da * u[i] * ds);
-          gu[8 * q + i] = __float_as_uint(da * si);
-        }
-      }
-      store_bf16x32(dH + c, gh);
-      store_bf16x32(dU + c, gu);
     }
   } else if (p.epi == EPI_SWIGLU_FWD_MX) {
     // accumulator columns [0, 64) are H, [64, 128) are U for f columns n_tile*64 + [0, 64)
@@ -670,44 +633,6 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
       const size_t so = sf_offset(row, (fc + c) / 32, p.osf_kb);
       mx_store32(gh, dHq + c, p.osf0 + so);
       mx_store32(gu, dUq + c, p.osf1 + so);
-    }
-  } else if (p.epi == EPI_F32) {
-    const bool hi = ti.m_tile >= p.m_split;
-    float* out = static_cast<float*>(hi ? p.out1 : p.out0) + (int64_t)ti.e * p.out_group_stride +
-                 ((int64_t)(ti.m_tile - (hi ? p.m_split : 0)) * kTileM + r) * p.ldo +
-                 (int64_t)ti.n_tile * p.BN;
-    for (int c = c0; c < c1; c += 32) {
-      float4* d4 = reinterpret_cast<float4*>(out + c);
-      if (ti.ks == 0) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) d4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        tmem_ld32(tb + c, v);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-      }
-    }
-  } else {  // EPI_ROUTER: fp32 logits (+ bias), rows < T and columns < E only
-    // With the K loop split in two, each part adds its sum into the zeroed
-    // logits (the first part with the bias): (0 + a) + b == (0 + b) + a, so the
-    // result does not depend on which part lands first.
-    const int64_t row = (int64_t)ti.m_tile * kTileM + r;
-    float* out = static_cast<float*>(p.out0);
-    const bool add_bias = p.bias != nullptr && ti.kb == 0;
-    for (int c = c0; c < c1; c += 32) {
-      tmem_ld32(tb + c, v);      // warp-collective: executed by every lane
-      if (row < p.m_valid) {
-        for (int i = 0; i < 32 && c + i < p.n_valid; ++i) {
-          float val = __uint_as_float(v[i]);
-          if (add_bias) val += p.bias[row * p.n_valid + c + i];
-          if (p.k_parts > 1)
-            atomicAdd(out + row * p.n_valid + c + i, val);
-          else
-            out[row * p.n_valid + c + i] = val;
-        }
-      }
     }
   }
 }
@@ -893,7 +818,7 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
   }
 }
 
-template <bool PAIR>
+template <bool MX, bool PAIR>
 MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                       uint8_t* stage_out, const CUtensorMap* tO0, const CUtensorMap* tO1,
                       const CUtensorMap* tO2, int rank) {
@@ -933,10 +858,10 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     tc_fence_after();
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
     if (valid) {
-      if (p.tma_store)
+      if (!MX && p.tma_store)
         epilogue_tile_tma(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
       else
-        epilogue_tile(p, ti, r, tb, c0, c1);
+        epilogue_tile<MX>(p, ti, r, tb, c0, c1);
     }
     tc_fence_before();
     if (PAIR)
@@ -1036,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_issuer<MX>(p, s, ring, tmem_base);
     }
   } else {
-    epilogue<PAIR>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
+    epilogue<MX, PAIR>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
   }
 
   tc_fence_before();
