@@ -353,6 +353,9 @@ def run_ours(args, cfg):
         tbo = two_batch_overlap(m, cfg, x, wr, bias, wg, wu, wd, dO, dev, stream, args.steps,
                                 world)
 
+    # ---- MXFP8 weight gradient on the natural layout vs dequantise + BF16
+    mxw = mx_wgrad_variants(m, dev, stream) if not args.no_extras else None
+
     # ---- end to end through the public API with host buffers
     e2e = end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, args.steps, world)
 
@@ -376,6 +379,7 @@ def run_ours(args, cfg):
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
         "recompute": recompute, "load_balance": lb_line, "two_batch_overlap": tbo,
+        "mx_wgrad": mxw,
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:
@@ -597,6 +601,68 @@ def two_batch_overlap(m, cfg, x, wr, bias, wg, wu, wd, dO, dev, stream, steps, w
     return res
 
 
+def mx_wgrad_variants(m, dev, stream, sizes=(2048, 4096, 8192), rows=16384, E=8, reps=10):
+    """The down-projection weight gradient dW[e] = dY_e^T A_e (K = N = d = f) on
+    an MXFP8 activation operand, 16384 rows over 8 experts of 2048 rows: the
+    natural-layout kernel (codes dequantised inside the GEMM) against the global
+    dequantisation followed by the BF16 grouped GEMM.  L2 is flushed before each
+    timed launch."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    res = {}
+    for K in sizes:
+        s = m.shape(rows // 4, K, E, 4, K, prec=m.MXFP8)
+        n = m.rows_max(s)
+        tiles = rows // E // 128
+        to = torch.arange(E + 1, dtype=torch.int32, device=dev) * tiles
+        ws = torch.zeros(m.workspace_size(s), dtype=torch.uint8, device=dev)
+        dY = torch.zeros(n, K, dtype=torch.bfloat16, device=dev)
+        A = torch.zeros(n, K, dtype=torch.bfloat16, device=dev)
+        dY[:rows].normal_(generator=g)
+        A[:rows].normal_(generator=g)
+        Aq = torch.empty(n, K, dtype=torch.uint8, device=dev)
+        As = torch.empty(n * K // 32, dtype=torch.uint8, device=dev)
+        m.quantize_mxfp8(1, n, K, 1, A, Aq, As, stream=stream)
+        del A
+        Adq = torch.empty(n, K, dtype=torch.bfloat16, device=dev)
+        dW = torch.empty(E, K, K, dtype=torch.float32, device=dev)
+        arms = {
+            "natural": lambda: m.grouped_gemm(s, m.GEMM_WGRAD2_NATURAL, ws, stream=stream,
+                                              tile_offsets=to, a0=dY, a1=Aq, sfb0=As, out0=dW),
+            "dq_bf16": lambda: (m.dequantize_mxfp8(n, K, Aq, As, Adq, stream=stream),
+                                m.grouped_gemm(s, m.GEMM_WGRAD2, ws, stream=stream,
+                                               tile_offsets=to, a0=dY, a1=Adq, out0=dW)),
+            "bf16_gemm_alone": lambda: m.grouped_gemm(s, m.GEMM_WGRAD2, ws, stream=stream,
+                                                      tile_offsets=to, a0=dY, a1=Adq, out0=dW),
+        }
+        row = {}
+        for name, fn in arms.items():
+            for _ in range(3):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            with torch.cuda.stream(stream):
+                for e0, e1 in ev:
+                    flush.fill_(1)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+            torch.cuda.synchronize()
+            ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / reps
+            row[name + "_ms"] = round(ms, 5)
+            row[name + "_tflops"] = round(2.0 * rows * K * K / (ms / 1000.0) / 1e12, 1)
+        if m.read_error(ws) != 0:
+            raise RuntimeError("device error word set in the MXFP8 weight-gradient comparison")
+        res[str(K)] = row
+        del dY, Aq, As, Adq, dW, ws
+    res["what"] = (f"dW_down weight gradient, K = N, {rows} rows over {E} experts: natural "
+                   "MXFP8 layout dequantised inside the GEMM vs global dequantisation + BF16 "
+                   "grouped GEMM (and that GEMM alone)")
+    return res
+
+
 def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world):
     """Same step through the public API, with the step's inputs (x, dOut) copied
     from pinned host memory and its results (out, dx) copied back, every step.
@@ -689,6 +755,8 @@ def main(argv=None):
     ap.add_argument("--config", default="fine_grained")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the MXFP8 weight-gradient comparison")
     args = ap.parse_args(argv)
     from synth import CONFIGS
     cfg = CONFIGS[args.config]

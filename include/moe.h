@@ -281,7 +281,9 @@ typedef enum {
   MOE_GEMM_DGRAD2_SWIGLU = 2,
   MOE_GEMM_DGRAD1 = 3,
   MOE_GEMM_WGRAD2 = 4,
-  MOE_GEMM_WGRAD1 = 5
+  MOE_GEMM_WGRAD1 = 5,
+  MOE_GEMM_WGRAD2_NATURAL = 6,
+  MOE_GEMM_WGRAD1_NATURAL = 7
 } moe_gemm_op_t;
 
 typedef struct {
@@ -315,7 +317,24 @@ typedef struct {
  *                 aux0 = H, aux1 = U (bf16)                out2 = dH_q, out3 = dU_q, osf0/osf1
  *   DGRAD1        a0 = dH_q, a1 = dU_q; w0 = gateT_q,      out0 = dXd (bf16)
  *                 w1 = upT_q
- * WGRAD1/WGRAD2 stay BF16 (on dequantised activations, moe_dequantize_mxfp8). */
+ * WGRAD1/WGRAD2 stay BF16 (on dequantised activations, moe_dequantize_mxfp8).
+ *
+ * Weight gradients on the forward's natural MXFP8 layout ("MXFP8 Wgrad",
+ * Section 24.2, Evidence 7 / Table 33 of "Supercharging Olmo-core for
+ * Efficient and Scalable MoE Training": a weight-gradient kernel that keeps
+ * the row-wise scales instead of converting the operand first).  The
+ * activation operand is given as the uint8 E4M3 codes the forward produced
+ * (one E8M0 scale per 32 columns of a row, MOE_SF layout, in sfb0) and is
+ * dequantised inside the GEMM; the other operand stays bf16.  Either precision
+ * mode:
+ *   WGRAD2_NATURAL  a0 = dY [rows,d] bf16, a1 = A_q [rows,f], sfb0 = A's scales
+ *                   out0 = dW_down fp32 [E,d,f]        (d, f multiples of 256)
+ *   WGRAD1_NATURAL  a0 = dH, a1 = dU [rows,f] bf16, aux0 = Xd_q [rows,d],
+ *                   sfb0 = Xd's scales; out0 = dW_gate, out1 = dW_up fp32 [E,f,d]
+ *                   (d a multiple of 256)
+ * The result is bit for bit that of moe_dequantize_mxfp8 followed by
+ * WGRAD2/WGRAD1 on the dequantised copy (same bf16 values, same MMA order).
+ * Other shapes return MOE_ERR_INVALID. */
 
 MOE_API int moe_grouped_gemm(const moe_shape_t* shape, int32_t op, const moe_gemm_args_t* args,
                      void* ws, void* stream);

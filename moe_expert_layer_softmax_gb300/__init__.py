@@ -27,6 +27,8 @@ GEMM_DGRAD2_SWIGLU = 2
 GEMM_DGRAD1 = 3
 GEMM_WGRAD2 = 4
 GEMM_WGRAD1 = 5
+GEMM_WGRAD2_NATURAL = 6   # activation operand as MXFP8 codes + scales, dequantised in the kernel
+GEMM_WGRAD1_NATURAL = 7
 
 DEVERR_NONFINITE_LOGIT = 0x1
 DEVERR_TIMEOUT = 0x2

@@ -152,6 +152,8 @@ int gemm_impl(const moe_shape_t* s, int op, const moe_gemm_args_t* a, void* ws, 
       default: break;   // weight gradients stay BF16
     }
   }
+  if (op == MOE_GEMM_WGRAD2_NATURAL) g.op = OP_WGRAD2_NAT;
+  if (op == MOE_GEMM_WGRAD1_NATURAL) g.op = OP_WGRAD1_NAT;
   g.sfa0 = a->sfa0; g.sfa1 = a->sfa1; g.sfb0 = a->sfb0; g.sfb1 = a->sfb1;
   g.out3 = a->out3; g.osf0 = a->osf0; g.osf1 = a->osf1;
   g.T = s->T; g.d = s->d_model; g.E = s->n_experts; g.f = s->d_ff;
@@ -247,6 +249,14 @@ int check_gemm_args(int op, const moe_gemm_args_t* a) {
     case MOE_GEMM_WGRAD1:
       MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->a1); MOE_NONNULL_ALIGNED(a->aux0);
       MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1);
+      break;
+    case MOE_GEMM_WGRAD2_NATURAL:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->a1); MOE_NONNULL_ALIGNED(a->sfb0);
+      MOE_NONNULL_ALIGNED(a->out0);
+      break;
+    case MOE_GEMM_WGRAD1_NATURAL:
+      MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->a1); MOE_NONNULL_ALIGNED(a->aux0);
+      MOE_NONNULL_ALIGNED(a->sfb0); MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1);
       break;
     default:
       return MOE_ERR_INVALID;
@@ -482,6 +492,12 @@ int moe_grouped_gemm(const moe_shape_t* s, int32_t op, const moe_gemm_args_t* ar
     MOE_TRY(check_gemm_args_mx(op, args));
   else
     MOE_TRY(check_gemm_args(op, args));
+  if (op == MOE_GEMM_WGRAD2_NATURAL &&
+      !natural_wgrad_supported(OP_WGRAD2_NAT, s->d_model, s->d_ff))
+    return MOE_ERR_INVALID;
+  if (op == MOE_GEMM_WGRAD1_NATURAL &&
+      !natural_wgrad_supported(OP_WGRAD1_NAT, s->d_model, s->d_ff))
+    return MOE_ERR_INVALID;
   MOE_NONNULL_ALIGNED(ws);
   return gemm_impl(s, op, args, ws, static_cast<cudaStream_t>(stream));
 }

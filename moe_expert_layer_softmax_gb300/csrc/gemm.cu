@@ -25,6 +25,9 @@
 // CTA pairs (clusters of 2, the bf16 data GEMMs): one 256-row tile per pair
 // with tcgen05.mma.cta_group::2; each CTA stages its 128 A rows and half of B,
 // the even CTA issues the MMAs (see "CTA pairs" below).
+// Weight gradients on the natural MXFP8 layout (the third template flag): B
+// arrives as E4M3 codes + scale atoms and 8 more warps (converters) write the
+// dequantised bf16 B tile for each stage; 576 threads.
 // Every wait is bounded (error word + abort flag); an aborted CTA waits for
 // its own copies in flight and frees its tensor memory before returning.
 //
@@ -65,12 +68,32 @@ constexpr int kEpiThreads = 256;
 constexpr int kMaxE = 256;
 constexpr uint32_t kTmemCols = 512;           // two 256-column fp32 accumulators
 
+// Weight gradients whose B operand stays in the forward's MXFP8 layout (codes
+// with one E8M0 scale per 32 columns of a row) and is dequantised inside the
+// kernel: each ring stage holds the TMA-loaded A tile, 64 rows x 128 codes of
+// B and the 512-byte scale atom covering them; converter warps write the bf16
+// B tile into one of kDqSlots slots after the stages, in the 128-byte-swizzled
+// M/N-major layout a TMA load of the dequantised tensor would have produced.
+constexpr int kConvWarps = 8;
+constexpr int kThreadsDq = kThreads + 32 * kConvWarps;
+constexpr int kDqRawBytes = kBK * 128;                // 64 rows x 128 E4M3 codes
+constexpr int kDqStageBytes = 25 * 1024;              // A + codes + scale atom, 1 KB multiple
+constexpr int kDqSlotBytes = kBK * 128 * 2;           // one bf16 B tile (64 x 128)
+constexpr int kDqSlots = 4;
+constexpr int kDqStages = (kRingBytes - kDqSlots * kDqSlotBytes) / kDqStageBytes;
+static_assert(kABytes + kDqRawBytes + 512 <= kDqStageBytes, "stage layout");
+static_assert(kDqStages >= 4 && kDqStages <= kMaxStages, "ring depth");
+static_assert(kDqSlots >= 2 && kDqSlots <= 4, "B slots");
+
 struct __align__(8) Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t fin;
+  uint64_t rawfull[kMaxStages];  // in-kernel dequantisation: this CTA's codes + scales landed
+  uint64_t bfull[4];             // converted B slot ready (even CTA, both CTAs' converters)
+  uint64_t bempty[4];            // B slot free again (the pair's MMAs that read it are done)
   uint32_t tmem_base;
   int abort;
   int32_t tile_off[kMaxE + 1];
@@ -120,6 +143,9 @@ struct Params {
   int num_acc;           // TMEM accumulators (2: the epilogue overlaps the next tile)
   int tmem_cols;         // TMEM columns allocated
   int pair_half_bytes;   // CTA pairs: bytes one CTA's copies deliver per stage
+  int dq_b;              // B is MXFP8 codes (map B0, uint8) dequantised in the kernel
+  const uint8_t* sfq;    //   its scales (sf_offset layout)
+  int sfq_k;             //   scale atoms per 128-row block (B columns / 128)
   void* out0;
   void* out1;
   void* out2;
@@ -410,6 +436,38 @@ MOE_DEV void stage_loads_pair(const Params& p, const TileInfo& ti, int ks, int r
   }
 }
 
+// In-kernel dequantisation: this CTA's copies of one stage.  A goes to the even
+// CTA's full barrier as on every pair; the B codes (64 rows x 128 columns) and
+// the scale atom that covers them land on this CTA's rawfull barrier.
+MOE_DEV void stage_loads_pair_dq(const Params& p, const TileInfo& ti, int ks, int rank,
+                                 uint8_t* sa, uint32_t fb, uint64_t* rb, const CUtensorMap* tA0,
+                                 const CUtensorMap* tA1, const CUtensorMap* tB0) {
+  const bool hi = ti.m_tile >= p.m_split;
+  const CUtensorMap* ma = hi ? tA1 : tA0;
+  const int mcol = (ti.m_tile - (hi ? p.m_split : 0)) * kTileM;
+  const int krow = ti.k0row + ks * kBK;
+  tma_load_2d_pair(sa, ma, fb, mcol, krow);
+  tma_load_2d_pair(sa + kABytes / 2, ma, fb, mcol + 64, krow);
+  const int n0 = ti.n_tile * p.BN + rank * (p.BN / 2);   // a multiple of 128
+  mbar_arrive_expect_tx(rb, (uint32_t)(kDqRawBytes + 512));
+  tma_load_2d(sa + kABytes, tB0, rb, n0, krow);
+  bulk_load(sa + kABytes + kDqRawBytes,
+            p.sfq + ((size_t)(krow >> 7) * (size_t)p.sfq_k + (size_t)(n0 >> 7)) * 512u, 512u, rb);
+}
+
+// Bounded wait for the last `stages` completions of one barrier array (copies
+// still in flight when a CTA gives up).
+MOE_DEV void drain_stages(uint64_t* bars, long issued, int stages) {
+  for (long i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+    const uint32_t a = smem_u32(&bars[(int)(i % stages)]);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, (uint32_t)((i / stages) & 1))) {
+      if (globaltimer() - t0 > kWaitLimitNs) break;
+    }
+  }
+}
+
+template <bool DQB>
 MOE_DEV void producer_pair(const Params& p, Ctl& s, uint8_t* ring, int rank,
                            const CUtensorMap* tA0, const CUtensorMap* tA1, const CUtensorMap* tB0,
                            const CUtensorMap* tB1) {
@@ -428,30 +486,32 @@ MOE_DEV void producer_pair(const Params& p, Ctl& s, uint8_t* ring, int rank,
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
       if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)p.pair_half_bytes);
       ++issued;
-      stage_loads_pair(p, ti, ks, rank, ring + stage * p.stage_bytes, full0 + 8u * (uint32_t)stage,
-                       tA0, tA1, tB0, tB1);
+      if constexpr (DQB)
+        stage_loads_pair_dq(p, ti, ks, rank, ring + stage * p.stage_bytes,
+                            full0 + 8u * (uint32_t)stage, &s.rawfull[stage], tA0, tA1, tB0);
+      else
+        stage_loads_pair(p, ti, ks, rank, ring + stage * p.stage_bytes,
+                         full0 + 8u * (uint32_t)stage, tA0, tA1, tB0, tB1);
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
   if (!ok) {
-    // copies in flight land on the even CTA's barriers: the even CTA waits for
-    // the stages it armed; both give their copies time to land before leaving
-    if (rank == 0) {
-      for (long i = (issued > p.stages ? issued - p.stages : 0); i < issued; ++i) {
-        const uint32_t a = smem_u32(&s.full[(int)(i % p.stages)]);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(a, (uint32_t)((i / p.stages) & 1))) {
-          if (globaltimer() - t0 > kWaitLimitNs) break;
-        }
-      }
-    }
+    // copies in flight land on the even CTA's barriers (and, dequantising, on
+    // this CTA's rawfull): the even CTA waits for the stages it armed; both
+    // give their copies time to land before leaving
+    if (rank == 0) drain_stages(s.full, issued, p.stages);
+    if (DQB) drain_stages(s.rawfull, issued, p.stages);
     const uint64_t t0 = globaltimer();
     while (globaltimer() - t0 < 100000ull) {}   // 100 us
   }
 }
 
+template <bool DQB>
 MOE_DEV void mma_issuer_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_base, int rank) {
   if (rank == 0) {
+    uint8_t* slots = ring + p.stages * p.stage_bytes;   // DQB: the converted B tiles
+    int slot = 0;
+    uint32_t sphase = 0;
     const int nt = total_tiles_pair(p, s);
     const int nclusters = (int)gridDim.x / 2;
     const int n_mma = p.b_dual ? 256 : p.BN;
@@ -470,9 +530,10 @@ MOE_DEV void mma_issuer_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tm
       const uint32_t tmem_d = tmem_base + (uint32_t)(acc * p.acc_cols);
       for (int ks = 0; ks < ti.ks; ++ks) {
         if (!mbar_wait(&s.full[stage], phase, &s.abort, p.err)) { ok = false; break; }
+        if (DQB && !mbar_wait(&s.bfull[slot], sphase, &s.abort, p.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t a_addr = smem_u32(ring + stage * p.stage_bytes);
-        const uint32_t b_addr = a_addr + kABytes;
+        const uint32_t b_addr = DQB ? smem_u32(slots + slot * kDqSlotBytes) : a_addr + kABytes;
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
           const uint64_t ad = p.a_mn ? smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
@@ -483,6 +544,10 @@ MOE_DEV void mma_issuer_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tm
         }
         tc_commit_pair(&s.empty[stage]);
         if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+        if constexpr (DQB) {
+          tc_commit_pair(&s.bempty[slot]);
+          if (++slot == kDqSlots) { slot = 0; sphase ^= 1u; }
+        }
       }
       if (!ok) break;
       tc_commit_pair(&s.tfull[acc]);
@@ -554,6 +619,62 @@ MOE_DEV void epilogue_router(const Params& p, const TileInfo& ti, int r, uint32_
         else
           out[row * p.n_valid + c + i] = val;
       }
+    }
+  }
+}
+
+// E8M0 scale byte -> 2^(s - 127) as a binary32: the biased exponent field is s
+// itself for s >= 1; 2^-127 (s = 0) is the subnormal with only mantissa bit 22.
+MOE_DEV float e8m0_value(uint32_t sb) { return __uint_as_float(sb != 0u ? sb << 23 : 0x00400000u); }
+
+// Converter warps (in-kernel dequantisation of B): for every stage in the
+// producer's order, wait for this CTA's codes and scales, wait for a free B
+// slot, write value = E4M3 code x 2^(scale - 127) rounded to bf16 (the same
+// arithmetic as the global dequantisation) into the slot's two 64-column
+// halves, 128-byte swizzled, and arrive on the even CTA's bfull barrier.
+// Thread i converts 16-byte output chunks i, i + 32 kConvWarps, ... of the 64 x 128
+// tile: chunk c is row c / 16, columns 8 (c % 16) .. + 7.
+MOE_DEV void converter_pair(const Params& p, Ctl& s, uint8_t* ring, int ctid, int lane) {
+  const int nt = total_tiles_pair(p, s);
+  const int nclusters = (int)gridDim.x / 2;
+  const int rank = (int)cluster_ctarank();
+  const uint32_t bfull0 = mapa_shared(smem_u32(&s.bfull[0]), 0);
+  uint8_t* slots = ring + p.stages * p.stage_bytes;
+  int stage = 0, slot = 0;
+  uint32_t phase = 0, sphase = 0;
+  for (int t = (int)blockIdx.x / 2; t < nt; t += nclusters) {
+    bool valid;
+    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    for (int ks = 0; ks < ti.ks; ++ks) {
+      bool ok = mbar_wait(&s.rawfull[stage], phase, &s.abort, p.err);
+      ok = ok && mbar_wait(&s.bempty[slot], sphase ^ 1u, &s.abort, p.err);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      const uint8_t* raw = ring + stage * p.stage_bytes + kABytes;
+      const uint8_t* sf = raw + kDqRawBytes;
+      uint8_t* dst = slots + slot * kDqSlotBytes;
+      const int r0 = (ti.k0row + ks * kBK) & 127;   // first row of the stage inside the atom
+#pragma unroll 4
+      for (int i = 0; i < (kBK * 16) / (32 * kConvWarps); ++i) {
+        const int c = ctid + 32 * kConvWarps * i;
+        const int r = c >> 4, j = c & 15;
+        const uint2 w = *reinterpret_cast<const uint2*>(raw + r * 128 + j * 8);
+        const int R = r0 + r;
+        const float scale = e8m0_value(sf[(R & 31) * 16 + (R >> 5) * 4 + (j >> 2)]);
+        float f[8];
+        e4m3x2_to_f32(w.x & 0xFFFFu, f[0], f[1]);
+        e4m3x2_to_f32(w.x >> 16, f[2], f[3]);
+        e4m3x2_to_f32(w.y & 0xFFFFu, f[4], f[5]);
+        e4m3x2_to_f32(w.y >> 16, f[6], f[7]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] *= scale;
+        *reinterpret_cast<uint4*>(dst + (j >> 3) * 8192 + r * 128 + (((j & 7) ^ (r & 7)) << 4)) =
+            pack8(f);
+      }
+      fence_proxy_async_smem();   // the MMA (async proxy) reads what was just written
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(bfull0 + 8u * (uint32_t)slot);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+      if (++slot == kDqSlots) { slot = 0; sphase ^= 1u; }
     }
   }
 }
@@ -726,12 +847,14 @@ MOE_DEV void swiglu_bwd8(const uint32_t* da, const uint4& hq, const uint4& uq, u
 
 // Columns [c0, c1) of the tile through the stager (bf16 outputs 64 columns per
 // store, fp32 outputs 32 columns per store).
+// F32_ONLY: the instantiation serves weight gradients alone (EPI_F32).
+template <bool F32_ONLY>
 MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb, int c0, int c1,
                                const OutStager& st, const CUtensorMap* tO0,
                                const CUtensorMap* tO1, const CUtensorMap* tO2) {
   uint32_t v0[32], v1[32];
   const int y = ti.m_tile * kTileM;
-  if (p.epi == EPI_BF16) {
+  if (!F32_ONLY && p.epi == EPI_BF16) {
     const int xb = ti.n_tile * p.BN;
     for (int c = c0; c < c1; c += 64) {
       tmem_ld32x2(tb + c, tb + c + 32, v0, v1);
@@ -739,7 +862,7 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
       st.row_bf16(v0, v1);
       st.end(tO0, xb + c, y);
     }
-  } else if (p.epi == EPI_SWIGLU_FWD) {
+  } else if (!F32_ONLY && p.epi == EPI_SWIGLU_FWD) {
     // accumulator columns [0, 128) are H, [128, 256) are U
     const int xb = ti.n_tile * 128;
     for (int c = c0; c < c1; c += 64) {
@@ -772,7 +895,7 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
                                    pack_bf16x2(__uint_as_float(h[8 * j + 6]), __uint_as_float(h[8 * j + 7]))));
       st.end(tO2, xb + c, y);
     }
-  } else if (p.epi == EPI_SWIGLU_BWD) {
+  } else if (!F32_ONLY && p.epi == EPI_SWIGLU_BWD) {
     const int xb = ti.n_tile * p.BN;
     const int64_t off = (int64_t)(y + st.r) * p.ldo + xb;
     const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
@@ -818,7 +941,7 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
   }
 }
 
-template <bool MX, bool PAIR>
+template <bool MX, bool PAIR, bool DQB>
 MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                       uint8_t* stage_out, const CUtensorMap* tO0, const CUtensorMap* tO1,
                       const CUtensorMap* tO2, int rank) {
@@ -859,7 +982,7 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
     if (valid) {
       if (!MX && p.tma_store)
-        epilogue_tile_tma(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
+        epilogue_tile_tma<DQB>(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
       else
         epilogue_tile<MX>(p, ti, r, tb, c0, c1);
     }
@@ -872,8 +995,8 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
 }
 
-template <bool MX, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool MX, bool PAIR, bool DQB = false>
+__global__ void __launch_bounds__(DQB ? kThreadsDq : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                         const __grid_constant__ CUtensorMap tA1,
                         const __grid_constant__ CUtensorMap tB0,
@@ -903,6 +1026,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], PAIR ? 2 * kEpiThreads : kEpiThreads);
+    }
+    if (DQB) {
+      for (int i = 0; i < p.stages; ++i) mbar_init(&s.rawfull[i], 1);
+      for (int i = 0; i < kDqSlots; ++i) {
+        mbar_init(&s.bfull[i], 2 * kConvWarps);   // one arrival per converter warp of the pair
+        mbar_init(&s.bempty[i], 1);
+      }
     }
     mbar_init(&s.fin, 1);
     s.abort = 0;
@@ -949,19 +1079,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       if (PAIR)
-        producer_pair(p, s, ring, rank, &tA0, &tA1, &tB0, &tB1);
+        producer_pair<DQB>(p, s, ring, rank, &tA0, &tA1, &tB0, &tB1);
       else
         producer<MX>(p, s, ring, &tA0, &tA1, &tB0, &tB1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       if (PAIR)
-        mma_issuer_pair(p, s, ring, tmem_base, rank);
+        mma_issuer_pair<DQB>(p, s, ring, tmem_base, rank);
       else
         mma_issuer<MX>(p, s, ring, tmem_base);
     }
-  } else {
-    epilogue<MX, PAIR>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
+  } else if (warp < kThreads / 32) {
+    epilogue<MX, PAIR, DQB>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
+  } else if (DQB && PAIR) {
+    converter_pair(p, s, ring, (int)threadIdx.x - kThreads, lane);
   }
 
   tc_fence_before();
@@ -987,7 +1119,7 @@ std::atomic<int> g_inject_stall{0};
 // fwd1 -3%, dgrad2 -4%); the narrow router GEMM stays on single CTAs.
 bool op_uses_pairs(int op) {
   return op == OP_FWD1_SWIGLU || op == OP_FWD2 || op == OP_DGRAD2_SWIGLU || op == OP_DGRAD1 ||
-         op == OP_WGRAD1 || op == OP_WGRAD2;
+         op == OP_WGRAD1 || op == OP_WGRAD2 || op == OP_WGRAD1_NAT || op == OP_WGRAD2_NAT;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1009,7 +1141,7 @@ bool get_encoder() {
 // box of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
 enum MapType { MAP_BF16 = 0, MAP_U8 = 1, MAP_F32 = 2 };
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, int type = MAP_BF16, bool swizzle64 = false) {
+              uint32_t box_outer, int type = MAP_BF16, int swizzle = 128) {
   const int esz = type == MAP_U8 ? 1 : (type == MAP_F32 ? 4 : 2);
   const CUtensorMapDataType dt = type == MAP_U8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : (type == MAP_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -1020,7 +1152,9 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   cuuint32_t estr[2] = {1, 1};
   return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  swizzle == 64    ? CU_TENSOR_MAP_SWIZZLE_64B
+                  : swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1035,6 +1169,9 @@ cudaError_t gemm_init_attributes() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(grouped_gemm_kernel<true, false>,
@@ -1094,8 +1231,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       ok = make_map(&A0, g.a0, d, rows, 64, 128) && make_map(&B0, g.w0, f, (uint64_t)E * d, 64, 64);
       A1 = A0; B1 = B0;
       p.out0 = g.out0; p.out1 = g.out1; p.aux0 = g.aux0; p.aux1 = g.aux1; p.ldo = f;
-      ok = ok && make_map(&O0, g.out0, f, rows, 32, 128, MAP_BF16, true) &&
-           make_map(&O1, g.out1, f, rows, 32, 128, MAP_BF16, true);
+      ok = ok && make_map(&O0, g.out0, f, rows, 32, 128, MAP_BF16, 64) &&
+           make_map(&O1, g.out1, f, rows, 32, 128, MAP_BF16, 64);
       O2 = O0;
       p.tma_store = 1;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
@@ -1131,6 +1268,37 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       ok = make_map(&A0, g.a0, f, rows, 64, 64) && make_map(&A1, g.a1, f, rows, 64, 64) &&
            make_map(&B0, g.aux0, d, rows, 64, 64);
       B1 = B0;
+      p.out0 = g.out0; p.out1 = g.out1; p.ldo = d; p.out_group_stride = (int64_t)f * d;
+      ok = ok && make_map(&O0, g.out0, d, (uint64_t)E * f, 32, 128, MAP_F32) &&
+           make_map(&O1, g.out1, d, (uint64_t)E * f, 32, 128, MAP_F32);
+      O2 = O0;
+      p.tma_store = 1;
+      p.out_rows_per_group = f;
+      max_tiles = (int64_t)E * p.m_tiles * p.n_tiles;
+      break;
+    case OP_WGRAD2_NAT:   // B = A_q (codes [rows, f]) dequantised in the kernel
+      if (!natural_wgrad_supported(g.op, d, f)) return cudaErrorInvalidValue;
+      p.mode = MODE_KGROUP; p.epi = EPI_F32; p.a_mn = 1; p.b_mn = 1; p.dq_b = 1;
+      p.BN = 256; p.m_tiles = d / kTileM; p.n_tiles = f / p.BN;
+      ok = make_map(&A0, g.a0, d, rows, 64, 64) && make_map(&B0, g.a1, f, rows, 128, kBK, MAP_U8, 0);
+      A1 = A0; B1 = B0;
+      p.sfq = g.sfb0; p.sfq_k = f / 128;
+      p.out0 = g.out0; p.ldo = f; p.out_group_stride = (int64_t)d * f;
+      ok = ok && make_map(&O0, g.out0, f, (uint64_t)E * d, 32, 128, MAP_F32);
+      O1 = O2 = O0;
+      p.tma_store = 1;
+      p.out_rows_per_group = d;
+      max_tiles = (int64_t)E * p.m_tiles * p.n_tiles;
+      break;
+    case OP_WGRAD1_NAT:   // B = Xd_q (codes [rows, d]) dequantised in the kernel
+      if (!natural_wgrad_supported(g.op, d, f)) return cudaErrorInvalidValue;
+      p.mode = MODE_KGROUP; p.epi = EPI_F32; p.a_mn = 1; p.b_mn = 1; p.dq_b = 1;
+      p.BN = 256; p.m_tiles = 2 * f / kTileM; p.m_split = f / kTileM;
+      p.n_tiles = d / p.BN;
+      ok = make_map(&A0, g.a0, f, rows, 64, 64) && make_map(&A1, g.a1, f, rows, 64, 64) &&
+           make_map(&B0, g.aux0, d, rows, 128, kBK, MAP_U8, 0);
+      B1 = B0;
+      p.sfq = g.sfb0; p.sfq_k = d / 128;
       p.out0 = g.out0; p.out1 = g.out1; p.ldo = d; p.out_group_stride = (int64_t)f * d;
       ok = ok && make_map(&O0, g.out0, d, (uint64_t)E * f, 32, 128, MAP_F32) &&
            make_map(&O1, g.out1, d, (uint64_t)E * f, 32, 128, MAP_F32);
@@ -1209,6 +1377,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   // CTA pairs: bf16 M-grouped GEMMs, and K-grouped ones with an even number of M tiles
   const bool pair = op_uses_pairs(g.op) && !mx && p.tma_store &&
                     (p.mode == MODE_MGROUP || (p.mode == MODE_KGROUP && p.m_tiles % 2 == 0));
+  if (p.dq_b && !pair) return cudaErrorInvalidValue;
   if (pair && p.mode == MODE_MGROUP && !p.b_mn && !p.b_dual) {
     // K-major B: each CTA of the pair loads BN/2 rows
     const void* wb = (g.op == OP_FWD2) ? g.w0 : nullptr;
@@ -1221,6 +1390,13 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.acc_cols = 128;
     p.tx_bytes = kABytes + p.BN * 128 + 512 * (1 + p.BN / 128);
     p.stage_bytes = (p.tx_bytes + 1023) & ~1023;
+  } else if (p.dq_b) {
+    // the ring holds A + codes + scale atom per stage; B's bf16 slots follow it
+    p.pair_half_bytes = kABytes;
+    p.tx_bytes = 2 * kABytes;
+    p.stage_bytes = kDqStageBytes;
+    p.num_acc = 2;
+    p.tmem_cols = 512;
   } else if (pair) {
     p.pair_half_bytes = kABytes + (p.BN / 2) * kBK * 2;
     p.tx_bytes = 2 * p.pair_half_bytes;
@@ -1233,7 +1409,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     p.tx_bytes = kABytes + (p.b_dual ? kBBytesMax : p.BN * kBK * 2);
     p.stage_bytes = p.tx_bytes;
   }
-  p.stages = kRingBytes / p.stage_bytes;
+  p.stages = p.dq_b ? kDqStages : kRingBytes / p.stage_bytes;
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2 || p.stage_bytes % 1024 != 0) return cudaErrorInvalidValue;
   int grid = (int)(max_tiles < di->sm_count ? max_tiles : di->sm_count);
@@ -1242,7 +1418,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     const int64_t pairs = (p.mode == MODE_MGROUP) ? (max_tiles / 2 + (int64_t)E * p.n_tiles)
                                                   : max_tiles / 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(p.dq_b ? kThreadsDq : kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1273,6 +1449,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     attr2[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr2;
     cfg.numAttrs = 2;
+    // (the dequantising kernel has the same shared memory: one CTA per SM too)
+    if (p.dq_b)
+      return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true, true>, A0, A1, B0, B1, O0,
+                                O1, O2, p);
     return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true>, A0, A1, B0, B1, O0, O1, O2,
                               p);
   }

@@ -104,7 +104,18 @@ enum GemmOp {
   OP_MX_FWD2 = 8,          // A = A_q;  B = W_down cache
   OP_MX_DGRAD2_SWIGLU = 9, // A = dY_q; B = W_down^T cache
   OP_MX_DGRAD1 = 10,       // A0/A1 = dH_q/dU_q; B0/B1 = W_gate^T / W_up^T caches
+  // weight gradients whose activation operand (B) is MXFP8 codes in the
+  // forward's row layout, dequantised inside the kernel (scales in sfb0)
+  OP_WGRAD2_NAT = 11,      // as OP_WGRAD2 with a1 = A_q
+  OP_WGRAD1_NAT = 12,      // as OP_WGRAD1 with aux0 = Xd_q
 };
+// The in-kernel dequantisation needs 256-column B tiles on CTA pairs: both
+// weight-gradient shapes' column counts (N) and WGRAD2's M a multiple of 256.
+inline bool natural_wgrad_supported(int op, int d, int f) {
+  if (op == OP_WGRAD2_NAT) return d % 256 == 0 && f % 256 == 0;
+  if (op == OP_WGRAD1_NAT) return d % 256 == 0;
+  return false;
+}
 
 struct GemmLaunch {
   int op;

@@ -119,3 +119,45 @@ def test_dense_router_backward(moe_gpu, T, d, E, k, f):
     assert max_abs_rel(f64(buf.grads["dx"])[same], bwd["dx"][same]) <= TOL
     if same.all():
         assert max_abs_rel(f64(buf.grads["dw_router"]), bwd["dW_router"]) <= 1e-3
+
+
+def test_recompute_with_the_balance_term_is_bitwise_the_saved_one(moe_gpu):
+    """Both options together: recomputed activations and the loss term give the
+    same gradients, bit for bit, as the saving backward with the term."""
+    m, dev = moe_gpu
+    T, d, E, k, f = 1000, 256, 16, 4, 256
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=31)
+    buf = run_layer_lb(m, dev, inp, k, 3.0, use_router=True)
+    names = ("dx", "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits")
+    saved = {n: buf.grads[n].clone() for n in names}
+    for n in ("xd", "h", "u", "a", "y"):
+        buf.saved[n].fill_(float("nan"))
+    t = {n: to_dev_bf16(inp[n], dev) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out")}
+    m.backward(buf, t["d_out"], t["x"], t["w_router"], t["w_gate"], t["w_up"], t["w_down"],
+               recompute=True, lb_coef=3.0)
+    assert m.read_error(buf.ws) == 0
+    for n in names:
+        assert torch.equal(buf.grads[n], saved[n]), n
+
+
+def test_invalid_backward_options_are_rejected(moe_gpu):
+    m, dev = moe_gpu
+    T, d, E, k, f = 64, 128, 4, 2, 128
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=2)
+    buf = run_layer_lb(m, dev, inp, k, 0.0, use_router=True)
+    t = {n: to_dev_bf16(inp[n], dev) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out")}
+    with pytest.raises(m.MoEError):
+        m.backward(buf, t["d_out"], t["x"], t["w_router"], t["w_gate"], t["w_up"], t["w_down"],
+                   lb_coef=float("nan"))
+    with pytest.raises(m.MoEError):
+        m.backward(buf, t["d_out"], t["x"], t["w_router"], t["w_gate"], t["w_up"], t["w_down"],
+                   lb_coef=float("inf"))
+    # recompute is a 0/1 flag; any other value is refused before anything runs
+    g = buf.grads
+    ba = m.BwdArgs(d_out=t["d_out"].data_ptr(), x=t["x"].data_ptr(),
+                   w_router=t["w_router"].data_ptr(), w_gate=t["w_gate"].data_ptr(),
+                   w_up=t["w_up"].data_ptr(), w_down=t["w_down"].data_ptr(),
+                   recompute=2, lb_coef=0.0, **{n: v.data_ptr() for n, v in g.items()})
+    with pytest.raises(m.MoEError):
+        m.layer_bwd(buf.shape, ba, buf.saved_struct(), buf.ws)
+    assert m.read_error(buf.ws) == 0

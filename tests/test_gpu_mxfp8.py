@@ -344,3 +344,115 @@ def test_mx_recompute_backward_is_bitwise_the_saved_one(mcase):
     assert m.read_error(buf.ws) == 0
     for n in names:
         assert torch.equal(buf.grads[n], saved_grads[n]), n
+
+
+# ------------------------------------------------ weight gradients, natural layout
+def natural_wgrads(m, s, ws, tile_offsets, dY, A_q, A_s, dH, dU, Xd_q, Xd_s, n, d, f, E):
+    """(dW_down, dW_gate, dW_up) from the natural-layout ops, and the same from
+    the global dequantisation followed by the BF16 weight-gradient GEMMs."""
+    dev = dY.device
+    out = {}
+    for arm in ("natural", "dq_bf16"):
+        dWd = torch.full((E, d, f), float("nan"), dtype=torch.float32, device=dev)
+        dWg, dWu = (torch.full((E, f, d), float("nan"), dtype=torch.float32, device=dev)
+                    for _ in range(2))
+        if arm == "natural":
+            if f % 256 == 0:
+                m.grouped_gemm(s, m.GEMM_WGRAD2_NATURAL, ws, tile_offsets=tile_offsets, a0=dY,
+                               a1=A_q, sfb0=A_s, out0=dWd)
+            m.grouped_gemm(s, m.GEMM_WGRAD1_NATURAL, ws, tile_offsets=tile_offsets, a0=dH, a1=dU,
+                           aux0=Xd_q, sfb0=Xd_s, out0=dWg, out1=dWu)
+        else:
+            a_dq = torch.empty(n, f, dtype=torch.bfloat16, device=dev)
+            x_dq = torch.empty(n, d, dtype=torch.bfloat16, device=dev)
+            m.dequantize_mxfp8(n, f, A_q, A_s, a_dq)
+            m.dequantize_mxfp8(n, d, Xd_q, Xd_s, x_dq)
+            m.grouped_gemm(s, m.GEMM_WGRAD2, ws, tile_offsets=tile_offsets, a0=dY, a1=a_dq,
+                           out0=dWd)
+            m.grouped_gemm(s, m.GEMM_WGRAD1, ws, tile_offsets=tile_offsets, a0=dH, a1=dU,
+                           aux0=x_dq, out0=dWg, out1=dWu)
+        out[arm] = (dWd, dWg, dWu)
+    return out
+
+
+def test_natural_wgrad_is_bitwise_the_dequantised_one(mcase):
+    """The weight gradients on the forward's MXFP8 codes (dequantised inside the
+    GEMM) equal, bit for bit, global dequantisation + BF16 GEMM, and match the
+    MXFP8 oracle; an expert without rows gets exact zeros."""
+    c = mcase
+    m, dev, n, d, f, E = c["m"], c["dev"], c["n"], c["d"], c["f"], c["E"]
+    aq, as_ = c["rows_q"](c["fwd"]["Aq"], f)
+    xq, xs = c["rows_q"](c["fwd"]["Xd"], d)
+    dY = c["rows_bf"](c["bwd"]["dY"], d)
+    dH = c["rows_bf"](c["bwd"]["dH"], f)
+    dU = c["rows_bf"](c["bwd"]["dU"], f)
+    got = natural_wgrads(m, c["s"], c["ws"], c["tile_offsets"], dY, aq, as_, dH, dU, xq, xs, n, d,
+                         f, E)
+    assert m.read_error(c["ws"]) == 0
+    nat, ref = got["natural"], got["dq_bf16"]
+    if f % 256 == 0:
+        assert torch.equal(nat[0], ref[0])
+        assert max_abs_rel(f64(nat[0]), c["bwd"]["dW_down"]) <= TOL
+    assert torch.equal(nat[1], ref[1]) and torch.equal(nat[2], ref[2])
+    assert max_abs_rel(f64(nat[1]), c["bwd"]["dW_gate"]) <= TOL
+    assert max_abs_rel(f64(nat[2]), c["bwd"]["dW_up"]) <= TOL
+    empty = np.where(c["fwd"]["counts"] == 0)[0]   # none when top-k selects every expert
+    assert (f64(nat[1])[empty] == 0).all() and (f64(nat[2])[empty] == 0).all()
+
+
+def test_natural_wgrad_refuses_unsupported_shapes(mcase):
+    c = mcase
+    m, dev, n, d, f, E = c["m"], c["dev"], c["n"], c["d"], c["f"], c["E"]
+    if f % 256 == 0:
+        pytest.skip("both natural ops support this shape")
+    aq, as_ = c["rows_q"](c["fwd"]["Aq"], f)
+    dW = torch.empty(E, d, f, dtype=torch.float32, device=dev)
+    with pytest.raises(m.MoEError):
+        m.grouped_gemm(c["s"], m.GEMM_WGRAD2_NATURAL, c["ws"], tile_offsets=c["tile_offsets"],
+                       a0=c["rows_bf"](c["bwd"]["dY"], d), a1=aq, sfb0=as_, out0=dW)
+    with pytest.raises(m.MoEError):   # scales missing
+        m.grouped_gemm(c["s"], m.GEMM_WGRAD1_NATURAL, c["ws"], tile_offsets=c["tile_offsets"],
+                       a0=dW, a1=dW, aux0=aq, out0=dW, out1=dW)
+    assert m.read_error(c["ws"]) == 0
+
+
+@pytest.mark.parametrize("T,d,E,k,f", [(4096, 512, 8, 4, 512), (3000, 768, 5, 2, 256)],
+                         ids=lambda v: str(v))
+def test_natural_wgrad_long_k(moe_gpu, T, d, E, k, f):
+    """Many K steps per expert (the ring and both B slots wrap many times) and a
+    ragged last tile: still bit for bit the dequantised BF16 result."""
+    m, dev = moe_gpu
+    rng = np.random.default_rng(T)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts = O.expert_counts(idx, E)
+    tile_offsets, row_offsets = O.tile_layout(counts, 128)
+    s = m.shape(T, d, E, k, f, prec=m.MXFP8)
+    n = m.rows_max(s)
+    used = int(row_offsets[-1])
+    ws = torch.zeros(m.workspace_size(s), dtype=torch.uint8, device=dev)
+
+    def qrows(width, scale):
+        a = np.zeros((n, width))
+        a[:used] = rng.standard_normal((used, width)) * scale
+        # zero rows between each expert's count and its tile boundary
+        for e in range(E):
+            a[int(row_offsets[e]) + int(counts[e]): int(tile_offsets[e + 1]) * 128] = 0.0
+        codes, sc = q_rows(a)
+        return a, u8(codes, dev), u8(sf_pack(sc), dev)
+
+    def brows(width):
+        a = np.zeros((n, width))
+        a[:used] = rng.standard_normal((used, width))
+        for e in range(E):
+            a[int(row_offsets[e]) + int(counts[e]): int(tile_offsets[e + 1]) * 128] = 0.0
+        return bf(a, dev)
+
+    _, aq, as_ = qrows(f, 0.5)
+    _, xq, xs = qrows(d, np.exp(rng.standard_normal((1, d))))
+    dY, dH, dU = brows(d), brows(f), brows(f)
+    to = torch.from_numpy(tile_offsets.astype(np.int32)).to(dev)
+    got = natural_wgrads(m, s, ws, to, dY, aq, as_, dH, dU, xq, xs, n, d, f, E)
+    assert m.read_error(ws) == 0
+    for a, b in zip(got["natural"], got["dq_bf16"]):
+        assert torch.equal(a, b)
+    assert torch.isfinite(got["natural"][1]).all()
