@@ -757,12 +757,32 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the MXFP8 weight-gradient comparison")
+    ap.add_argument("--mx-wgrad-only", action="store_true",
+                    help="run only the MXFP8 weight-gradient comparison and print its JSON")
+    ap.add_argument("--mx-wgrad-sizes", default="2048,4096,8192")
+    ap.add_argument("--mx-wgrad-reps", type=int, default=10)
     args = ap.parse_args(argv)
     from synth import CONFIGS
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.mx_wgrad_only:
+        return run_mx_wgrad_only(args)
     return run_ours(args, cfg)
+
+
+def run_mx_wgrad_only(args):
+    import torch
+    import moe_expert_layer_softmax_gb300 as m
+    m.load()
+    torch.cuda.set_device(0)
+    m.init(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    sizes = tuple(int(v) for v in args.mx_wgrad_sizes.split(","))
+    res = mx_wgrad_variants(m, dev, stream, sizes=sizes, reps=args.mx_wgrad_reps)
+    print(json.dumps({"mx_wgrad": res}), flush=True)
+    return 0
 
 
 if __name__ == "__main__":
