@@ -604,20 +604,43 @@ MOE_DEV void epilogue_router(const Params& p, const TileInfo& ti, int r, uint32_
   // EPI_ROUTER: fp32 logits (+ bias), rows < T and columns < E only
   // With the K loop split in two, each part adds its sum into the zeroed
   // logits (the first part with the bias): (0 + a) + b == (0 + b) + a, so the
-  // result does not depend on which part lands first.
+  // result does not depend on which part lands first.  Lane = row: the lanes
+  // of a warp touch 32 different rows (cache lines) per access; whole 32-column
+  // chunks of rows that start on 16 bytes go out as 4-wide loads, stores and
+  // atomics (8 per lane instead of 32).
   const int64_t row = (int64_t)ti.m_tile * kTileM + r;
   float* out = static_cast<float*>(p.out0);
   const bool add_bias = p.bias != nullptr && ti.kb == 0;
   for (int c = c0; c < c1; c += 32) {
     tmem_ld32(tb + c, v);      // warp-collective: executed by every lane
-    if (row < p.m_valid) {
+    if (row >= p.m_valid) continue;
+    float* o = out + row * p.n_valid + c;
+    const float* bz = add_bias ? p.bias + row * p.n_valid + c : nullptr;
+    if (p.n_valid % 4 == 0 && c + 32 <= p.n_valid) {
+      float4 b4[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        b4[q] = add_bias ? *reinterpret_cast<const float4*>(bz + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 val = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        if (add_bias) {
+          val.x += b4[q].x; val.y += b4[q].y; val.z += b4[q].z; val.w += b4[q].w;
+        }
+        if (p.k_parts > 1)
+          atomicAdd(reinterpret_cast<float4*>(o + 4 * q), val);
+        else
+          *reinterpret_cast<float4*>(o + 4 * q) = val;
+      }
+    } else {
       for (int i = 0; i < 32 && c + i < p.n_valid; ++i) {
         float val = __uint_as_float(v[i]);
-        if (add_bias) val += p.bias[row * p.n_valid + c + i];
+        if (add_bias) val += bz[i];
         if (p.k_parts > 1)
-          atomicAdd(out + row * p.n_valid + c + i, val);
+          atomicAdd(o + i, val);
         else
-          out[row * p.n_valid + c + i] = val;
+          o[i] = val;
       }
     }
   }
@@ -981,7 +1004,7 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     tc_fence_after();
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
     if (valid) {
-      if (!MX && p.tma_store)
+      if (DQB || (!MX && p.tma_store))
         epilogue_tile_tma<DQB>(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
       else
         epilogue_tile<MX>(p, ti, r, tb, c0, c1);
