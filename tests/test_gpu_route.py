@@ -120,10 +120,14 @@ def test_nonfinite_logits_flag_and_zero_gates(moe_gpu):
 
 
 @pytest.mark.parametrize("T,d,E,k,routing", [(300, 256, 8, 2, "none"), (1000, 512, 32, 4, "normal"),
-                                             (2048, 2048, 128, 4, "normal"), (257, 128, 16, 16, "normal")])
+                                             (2048, 2048, 128, 4, "normal"), (257, 128, 16, 16, "normal"),
+                                             (10000, 256, 12, 2, "normal"), (10000, 256, 16, 4, "normal")])
 def test_router_projection(moe_gpu, T, d, E, k, routing):
     """tcgen05 router GEMM: logits within 1e-5 of the fp64 oracle (relative to the
-    largest logit); the selection equals the oracle's except at near-ties."""
+    largest logit); the selection equals the oracle's except at near-ties.  The
+    10000-token cases have more row tiles than half the SMs, so the K loop is
+    not split and the epilogue stores directly (E = 12: column by column,
+    E = 16: 4-wide)."""
     m, dev = moe_gpu
     inp = make_inputs(T=T, d=d, E=E, k=k, f=128, seed=T + d, routing=routing, with_grad=False)
     x = to_dev_bf16(inp["x"], dev)
