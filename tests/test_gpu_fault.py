@@ -50,3 +50,51 @@ def test_stalled_gemm_times_out_and_context_survives(moe_gpu):
     assert m.read_error(ws) == 0
     assert max_abs_rel(f64(H)[:used], fwd["H"]) <= 2e-2
     assert max_abs_rel(f64(A)[:used], fwd["A"]) <= 2e-2
+
+
+def test_stalled_natural_wgrad_times_out_and_context_survives(moe_gpu):
+    """The same hook on the weight gradient that dequantises its MXFP8 operand
+    inside the kernel: the converter warps' bounded waits (for codes that never
+    arrive) run out as well, the kernel reports the timeout and returns, and the
+    next launch equals global dequantisation + the BF16 weight gradient."""
+    m, dev = moe_gpu
+    T, d, E, k, f = 300, 256, 4, 2, 256
+    rng = np.random.default_rng(78)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts = O.expert_counts(idx, E)
+    tile_offsets, row_offsets = O.tile_layout(counts, 128)
+    s = m.shape(T, d, E, k, f, prec=m.MXFP8)
+    n = m.rows_max(s)
+    used = int(row_offsets[-1])
+    ws = torch.zeros(m.workspace_size(s), dtype=torch.uint8, device=dev)
+    dY = torch.zeros(n, d, dtype=torch.bfloat16, device=dev)
+    A = torch.zeros(n, f, dtype=torch.bfloat16, device=dev)
+    dY[:used] = torch.from_numpy(rng.standard_normal((used, d)).astype(np.float32)).to(dev)
+    A[:used] = torch.from_numpy(rng.standard_normal((used, f)).astype(np.float32)).to(dev)
+    Aq = torch.empty(n, f, dtype=torch.uint8, device=dev)
+    As = torch.empty(n * f // 32, dtype=torch.uint8, device=dev)
+    m.quantize_mxfp8(1, n, f, 1, A, Aq, As)
+    to = torch.from_numpy(tile_offsets.astype(np.int32)).to(dev)
+    dW = torch.zeros(E, d, f, dtype=torch.float32, device=dev)
+
+    def run():
+        m.grouped_gemm(s, m.GEMM_WGRAD2_NATURAL, ws, tile_offsets=to, a0=dY, a1=Aq, sfb0=As,
+                       out0=dW)
+
+    prev = m.debug_inject_stall(1)
+    try:
+        m.clear_error(ws)
+        run()
+        err = m.read_error(ws)
+    finally:
+        m.debug_inject_stall(prev)
+    assert err & m.DEVERR_TIMEOUT
+    m.clear_error(ws)
+    run()
+    assert m.read_error(ws) == 0
+    Adq = torch.empty(n, f, dtype=torch.bfloat16, device=dev)
+    m.dequantize_mxfp8(n, f, Aq, As, Adq)
+    ref = torch.zeros_like(dW)
+    m.grouped_gemm(s, m.GEMM_WGRAD2, ws, tile_offsets=to, a0=dY, a1=Adq, out0=ref)
+    assert m.read_error(ws) == 0
+    assert torch.equal(dW, ref)
