@@ -156,11 +156,26 @@ __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] *= inv;
   const size_t row_out = (size_t)n0 + n;
-  uint2* out = reinterpret_cast<uint2*>(q_c + (size_t)mat * C * R + row_out * R + k0 + kb * 32);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) out[u] = e4m3x8(v + 8 * u);
   s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)row_out, (k0 / 32) + kb, R / 32)] =
       (uint8_t)(e + 127);
+  // Stage the 64 x 128 codes of the transposed tile in the (now free) tile
+  // memory, 8-byte chunk q of row n at chunk q ^ (n & 15) (conflict-free for
+  // the column-wise writes), then store whole 128-byte rows: 8 lanes per row,
+  // 16 bytes each.
+  __syncthreads();
+  uint2* st = reinterpret_cast<uint2*>(&tile[0][0]);   // 64 rows x 16 chunks
+#pragma unroll
+  for (int u = 0; u < 4; ++u) st[n * 16 + ((kb * 4 + u) ^ (n & 15))] = e4m3x8(v + 8 * u);
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int idx = threadIdx.x + u * kQThreads;   // 512 16-byte pieces
+    const int rn = idx >> 3, c = idx & 7;
+    const uint2 lo = st[rn * 16 + ((2 * c) ^ (rn & 15))];
+    const uint2 hi = st[rn * 16 + ((2 * c + 1) ^ (rn & 15))];
+    *reinterpret_cast<uint4*>(q_c + (size_t)mat * C * R + ((size_t)n0 + rn) * R + k0 + 16 * c) =
+        make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
 }
 
 // Warp per token: a lane holds 8 values of a 256-column chunk; 4 lanes form a
