@@ -12,7 +12,7 @@
 // Kernel structure (persistent, one CTA per SM, 320 threads):
 //   warp 0     TMA producer: 128-byte-swizzled A/B tiles into a 192 KB ring
 //              (6 stages of 32 KB on CTA pairs, 4 of 48 KB on single CTAs,
-//              up to 12 for the narrow router tile, 6 of 33 KB for MXFP8)
+//              up to 12 for the narrow router tile, 5 of 33 KB for MXFP8)
 //   warp 1     TMEM allocator and single-thread tcgen05.mma issuer (bf16 or
 //              block-scaled fp8 in, fp32 accumulators in tensor memory, two
 //              accumulators so the epilogue of one tile overlaps the main loop
