@@ -366,7 +366,10 @@ def run_ours(args, cfg):
     # by re-quantising 1.6 G weight values in numpy, so it is not run there
     cpu = (oracle_sample(cfg, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline
                                      and not mx) else None)
-    launches_per_step = (16 if wr is not None else 14) + (9 if mx else 0)
+    # router GEMM, top-k, scan + slots | dispatch, fwd1, fwd2, combine | combine bwd, dgrad2,
+    # wgrad2, dgrad1, wgrad1, dispatch bwd, router bwd (2); MXFP8 adds the three weight-cache
+    # quantisers, the dY quantiser and the A and Xd dequantisations
+    launches_per_step = (15 if wr is not None else 12) + (6 if mx else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,

@@ -252,7 +252,8 @@ typedef struct {
   uint8_t* upT_s;
 } moe_mx_weights_t;
 
-/* Fill all MXFP8 weight caches from the bf16 master weights (5 quantiser launches). */
+/* Fill all MXFP8 weight caches from the bf16 master weights (3 launches: one fused
+ * pass per weight writes both of its orientations). */
 MOE_API int moe_build_mx_weights(const moe_shape_t* shape, const void* w_gate, const void* w_up,
                                  const void* w_down, const moe_mx_weights_t* cache, void* stream);
 

@@ -122,10 +122,9 @@ int route_impl(const moe_shape_t* s, const void* x, const void* w_router, const 
   }
   MOE_CUDA(launch_route_topk(logits, s->T, s->n_experts, s->top_k, topk_idx, gates, rank, hist,
                              err, st));
-  MOE_CUDA(launch_route_scan(hist, n_route_blocks(s), s->n_experts, counts, offsets, tile_offsets,
-                             st));
-  MOE_CUDA(launch_route_slots(topk_idx, rank, hist, counts, tile_offsets, s->T, s->n_experts,
-                              s->top_k, rows_max_of(s), slot_of_route, route_of_slot, err, st));
+  MOE_CUDA(launch_route_scan_slots(hist, n_route_blocks(s), topk_idx, rank, s->T, s->n_experts,
+                                   s->top_k, rows_max_of(s), counts, offsets, tile_offsets,
+                                   slot_of_route, route_of_slot, err, st));
   return MOE_OK;
 }
 

@@ -49,6 +49,13 @@ cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_ran
                                const int32_t* tile_offsets, int T, int E, int k, int64_t rows_max,
                                int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
                                cudaStream_t s);
+// scan + slots in one kernel (block_hist is only read)
+cudaError_t launch_route_scan_slots(const int32_t* block_hist, int n_blocks,
+                                    const int32_t* topk_idx, const int32_t* local_rank, int T,
+                                    int E, int k, int64_t rows_max, int32_t* counts,
+                                    int32_t* offsets, int32_t* tile_offsets,
+                                    int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
+                                    cudaStream_t s);
 
 // ---------------------------------------------------------------- data movement
 cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,

@@ -229,6 +229,140 @@ __global__ void __launch_bounds__(256) route_slots_kernel(
   }
 }
 
+// Scan and slots in one kernel.  Block b < n_route_blk handles the routes of
+// routing blocks [4b, 4b + 4) (64 tokens); the blocks after them mark the
+// padding rows.  Every block re-derives from the per-block histograms (read
+// only, L2-resident) the per-expert totals and tile offsets, and a route block
+// the prefix over the routing blocks before its own; block 0 writes counts,
+// offsets and tile_offsets.  The slots are those of the sequential walk over
+// routes in (t, j) order, as with the separate scan and slots kernels.
+constexpr int kSsThreads = 256;
+constexpr int kSsRouteBlocks = 4;   // routing blocks (16 tokens each) per block
+__global__ void __launch_bounds__(kSsThreads) route_scan_slots_kernel(
+    const int32_t* __restrict__ block_hist, int n_blocks, const int32_t* __restrict__ topk_idx,
+    const int32_t* __restrict__ local_rank, int T, int E, int k, int64_t rows_max,
+    int n_route_blk, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ tile_offsets, int32_t* __restrict__ slot_of_route,
+    int32_t* __restrict__ route_of_slot, int32_t* __restrict__ err) {
+  pdl_begin();
+  __shared__ int32_t s_ptot[4 * kSsThreads];   // [part][expert] partial sums
+  __shared__ int32_t s_ppre[4 * kSsThreads];
+  __shared__ int32_t s_c[256];                   // counts, then their inclusive scan
+  __shared__ int32_t s_t[256];                   // tiles, then their inclusive scan
+  __shared__ int32_t s_pre[256];
+  __shared__ int32_t s_tot[256];
+  __shared__ int32_t s_base[kSsRouteBlocks][256];
+  const int tid = threadIdx.x;
+  const bool route_blk = (int)blockIdx.x < n_route_blk;
+  const int rb0 = route_blk ? (int)blockIdx.x * kSsRouteBlocks : n_blocks;
+
+  // 1. per-expert sums over all routing blocks and over those before rb0:
+  //    thread (part p, column group g) sums V experts over a range of rows
+  const int V = (E % 4 == 0) ? 4 : 1;
+  const int ng = E / V;
+  const int P = kSsThreads / ng;
+  const int p = tid / ng, g = tid - (tid / ng) * ng;
+  if (p < P) {
+    int tot[4] = {0, 0, 0, 0}, pre[4] = {0, 0, 0, 0};
+    const int per = (n_blocks + P - 1) / P;
+    const int r0 = min(n_blocks, p * per), r1 = min(n_blocks, r0 + per);
+    for (int r = r0; r < r1; r += 8) {
+      int4 h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        h[u] = make_int4(0, 0, 0, 0);
+        if (r + u < r1) {
+          const int32_t* row = block_hist + (size_t)(r + u) * E + V * g;
+          if (V == 4) h[u] = *reinterpret_cast<const int4*>(row);
+          else h[u].x = *row;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        tot[0] += h[u].x; tot[1] += h[u].y; tot[2] += h[u].z; tot[3] += h[u].w;
+        if (r + u < rb0) {
+          pre[0] += h[u].x; pre[1] += h[u].y; pre[2] += h[u].z; pre[3] += h[u].w;
+        }
+      }
+    }
+    for (int c = 0; c < V; ++c) {
+      s_ptot[p * E + V * g + c] = tot[c];
+      s_ppre[p * E + V * g + c] = pre[c];
+    }
+  }
+  __syncthreads();
+  if (tid < 256) {
+    int tot = 0, pre = 0;
+    if (tid < E)
+      for (int q = 0; q < P; ++q) {
+        tot += s_ptot[q * E + tid];
+        pre += s_ppre[q * E + tid];
+      }
+    s_tot[tid] = tot;
+    s_pre[tid] = pre;
+    s_c[tid] = tot;
+    s_t[tid] = (tot + kTileM - 1) / kTileM;
+  }
+  __syncthreads();
+  // 2. inclusive scans of counts and tiles over 256 entries
+  for (int off = 1; off < 256; off <<= 1) {
+    int c = 0, t = 0;
+    if (tid >= off) {
+      c = s_c[tid - off];
+      t = s_t[tid - off];
+    }
+    __syncthreads();
+    s_c[tid] += c;
+    s_t[tid] += t;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0 && tid < E) {
+    counts[tid] = s_tot[tid];
+    offsets[tid + 1] = s_c[tid];
+    tile_offsets[tid + 1] = s_t[tid];
+    if (tid == 0) {
+      offsets[0] = 0;
+      tile_offsets[0] = 0;
+    }
+  }
+  if (!route_blk) {
+    // 3'. padding rows of each expert's last tile
+    const int q = ((int)blockIdx.x - n_route_blk) * kSsThreads + tid;
+    if (q < E * kTileM) {
+      const int e = q / kTileM;
+      const int tile0 = e > 0 ? s_t[e - 1] : 0;
+      const int row = tile0 * kTileM + s_tot[e] + q % kTileM;
+      if (row < s_t[e] * kTileM) route_of_slot[row] = -1;
+    }
+    return;
+  }
+  // 3. first row of each of this block's routing blocks' routes, per expert
+  if (tid < E) {
+    int base = (s_t[tid] - (s_tot[tid] + kTileM - 1) / kTileM) * kTileM + s_pre[tid];
+    for (int j = 0; j < kSsRouteBlocks; ++j) {
+      s_base[j][tid] = base;
+      if (rb0 + j < n_blocks) base += block_hist[(size_t)(rb0 + j) * E + tid];
+    }
+  }
+  __syncthreads();
+  // 4. the slots of this block's routes
+  const int64_t i0 = (int64_t)rb0 * kRouteTokensPerBlock * k;
+  const int64_t i1 = min((int64_t)T, (int64_t)(rb0 + kSsRouteBlocks) * kRouteTokensPerBlock) * k;
+  for (int64_t i = i0 + tid; i < i1; i += kSsThreads) {
+    const int t = (int)(i / k);
+    const int j = t / kRouteTokensPerBlock - rb0;
+    const int e = topk_idx[i];
+    const int slot = (e >= 0 && e < E) ? s_base[j][e] + local_rank[i] : -1;
+    if (slot < 0 || slot >= rows_max) {   // never expected
+      raise_error(err, MOE_DEVERR_BOUNDS);
+      slot_of_route[i] = 0;
+      continue;
+    }
+    slot_of_route[i] = slot;
+    route_of_slot[slot] = (int32_t)i;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
@@ -269,6 +403,20 @@ cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_ran
   const int nb = (int)((n + 255) / 256);
   launch_pdl(route_slots_kernel, dim3(nb), dim3(256), 0, s, topk_idx, local_rank, block_base, counts, tile_offsets, T,
                                         E, k, rows_max, slot_of_route, route_of_slot, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan_slots(const int32_t* block_hist, int n_blocks,
+                                    const int32_t* topk_idx, const int32_t* local_rank, int T,
+                                    int E, int k, int64_t rows_max, int32_t* counts,
+                                    int32_t* offsets, int32_t* tile_offsets,
+                                    int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
+                                    cudaStream_t s) {
+  const int n_route_blk = (n_blocks + kSsRouteBlocks - 1) / kSsRouteBlocks;
+  const int n_pad_blk = (E * kTileM + kSsThreads - 1) / kSsThreads;
+  launch_pdl(route_scan_slots_kernel, dim3((unsigned)(n_route_blk + n_pad_blk)), dim3(kSsThreads),
+             0, s, block_hist, n_blocks, topk_idx, local_rank, T, E, k, rows_max, n_route_blk,
+             counts, offsets, tile_offsets, slot_of_route, route_of_slot, err);
   return cudaGetLastError();
 }
 
