@@ -281,7 +281,8 @@ def test_mx_layer_small(mcase):
 def test_mx_full_size_workload_sampled(moe_gpu):
     """32768 tokens, d=4096, 64 experts, top-8, f=2048: routing and the dispatched
     codes in full, two experts' forward rows and weight gradients against the
-    oracle's per-expert MXFP8 math."""
+    oracle's per-expert MXFP8 math, and the natural-layout weight gradients bit
+    for bit against the layer's."""
     m, dev = moe_gpu
     cfg = CONFIGS["mxfp8"]
     inp = make_inputs(cfg, seed=0)
@@ -319,6 +320,20 @@ def test_mx_full_size_workload_sampled(moe_gpu):
         dYe = gsel[:, None] * dO[ros[a:b_] // cfg.k]
         dWd = dYe.T @ Aq
         assert max_abs_rel(f64(buf.grads["dw_down"][e]), dWd) <= TOL
+    # the natural-layout weight gradients on the layer's own codes and scales
+    # equal, bit for bit, the layer's (global dequantisation + BF16) ones
+    g = buf.grads
+    s = m.shape(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, prec=m.MXFP8)
+    to = buf.saved["tile_offsets"]
+    dWd = torch.empty_like(g["dw_down"])
+    m.grouped_gemm(s, m.GEMM_WGRAD2_NATURAL, buf.ws, tile_offsets=to, a0=g["dy"],
+                   a1=buf.mx["a_q"], sfb0=buf.mx["a_s"], out0=dWd)
+    dWg, dWu = torch.empty_like(g["dw_gate"]), torch.empty_like(g["dw_up"])
+    m.grouped_gemm(s, m.GEMM_WGRAD1_NATURAL, buf.ws, tile_offsets=to, a0=g["dh"], a1=g["du"],
+                   aux0=buf.mx["xd_q"], sfb0=buf.mx["xd_s"], out0=dWg, out1=dWu)
+    assert m.read_error(buf.ws) == 0
+    assert torch.equal(dWd, g["dw_down"])
+    assert torch.equal(dWg, g["dw_gate"]) and torch.equal(dWu, g["dw_up"])
 
 
 def test_mx_recompute_backward_is_bitwise_the_saved_one(mcase):
