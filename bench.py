@@ -750,6 +750,42 @@ def end_to_end(m, buf, cfg, inp, wr, bias, wg, wu, wd, dev, stream, steps, world
                        "the next step's upload and this step's `out` download overlap the backward"}
 
 
+def run_profile(args, cfg):
+    """Whole layer steps only (weight caches, forward, backward), nothing timed:
+    the command that ncu captures."""
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_softmax_gb300 as m
+    from synth import make_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    m.init(0)
+    inp = make_inputs(cfg, seed=0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, wr, wg, wu, wd, dO = (bf(inp[n]) for n in ("x", "w_router", "w_gate", "w_up", "w_down", "d_out"))
+    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+    mx = cfg.prec == "mxfp8"
+    s = m.shape(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, prec=m.MXFP8 if mx else m.BF16)
+    buf = m.allocate(s)
+    out = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=dev)
+    m.clear_error(buf.ws)
+    for _ in range(args.warmup + args.steps):
+        if mx:
+            m.build_mx_weights(s, wg, wu, wd, buf.mx_weights)
+        m.forward(buf, x, wr, bias, wg, wu, wd, out)
+        m.backward(buf, dO, x, wr, wg, wu, wd)
+    torch.cuda.synchronize()
+    err = m.read_error(buf.ws)
+    print(json.dumps({"profile_run": cfg.name, "steps": args.warmup + args.steps, "error_word": err}),
+          flush=True)
+    return 0 if err == 0 else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -764,6 +800,8 @@ def main(argv=None):
                     help="run only the MXFP8 weight-gradient comparison and print its JSON")
     ap.add_argument("--mx-wgrad-sizes", default="2048,4096,8192")
     ap.add_argument("--mx-wgrad-reps", type=int, default=10)
+    ap.add_argument("--profile-run", action="store_true",
+                    help="run warmup + steps whole layer steps untimed (the command ncu captures)")
     args = ap.parse_args(argv)
     from synth import CONFIGS
     cfg = CONFIGS[args.config]
@@ -771,6 +809,8 @@ def main(argv=None):
         return run_reference(args, cfg)
     if args.mx_wgrad_only:
         return run_mx_wgrad_only(args)
+    if args.profile_run:
+        return run_profile(args, cfg)
     return run_ours(args, cfg)
 
 

@@ -346,6 +346,30 @@ MOE_DEV void tc_mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, u
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled MXFP8 MMA of a CTA pair (M = 256): each CTA reads its own A
+// rows from its shared memory and its A scales from its own tensor memory;
+// the B scales of all N columns must be present in both CTAs' tensor memory.
+MOE_DEV void tc_mma_mxf8_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                              uint32_t tmem_sfa, uint32_t tmem_sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], "
+      "[%6], p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(tmem_sfa), "r"(tmem_sfb)
+      : "memory");
+}
+// Pair form of tc_cp_32x128b_x4, issued by the even CTA: each CTA's copy of the
+// 32 x 16-byte block at this shared-memory offset goes to its own tensor memory.
+MOE_DEV void tc_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Warpgroup-wide register reallocation (every warp of the warpgroup executes it).
+template <int N>
+MOE_DEV void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+MOE_DEV void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 // arrive once on the mbarrier at this offset in both CTAs of the pair when all
 // tcgen05 operations issued so far by this thread have completed
 MOE_DEV void tc_commit_pair(uint64_t* bar) {

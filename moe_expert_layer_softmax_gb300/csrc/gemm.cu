@@ -1134,6 +1134,361 @@ __global__ void __launch_bounds__(DQB ? kThreadsDq : kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ MXFP8 on CTA pairs
+// One 256 x 256 tile per pair with tcgen05.mma.cta_group::2.kind::mxf8f6f4
+// (M = 256, N = 256, K = 32 per instruction, 4 per 128-byte stage).  Each CTA
+// stages, per K step of 128 codes: its 128 A rows, its 128 of the tile's 256 B
+// rows, the 512-byte scale atom of its A rows and both scale atoms of the B
+// rows (every CTA needs the B scales of all N columns); all of it lands on the
+// even CTA's `full` barrier (.cta_group::2 TMA, the scales through a 2-D byte
+// view of the atom array).  The even CTA copies the stage's scale atoms to
+// tensor memory (tcgen05.cp.cta_group::2: each CTA's atoms to its own tensor
+// memory) and issues the MMAs.  Tensor memory: one 256-column accumulator,
+// then a ring of scale columns (16 per stage: A at +0, B at +4 and +8).  The
+// accumulator is single: the epilogue reads its 128 columns into registers,
+// releases the accumulator and only then computes and stores, so the next
+// tile's main loop overlaps all but the tensor-memory reads.
+// 384 threads in three warpgroups: warpgroup 0 (warp 0 producer, warp 1 MMA
+// issuer, warps 2-3 idle) gives registers back with setmaxnreg.dec, the two
+// epilogue warpgroups (warps 4-11, warp w on tensor-memory lane quarter w % 4,
+// column half (w - 4) / 4) take them with setmaxnreg.inc: 128 fp32 accumulator
+// values per thread stay in registers without spilling.
+// Register budget: launched at 168 per thread (384 x 168 = 64512 per CTA),
+// 128 x 80 + 256 x 208 = 63488 after the split; per SM sub-partition
+// (three warps) 32 x (80 + 2 x 208) = 15872 <= 16384.
+constexpr int kMxPairThreads = 384;
+constexpr int kMxPairLaunchRegs = 168;
+constexpr int kMxPairRoleRegs = 80;
+constexpr int kMxPairEpiRegs = 208;
+static_assert(128 * kMxPairRoleRegs + 256 * kMxPairEpiRegs <= kMxPairThreads * kMxPairLaunchRegs,
+              "setmaxnreg split exceeds the launch allocation");
+static_assert(32 * (kMxPairRoleRegs + 2 * kMxPairEpiRegs) <= 16384, "sub-partition registers");
+constexpr int kMxPairBN = 256;
+constexpr int kMxCodeBytes = kTileM * 128;                   // 128 rows x 128 E4M3 codes
+constexpr int kMxPairSfOff = 2 * kMxCodeBytes;               // scale atoms after A and B
+constexpr int kMxPairTx = 2 * kMxCodeBytes + 3 * 512;        // one CTA's bytes per stage
+constexpr int kMxPairStageBytes = (kMxPairTx + 1023) & ~1023;
+// the TMA-store staging buffers are not used by these epilogues: the ring takes them
+constexpr int kMxPairStages = (kRingBytes + 2 * kStageOutBytes) / kMxPairStageBytes;
+constexpr uint32_t kMxSfCol0 = 256;
+constexpr uint32_t kMxSfColsPerStage = 16;
+// bf16 outputs leave through shared memory and TMA bulk stores, 32 columns at a
+// time: one 8 KB buffer (128 rows x 64 bytes, 64-byte swizzle) per column half,
+// after the ring
+constexpr int kMxStageHalfBytes = kTileM * 64;
+static_assert(kMxPairStages * kMxPairStageBytes + 2 * kMxStageHalfBytes <=
+                  kRingBytes + 2 * kStageOutBytes, "MXFP8 pair shared memory");
+static_assert(kMxPairStages >= 4 && kMxPairStages <= kMaxStages, "MXFP8 pair ring depth");
+static_assert(kMxSfCol0 + kMxSfColsPerStage * kMxPairStages <= kTmemCols, "MXFP8 pair TMEM");
+
+struct MxMaps {           // A, B and their scale-atom views, sources 0 and 1
+  const CUtensorMap* a[2];
+  const CUtensorMap* b[2];
+  const CUtensorMap* sa[2];
+  const CUtensorMap* sb[2];
+};
+
+// One stage's copies of this CTA, counted on the even CTA's full barrier.
+MOE_DEV void stage_loads_mx_pair(const Params& p, const TileInfo& ti, int ks, int rank, uint8_t* sa,
+                                 uint32_t fb, const MxMaps& mp) {
+  const int src = ks >= p.k_split ? 1 : 0;
+  const int kk = (src ? ks - p.k_split : ks) * 128;
+  const int brow = ti.e * p.b_group_rows + ti.n_tile * kMxPairBN;   // first B row of the tile
+  tma_load_2d_pair(sa, mp.a[src], fb, kk, ti.m_tile * kTileM);
+  tma_load_2d_pair(sa + kMxCodeBytes, mp.b[src], fb, kk, brow + rank * kTileM);
+  uint8_t* sf = sa + kMxPairSfOff;
+  // atom views: two 256-byte rows per 512-byte atom
+  tma_load_2d_pair(sf, mp.sa[src], fb, 0, 2 * (ti.m_tile * p.sf_ka + kk / 128));
+  tma_load_2d_pair(sf + 512, mp.sb[src], fb, 0, 2 * ((brow >> 7) * p.sf_kb + kk / 128));
+  tma_load_2d_pair(sf + 1024, mp.sb[src], fb, 0, 2 * (((brow >> 7) + 1) * p.sf_kb + kk / 128));
+}
+
+MOE_DEV void producer_mx_pair(const Params& p, Ctl& s, uint8_t* ring, int rank, const MxMaps& mp) {
+  if (p.inject_stall) return;
+  const int nt = total_tiles_pair(p, s);
+  const int nclusters = (int)gridDim.x / 2;
+  const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);   // even CTA's full[0]
+  int stage = 0;
+  uint32_t phase = 0;
+  long issued = 0;
+  bool ok = true;
+  for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters) {
+    bool valid;
+    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    for (int ks = 0; ks < ti.ks; ++ks) {
+      if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
+      if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)kMxPairTx);
+      ++issued;
+      stage_loads_mx_pair(p, ti, ks, rank, ring + stage * p.stage_bytes,
+                          full0 + 8u * (uint32_t)stage, mp);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+  if (!ok) {
+    if (rank == 0) drain_stages(s.full, issued, p.stages);
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 100000ull) {}   // 100 us for the odd CTA's copies to land
+  }
+}
+
+MOE_DEV void mma_issuer_mx_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_base,
+                                int rank) {
+  if (rank == 0) {
+    const int nt = total_tiles_pair(p, s);
+    const int nclusters = (int)gridDim.x / 2;
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters, ++it) {
+      bool valid;
+      const TileInfo ti = decode_pair(p, s, t, 0, valid);
+      if (!mbar_wait(&s.tempty[0], ((uint32_t)it & 1u) ^ 1u, &s.abort, p.err)) { ok = false; break; }
+      tc_fence_after();
+      for (int ks = 0; ks < ti.ks; ++ks) {
+        if (!mbar_wait(&s.full[stage], phase, &s.abort, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(ring + stage * p.stage_bytes);
+        const uint32_t b_addr = a_addr + kMxCodeBytes;
+        const uint32_t sf = a_addr + kMxPairSfOff;
+        const uint32_t t_sfa = tmem_base + kMxSfCol0 + (uint32_t)stage * kMxSfColsPerStage;
+        const uint32_t t_sfb = t_sfa + 4u;
+        tc_cp_32x128b_x4_pair(t_sfa, smem_desc_noswz(sf));
+        tc_cp_32x128b_x4_pair(t_sfb, smem_desc_noswz(sf + 512u));
+        tc_cp_32x128b_x4_pair(t_sfb + 4u, smem_desc_noswz(sf + 1024u));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          tc_mma_mxf8_pair(tmem_base, ad, bd, idesc_mxf8(2 * kTileM, kMxPairBN, k), t_sfa, t_sfb,
+                           (ks | k) != 0 ? 1u : 0u);
+        }
+        tc_commit_pair(&s.empty[stage]);
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit_pair(&s.tfull[0]);
+    }
+    tc_commit_pair(&s.fin);
+  }
+  const uint32_t a = smem_u32(&s.fin);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, 0)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      raise_error(p.err, MOE_DEVERR_TIMEOUT);
+      break;
+    }
+  }
+}
+
+// Output staging of one column half (four warps, 128 rows): 64-byte rows,
+// 64-byte swizzle, stored by one elected thread with a TMA bulk store.
+struct MxStager {
+  uint8_t* buf;
+  int bar_id;
+  bool leader;
+  int r;
+  MOE_DEV void begin() const {   // the previous bulk store has read the buffer
+    if (leader) bulk_wait_read_all();
+    bar_sync(bar_id, kEpiThreads / 2);
+  }
+  MOE_DEV void put32(const uint32_t* v) const {   // 32 fp32 -> 32 bf16 of row r
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) =
+          make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                     pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                     pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                     pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+  }
+  MOE_DEV void end(const CUtensorMap* map, int x, int y) const {
+    fence_proxy_async_smem();
+    bar_sync(bar_id, kEpiThreads / 2);
+    if (leader) {
+      tma_store_2d(map, buf, x, y);
+      bulk_commit();
+    }
+  }
+  MOE_DEV void store32(const uint32_t* v, const CUtensorMap* map, int x, int y) const {
+    begin();
+    put32(v);
+    end(map, x, y);
+  }
+};
+
+// Thread (lane quarter q, column half h) owns accumulator row 32q + lane,
+// columns [128h, 128h + 128).  bf16 outputs go through the half's stager
+// (maps tO0, tO1), E4M3 codes and E8M0 scales are stored directly (each
+// thread writes whole 32-byte sectors of codes).
+MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
+                              int rank, uint8_t* stage_base, const CUtensorMap* tO0,
+                              const CUtensorMap* tO1) {
+  const int nt = total_tiles_pair(p, s);
+  const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
+  const int quarter = warp & 3;
+  const int half = (warp - 4) >> 2;
+  const int r = quarter * 32 + lane;
+  const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(128 * half);
+  MxStager st;
+  st.buf = stage_base + half * kMxStageHalfBytes;
+  st.bar_id = 1 + half;
+  st.leader = (warp == 4 + 4 * half) && (lane == 0);
+  st.r = r;
+  int it = 0;
+  for (int t = (int)blockIdx.x / 2; t < nt; t += (int)gridDim.x / 2, ++it) {
+    bool valid;
+    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    bool ok = mbar_wait(&s.tfull[0], (uint32_t)it & 1u, &s.abort, p.err);
+    // the half's named barriers below need all four of its warps: leave together
+    if (!bar_and(st.bar_id, kEpiThreads / 2, ok)) break;
+    tc_fence_after();
+    uint32_t v[128];
+    tmem_ld32x2(tb, tb + 32, v, v + 32);
+    tmem_ld32x2(tb + 64, tb + 96, v + 64, v + 96);
+    tc_fence_before();
+    mbar_arrive_cluster(tempty0);   // the next tile's MMAs may overwrite the accumulator
+    if (!valid) continue;
+    const int y = ti.m_tile * kTileM;
+    const int64_t row = (int64_t)y + r;
+    if (p.epi == EPI_BF16) {
+      const int x0 = ti.n_tile * kMxPairBN + 128 * half;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) st.store32(v + 32 * c, tO0, x0 + 32 * c, y);
+    } else if (p.epi == EPI_SWIGLU_FWD_MX) {
+      // columns [0, 64) of the half are W_gate rows, [64, 128) the matching W_up rows:
+      // f columns n_tile * 128 + 64 * half + [0, 64)
+      const int fc = ti.n_tile * 128 + 64 * half;
+      st.store32(v, tO0, fc, y);
+      st.store32(v + 32, tO0, fc + 32, y);
+      st.store32(v + 64, tO1, fc, y);
+      st.store32(v + 96, tO1, fc + 32, y);
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        v[i] = __float_as_uint(silu_f(__uint_as_float(v[i])) * __uint_as_float(v[64 + i]));
+      uint8_t* Aq = static_cast<uint8_t*>(p.out2) + row * p.ldo + fc;
+      mx_store32(v, Aq, p.osf0 + sf_offset(row, fc / 32, p.osf_kb));
+      mx_store32(v + 32, Aq + 32, p.osf0 + sf_offset(row, fc / 32 + 1, p.osf_kb));
+    } else {   // EPI_SWIGLU_BWD_MX: dA for f columns n_tile * 256 + 128 * half + [0, 128)
+      const int fc = ti.n_tile * kMxPairBN + 128 * half;
+      const int64_t off = row * p.ldo + fc;
+      const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
+      const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
+      uint8_t* dHq = static_cast<uint8_t*>(p.out2) + off;
+      uint8_t* dUq = static_cast<uint8_t*>(p.out3) + off;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t gu[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float h[8], u[8];
+          unpack8(H[4 * c + q], h);
+          unpack8(U[4 * c + q], u);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float da = __uint_as_float(v[32 * c + 8 * q + i]);
+            const float sg = sigmoid_f(h[i]);
+            v[32 * c + 8 * q + i] = __float_as_uint(da * u[i] * (sg * (1.0f + h[i] * (1.0f - sg))));
+            gu[8 * q + i] = __float_as_uint(da * (h[i] * sg));
+          }
+        }
+        st.store32(v + 32 * c, tO0, fc + 32 * c, y);
+        st.store32(gu, tO1, fc + 32 * c, y);
+        const size_t so = sf_offset(row, fc / 32 + c, p.osf_kb);
+        mx_store32(v + 32 * c, dHq + 32 * c, p.osf0 + so);
+        mx_store32(gu, dUq + 32 * c, p.osf1 + so);
+      }
+    }
+  }
+  if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
+}
+
+__global__ void __launch_bounds__(kMxPairThreads, 1)
+    grouped_gemm_mx_pair_kernel(const __grid_constant__ CUtensorMap tA0,
+                                const __grid_constant__ CUtensorMap tA1,
+                                const __grid_constant__ CUtensorMap tB0,
+                                const __grid_constant__ CUtensorMap tB1,
+                                const __grid_constant__ CUtensorMap tSA0,
+                                const __grid_constant__ CUtensorMap tSA1,
+                                const __grid_constant__ CUtensorMap tSB0,
+                                const __grid_constant__ CUtensorMap tSB1,
+                                const __grid_constant__ CUtensorMap tO0,
+                                const __grid_constant__ CUtensorMap tO1, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    pdl_wait();
+    if (threadIdx.x == 0) raise_error(p.err, MOE_DEVERR_BOUNDS);
+    return;
+  }
+  uint8_t* ring = smem_raw;
+  Ctl& s = *reinterpret_cast<Ctl*>(smem_raw + kRingBytes + 2 * kStageOutBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    mbar_init(&s.tfull[0], 1);
+    mbar_init(&s.tempty[0], 2 * kEpiThreads);
+    mbar_init(&s.fin, 1);
+    s.abort = 0;
+    fence_barrier_init();
+  }
+  pdl_wait();
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.tile_off[i] = p.tile_offsets[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int e = 0; e < p.E; ++e) {
+      s.pair_off[e] = run;
+      run += (s.tile_off[e + 1] - s.tile_off[e] + 1) / 2;
+    }
+    s.pair_off[p.E] = run;
+  }
+  cluster_sync();   // both CTAs' barriers are initialised before any remote arrive
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tA0);
+    prefetch_tensormap(&tA1);
+    prefetch_tensormap(&tB0);
+    prefetch_tensormap(&tB1);
+    prefetch_tensormap(&tSA0);
+    prefetch_tensormap(&tSA1);
+    prefetch_tensormap(&tSB0);
+    prefetch_tensormap(&tSB1);
+    prefetch_tensormap(&tO0);
+    prefetch_tensormap(&tO1);
+  }
+  if (warp == 1) tmem_alloc_pair(&s.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s.tmem_base;
+
+  if (warp < 4) {
+    setmaxnreg_dec<kMxPairRoleRegs>();
+    if (warp == 0 && lane == 0) {
+      const MxMaps mp = {{&tA0, &tA1}, {&tB0, &tB1}, {&tSA0, &tSA1}, {&tSB0, &tSB1}};
+      producer_mx_pair(p, s, ring, rank, mp);
+    } else if (warp == 1 && lane == 0) {
+      mma_issuer_mx_pair(p, s, ring, tmem_base, rank);
+    }
+  } else {
+    setmaxnreg_inc<kMxPairEpiRegs>();
+    epilogue_mx_pair(p, s, tmem_base, warp, lane, rank, ring + p.stages * p.stage_bytes, &tO0,
+                     &tO1);
+  }
+
+  tc_fence_before();
+  cluster_sync();   // the partner no longer reads this CTA's memory
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 std::atomic<int> g_inject_stall{0};
 
@@ -1182,6 +1537,101 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte view of an MXFP8 scale array (sf_offset layout) of a K-major
+// [rows, K] operand: two 256-byte rows per 512-byte atom, one atom per box.
+bool make_sf_map(CUtensorMap* m, const void* sf, uint64_t rows, uint64_t K) {
+  return make_map(m, sf, 256, rows / kTileM * (K / 128) * 2, 256, 2, MAP_U8, 0);
+}
+
+// Pairs that can be resident at once (the persistent grid of the pair kernels,
+// which all have the same shared memory and threads per CTA).
+int resident_pairs(const DeviceInfo* di) {
+  static int resident[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return di->sm_count / 2;
+  if (resident[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)di->sm_count);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<false, true>, &cfg) != cudaSuccess ||
+        n < 1)
+      n = di->sm_count / 2;
+    resident[dev] = n;
+  }
+  return resident[dev];
+}
+
+// MXFP8 data GEMM on CTA pairs: `p` arrives set up for 128-column tiles (maps
+// with 128 x 128-code boxes, n_tiles of 128); N is a multiple of 256.
+cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A1,
+                           const CUtensorMap& B0, const CUtensorMap& B1, const GemmLaunch& g,
+                           const DeviceInfo* di, cudaStream_t stream) {
+  const uint64_t rows = (uint64_t)g.rows_max;
+  p.n_tiles = p.n_tiles * p.BN / kMxPairBN;
+  p.BN = kMxPairBN;
+  p.kstep = 128;
+  p.acc_cols = 256;
+  p.num_acc = 1;
+  p.tmem_cols = (int)kTmemCols;
+  p.stages = kMxPairStages;
+  p.stage_bytes = kMxPairStageBytes;
+  p.tx_bytes = kMxPairTx;
+  p.tma_store = 0;
+  const uint64_t ka = (uint64_t)p.sf_ka * 128, kb = (uint64_t)p.sf_kb * 128;
+  const uint64_t brows = (uint64_t)g.E * (uint64_t)p.b_group_rows;
+  CUtensorMap SA0, SA1, SB0, SB1;
+  bool ok = make_sf_map(&SA0, p.sfa0, rows, ka) && make_sf_map(&SB0, p.sfb0, brows, kb);
+  SA1 = SA0;
+  SB1 = SB0;
+  if (ok && p.sfa1 != p.sfa0) ok = make_sf_map(&SA1, p.sfa1, rows, ka);
+  if (ok && p.sfb1 != p.sfb0) ok = make_sf_map(&SB1, p.sfb1, brows, kb);
+  // bf16 outputs: out0 (H, Y, dH or dXd) and out1 (U or dU), 32-column boxes
+  CUtensorMap O0, O1;
+  const uint64_t ocols = (uint64_t)p.ldo;
+  ok = ok && make_map(&O0, p.out0, ocols, rows, 32, kTileM, MAP_BF16, 64);
+  O1 = O0;
+  if (ok && p.out1 != nullptr) ok = make_map(&O1, p.out1, ocols, rows, 32, kTileM, MAP_BF16, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  // the register split above assumes the launch allocation it was computed for
+  // (a smaller one would leave setmaxnreg.inc waiting for registers forever)
+  static int launch_regs = -1;
+  if (launch_regs < 0) {
+    cudaFuncAttributes fa = {};
+    launch_regs = cudaFuncGetAttributes(&fa, grouped_gemm_mx_pair_kernel) == cudaSuccess ? fa.numRegs : 0;
+  }
+  if (launch_regs != kMxPairLaunchRegs) return cudaErrorInvalidConfiguration;
+  const int64_t pairs = ((int64_t)(rows / kTileM) / 2 + g.E) * p.n_tiles;
+  int64_t np = resident_pairs(di);
+  if (pairs < np) np = pairs;
+  if (np < 1) np = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * np));
+  cfg.blockDim = dim3(kMxPairThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_pair_kernel, A0, A1, B0, B1, SA0, SA1, SB0, SB1,
+                            O0, O1, p);
+}
+
 }  // namespace
 
 int gemm_set_inject_stall(int mode) { return g_inject_stall.exchange(mode); }
@@ -1196,6 +1646,9 @@ cudaError_t gemm_init_attributes() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(grouped_gemm_mx_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(grouped_gemm_kernel<true, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1396,6 +1849,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if (mx && (p.n_tiles * p.BN) % kMxPairBN == 0)
+    return launch_mx_pair(p, A0, A1, B0, B1, g, di, stream);
   if (!p.tma_store) O0 = O1 = O2 = A0;   // unused by the direct-store epilogues
   // CTA pairs: bf16 M-grouped GEMMs, and K-grouped ones with an even number of M tiles
   const bool pair = op_uses_pairs(g.op) && !mx && p.tma_store &&
@@ -1452,18 +1907,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // as many pairs as can be resident at once (persistent tile loop)
-    static int resident[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && resident[dev] == 0) {
-      cfg.gridDim = dim3((unsigned)di->sm_count);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<false, true>, &cfg) != cudaSuccess ||
-          n < 1)
-        n = di->sm_count / 2;
-      resident[dev] = n;
-    }
-    int64_t np = (dev >= 0 && dev < 64) ? resident[dev] : di->sm_count / 2;
+    int64_t np = resident_pairs(di);
     if (pairs < np) np = pairs;
     if (np < 1) np = 1;
     cfg.gridDim = dim3((unsigned)(2 * np));

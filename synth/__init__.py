@@ -88,6 +88,11 @@ CONFIGS: dict[str, LayerConfig] = {
     "mxfp8": LayerConfig(
         "mxfp8", T=32768, d=4096, E=64, k=8, f=2048, prec="mxfp8", routing="normal",
         note="MXFP8 forward+backward, random routing"),
+    # reduced cases for ncu captures: the same d, f and rows per expert as the
+    # full workloads, with few experts so that a capture holds a few GB at most
+    "mxfp8_8x4096": LayerConfig(
+        "mxfp8_8x4096", T=4096, d=4096, E=8, k=8, f=2048, prec="mxfp8", routing="normal",
+        note="8 experts of 4096 rows each (every token routed to all 8), d=4096, f=2048"),
 }
 
 
