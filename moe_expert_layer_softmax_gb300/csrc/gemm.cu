@@ -94,6 +94,7 @@ struct __align__(8) Ctl {
   uint64_t rawfull[kMaxStages];  // in-kernel dequantisation: this CTA's codes + scales landed
   uint64_t bfull[4];             // converted B slot ready (even CTA, both CTAs' converters)
   uint64_t bempty[4];            // B slot free again (the pair's MMAs that read it are done)
+  uint64_t hufull[4];            // MXFP8 SwiGLU backward: H and U chunk landed (2 halves x 2 sets)
   uint32_t tmem_base;
   int abort;
   int32_t tile_off[kMaxE + 1];
@@ -1178,6 +1179,15 @@ constexpr uint32_t kMxSfColsPerStage = 16;
 constexpr int kMxStageHalfBytes = kTileM * 64;
 static_assert(kMxPairStages * kMxPairStageBytes + 2 * kMxStageHalfBytes <=
                   kRingBytes + 2 * kStageOutBytes, "MXFP8 pair shared memory");
+// The SwiGLU backward also reads H and U: each half has two sets of (H, U)
+// 32-column chunks (8 KB each, the output layout), TMA-loaded one chunk ahead;
+// dH and dU overwrite them in place and leave by TMA store.  A 4-stage ring
+// makes room.
+constexpr int kMxBwdStages = 4;
+constexpr int kMxHuSetBytes = 2 * kTileM * 64;
+constexpr int kMxHuHalfBytes = 2 * kMxHuSetBytes;
+static_assert(kMxBwdStages * kMxPairStageBytes + 2 * kMxHuHalfBytes <=
+                  kRingBytes + 2 * kStageOutBytes, "MXFP8 pair backward shared memory");
 static_assert(kMxPairStages >= 4 && kMxPairStages <= kMaxStages, "MXFP8 pair ring depth");
 static_assert(kMxSfCol0 + kMxSfColsPerStage * kMxPairStages <= kTmemCols, "MXFP8 pair TMEM");
 
@@ -1322,25 +1332,46 @@ struct MxStager {
 // thread writes whole 32-byte sectors of codes).
 MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                               int rank, uint8_t* stage_base, const CUtensorMap* tO0,
-                              const CUtensorMap* tO1) {
+                              const CUtensorMap* tO1, const CUtensorMap* tH,
+                              const CUtensorMap* tU) {
   const int nt = total_tiles_pair(p, s);
   const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
   const int quarter = warp & 3;
   const int half = (warp - 4) >> 2;
   const int r = quarter * 32 + lane;
   const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(128 * half);
+  const bool bwd = p.epi == EPI_SWIGLU_BWD_MX;
   MxStager st;
-  st.buf = stage_base + half * kMxStageHalfBytes;
+  st.buf = stage_base + half * (bwd ? kMxHuHalfBytes : kMxStageHalfBytes);
   st.bar_id = 1 + half;
   st.leader = (warp == 4 + 4 * half) && (lane == 0);
   st.r = r;
+  uint64_t* hu_bar = &s.hufull[2 * half];
   int it = 0;
   for (int t = (int)blockIdx.x / 2; t < nt; t += (int)gridDim.x / 2, ++it) {
     bool valid;
     const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    if (bwd && valid && st.leader) {
+      // H and U chunks 0 and 1 of this tile, into sets 0 and 1, once the
+      // previous tile's stores have read those sets
+      bulk_wait_read_all();
+      const int fc = ti.n_tile * kMxPairBN + 128 * half;
+      for (int j = 0; j < 2; ++j) {
+        uint8_t* set = st.buf + j * kMxHuSetBytes;
+        mbar_arrive_expect_tx(&hu_bar[j], (uint32_t)kMxHuSetBytes);
+        tma_load_2d(set, tH, &hu_bar[j], fc + 32 * j, ti.m_tile * kTileM);
+        tma_load_2d(set + kMxHuSetBytes / 2, tU, &hu_bar[j], fc + 32 * j, ti.m_tile * kTileM);
+      }
+    }
     bool ok = mbar_wait(&s.tfull[0], (uint32_t)it & 1u, &s.abort, p.err);
     // the half's named barriers below need all four of its warps: leave together
-    if (!bar_and(st.bar_id, kEpiThreads / 2, ok)) break;
+    if (!bar_and(st.bar_id, kEpiThreads / 2, ok)) {
+      if (bwd && st.leader) {   // H/U copies may be in flight: let them land first
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {}
+      }
+      break;
+    }
     tc_fence_after();
     uint32_t v[128];
     tmem_ld32x2(tb, tb + 32, v, v + 32);
@@ -1371,32 +1402,53 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
     } else {   // EPI_SWIGLU_BWD_MX: dA for f columns n_tile * 256 + 128 * half + [0, 128)
       const int fc = ti.n_tile * kMxPairBN + 128 * half;
       const int64_t off = row * p.ldo + fc;
-      const uint4* H = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux0) + off);
-      const uint4* U = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.aux1) + off);
       uint8_t* dHq = static_cast<uint8_t*>(p.out2) + off;
       uint8_t* dUq = static_cast<uint8_t*>(p.out3) + off;
+      bool fine = true;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        const int j = c & 1;
+        uint8_t* hb = st.buf + j * kMxHuSetBytes;
+        uint8_t* ub = hb + kMxHuSetBytes / 2;
+        // chunk c is the (c / 2)-th use of set j in this tile
+        fine = fine && mbar_wait(&hu_bar[j], (uint32_t)(c >> 1) & 1u, &s.abort, p.err);
         uint32_t gu[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float h[8], u[8];
-          unpack8(H[4 * c + q], h);
-          unpack8(U[4 * c + q], u);
+          const int so16 = r * 64 + ((q ^ ((r >> 1) & 3)) << 4);
+          float h[8], u[8], gh[8], g2[8];
+          unpack8(*reinterpret_cast<const uint4*>(hb + so16), h);
+          unpack8(*reinterpret_cast<const uint4*>(ub + so16), u);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float da = __uint_as_float(v[32 * c + 8 * q + i]);
             const float sg = sigmoid_f(h[i]);
-            v[32 * c + 8 * q + i] = __float_as_uint(da * u[i] * (sg * (1.0f + h[i] * (1.0f - sg))));
-            gu[8 * q + i] = __float_as_uint(da * (h[i] * sg));
+            gh[i] = da * u[i] * (sg * (1.0f + h[i] * (1.0f - sg)));
+            g2[i] = da * (h[i] * sg);
+            v[32 * c + 8 * q + i] = __float_as_uint(gh[i]);
+            gu[8 * q + i] = __float_as_uint(g2[i]);
+          }
+          *reinterpret_cast<uint4*>(hb + so16) = pack8(gh);   // dH, dU over H, U
+          *reinterpret_cast<uint4*>(ub + so16) = pack8(g2);
+        }
+        fence_proxy_async_smem();
+        bar_sync(st.bar_id, kEpiThreads / 2);
+        if (st.leader) {
+          tma_store_2d(tO0, hb, fc + 32 * c, y);
+          tma_store_2d(tO1, ub, fc + 32 * c, y);
+          bulk_commit();
+          if (c + 2 < 4) {   // chunk c + 2 into this set once the stores have read it
+            bulk_wait_read_all();
+            mbar_arrive_expect_tx(&hu_bar[j], (uint32_t)kMxHuSetBytes);
+            tma_load_2d(hb, tH, &hu_bar[j], fc + 32 * (c + 2), y);
+            tma_load_2d(ub, tU, &hu_bar[j], fc + 32 * (c + 2), y);
           }
         }
-        st.store32(v + 32 * c, tO0, fc + 32 * c, y);
-        st.store32(gu, tO1, fc + 32 * c, y);
         const size_t so = sf_offset(row, fc / 32 + c, p.osf_kb);
         mx_store32(v + 32 * c, dHq + 32 * c, p.osf0 + so);
         mx_store32(gu, dUq + 32 * c, p.osf1 + so);
       }
+      (void)fine;   // a wait that ran out has set the error word and the abort flag
     }
   }
   if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
@@ -1412,7 +1464,9 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
                                 const __grid_constant__ CUtensorMap tSB0,
                                 const __grid_constant__ CUtensorMap tSB1,
                                 const __grid_constant__ CUtensorMap tO0,
-                                const __grid_constant__ CUtensorMap tO1, const Params p) {
+                                const __grid_constant__ CUtensorMap tO1,
+                                const __grid_constant__ CUtensorMap tH,
+                                const __grid_constant__ CUtensorMap tU, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0) {
     pdl_wait();
@@ -1432,6 +1486,7 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
     }
     mbar_init(&s.tfull[0], 1);
     mbar_init(&s.tempty[0], 2 * kEpiThreads);
+    for (int i = 0; i < 4; ++i) mbar_init(&s.hufull[i], 1);
     mbar_init(&s.fin, 1);
     s.abort = 0;
     fence_barrier_init();
@@ -1459,6 +1514,10 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
     prefetch_tensormap(&tSB1);
     prefetch_tensormap(&tO0);
     prefetch_tensormap(&tO1);
+    if (p.epi == EPI_SWIGLU_BWD_MX) {
+      prefetch_tensormap(&tH);
+      prefetch_tensormap(&tU);
+    }
   }
   if (warp == 1) tmem_alloc_pair(&s.tmem_base, kTmemCols);
   tc_fence_before();
@@ -1477,7 +1536,7 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
   } else {
     setmaxnreg_inc<kMxPairEpiRegs>();
     epilogue_mx_pair(p, s, tmem_base, warp, lane, rank, ring + p.stages * p.stage_bytes, &tO0,
-                     &tO1);
+                     &tO1, &tH, &tU);
   }
 
   tc_fence_before();
@@ -1583,7 +1642,7 @@ cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A
   p.acc_cols = 256;
   p.num_acc = 1;
   p.tmem_cols = (int)kTmemCols;
-  p.stages = kMxPairStages;
+  p.stages = p.epi == EPI_SWIGLU_BWD_MX ? kMxBwdStages : kMxPairStages;
   p.stage_bytes = kMxPairStageBytes;
   p.tx_bytes = kMxPairTx;
   p.tma_store = 0;
@@ -1601,6 +1660,11 @@ cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A
   ok = ok && make_map(&O0, p.out0, ocols, rows, 32, kTileM, MAP_BF16, 64);
   O1 = O0;
   if (ok && p.out1 != nullptr) ok = make_map(&O1, p.out1, ocols, rows, 32, kTileM, MAP_BF16, 64);
+  // SwiGLU backward: H (aux0) and U (aux1) in the same 32-column boxes
+  CUtensorMap MH = O0, MU = O0;
+  if (ok && p.epi == EPI_SWIGLU_BWD_MX)
+    ok = make_map(&MH, p.aux0, ocols, rows, 32, kTileM, MAP_BF16, 64) &&
+         make_map(&MU, p.aux1, ocols, rows, 32, kTileM, MAP_BF16, 64);
   if (!ok) return cudaErrorInvalidValue;
   // the register split above assumes the launch allocation it was computed for
   // (a smaller one would leave setmaxnreg.inc waiting for registers forever)
@@ -1629,7 +1693,7 @@ cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_pair_kernel, A0, A1, B0, B1, SA0, SA1, SB0, SB1,
-                            O0, O1, p);
+                            O0, O1, MH, MU, p);
 }
 
 }  // namespace
