@@ -5,17 +5,19 @@
 One step = moe_layer_fwd + moe_layer_bwd over one batch of synthetic tokens
 (router projection, softmax/top-k, counts/offsets/slots, rowwise dispatch,
 grouped SwiGLU GEMMs, combine, and the whole backward), inputs resident in HBM.
-The default workload is the fine-grained layer: T=8192 tokens, d_model=2048,
-32 experts, top-4, d_ff=1024, bf16, seeded random routing.
+The default workload is the largest one that fits one GPU: the MXFP8 layer,
+T=32768 tokens, d_model=4096, 64 experts, top-8, d_ff=2048, seeded random
+routing; its weight caches are rebuilt from the bf16 master weights every step.
+`--config fine_grained|large_pool|skewed` runs the bf16 workloads.
 
 Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs an
 independent replica on its own tokens (the layer has no exchange step), so
 scaling is weak and `value` is the total tokens/s of all ranks; the step time
 is the maximum over ranks.
 
-`--impl reference` times the CPU oracle (float64 numpy, the correctness
-reference of this repository) on a bounded sample of the same workload on the
-host cores; it is a deliberately slow baseline, not a target.
+`--impl reference` times the CPU oracle (plain C++17 + OpenMP in double, the
+correctness reference of this repository) on a bounded sample of the same
+workload on the host cores; it is a deliberately slow baseline, not a target.
 """
 from __future__ import annotations
 
@@ -131,65 +133,93 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ the oracle arm
-_INPUT_CACHE = {}
+def oracle_sample(cfg, inp, budget_s: float = 15.0, max_experts: int = 0) -> dict:
+    """Time the C++ oracle on a bounded sample of the workload.
 
+    The sample is the routing of all T tokens (router projection, softmax/top-k,
+    counts, offsets, slots), then whole experts, one after the other in a seeded
+    order, each with every one of its routes: dispatch (MXFP8: tokens quantised),
+    forward (MXFP8: weights quantised in both orientations, A quantised), the
+    expert's rows of the combine backward, and the backward.  Experts are added
+    until `budget_s` has passed (at least one; at most `max_experts` when > 0).
+    The full step is extrapolated as routing + (experts with routes) x the mean
+    expert time; the combine and dispatch gather-sums over all tokens are O(T k d)
+    and are left out."""
+    import numpy as np
 
-def oracle_sample(cfg, seed: int, budget_s: float = 12.0, n_tok: int = 1024) -> dict:
-    """Time the CPU oracle's forward+backward on a bounded token sample (at
-    least one pass over `n_tok` tokens, repeated until `budget_s` has passed)."""
-    from oracle import moe_oracle as O
-    from synth import make_inputs
+    from oracle import cpp as O
 
-    key = (cfg.name, seed)
-    if key not in _INPUT_CACHE:
-        _INPUT_CACHE[key] = make_inputs(cfg, seed=seed)
-    inp = _INPUT_CACHE[key]
-    sl = slice(0, n_tok)
-    x, dO = inp["x"][sl], inp["d_out"][sl]
-    bias = inp["bias"][sl] if inp["bias"] is not None else None
-    done = 0
+    mx = cfg.prec == "mxfp8"
     t0 = time.perf_counter()
-    while True:
-        fwd = O.layer_forward(x, inp["w_router"], bias, inp["w_gate"], inp["w_up"], inp["w_down"],
-                              cfg.k)
-        O.layer_backward(fwd, dO, x, inp["w_router"], inp["w_gate"], inp["w_up"], inp["w_down"])
-        done += n_tok
-        el = time.perf_counter() - t0
-        if el >= budget_s:
+    logits = O.router_logits(inp["x"], inp["w_router"], inp["bias"])
+    idx, gates = O.softmax_topk_gates(logits, cfg.k)
+    counts = O.expert_counts(idx, cfg.E)
+    _, row_offsets = O.tile_layout(counts, 128)
+    sor, ros = O.assign_slots(idx, row_offsets)
+    t_route = time.perf_counter() - t0
+    order = [int(e) for e in np.random.default_rng(0).permutation(cfg.E) if counts[e] > 0]
+    lib = O.lib()
+    p = O._ptr
+    times, rows_done = [], 0
+    t_start = time.perf_counter()
+    for e in order:
+        a, b = int(row_offsets[e]), int(row_offsets[e]) + int(counts[e])
+        routes = ros[a:b]
+        tok = routes // cfg.k
+        n, d, f = b - a, cfg.d, cfg.f
+        t1 = time.perf_counter()
+        xe = O.as_f64(inp["x"][tok])
+        if mx:
+            xe = O._qdq(xe)
+        wg, wu, wd = (O.as_f64(inp[nm][e]) for nm in ("w_gate", "w_up", "w_down"))
+        H, U, A, Y = (np.empty((n, f)), np.empty((n, f)), np.empty((n, f)), np.empty((n, d)))
+        Aq = np.empty((n, f)) if mx else None
+        lib.mo_expert_forward(p(xe), n, d, f, p(wg), p(wu), p(wd), int(mx), p(H), p(U), p(A),
+                              p(Aq), p(Y))
+        dY = gates.reshape(-1)[routes][:, None] * O.as_f64(inp["d_out"][tok])
+        dH, dU, dX = np.empty((n, f)), np.empty((n, f)), np.empty((n, d))
+        dWg, dWu, dWd = np.empty((f, d)), np.empty((f, d)), np.empty((d, f))
+        lib.mo_expert_backward(p(dY), p(xe), p(H), p(U), p(Aq if mx else A), n, d, f, p(wg),
+                               p(wu), p(wd), int(mx), p(dH), p(dU), p(dX), p(dWg), p(dWu),
+                               p(dWd))
+        times.append(time.perf_counter() - t1)
+        rows_done += n
+        if time.perf_counter() - t_start >= budget_s or (max_experts and len(times) >= max_experts):
             break
-    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
-    cores = int(threads) if threads else (os.cpu_count() or 1)
-    return {"value": done / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n_tok} of {cfg.T} tokens of the '{cfg.name}' workload with all {cfg.E} "
-                      f"experts' full weights, forward+backward repeated {done // n_tok}x "
-                      f"({el:.1f} s, float64 numpy/OpenBLAS)",
-            "seconds": el}
+    step_s = t_route + len(order) * (sum(times) / len(times))
+    return {"value": cfg.T / step_s, "unit": UNIT, "cores": O.threads(), "kind": "oracle",
+            "extrapolated": True, "experts_timed": len(times), "seconds": t_route + sum(times),
+            "step_s_extrapolated": step_s,
+            "sample": (f"'{cfg.name}' workload: routing of all {cfg.T} tokens ({t_route:.1f} s), "
+                       f"then {len(times)} of its {len(order)} experts with routes, each with all "
+                       f"of its routes ({rows_done} rows in all), dispatch + "
+                       f"{'MXFP8 ' if mx else ''}forward + backward "
+                       f"({sum(times) / len(times):.2f} s per expert); the step is extrapolated "
+                       f"as routing + {len(order)} x the mean expert time; C++ oracle in double, "
+                       f"{O.threads()} OpenMP threads")}
 
 
 def run_reference(args, cfg):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    # each step is one bounded sample; the whole run stays near two minutes:
-    # 1024-token passes (about 1 s each on 16 cores) for up to ~100 steps,
-    # smaller samples beyond that
-    steps = max(args.steps, 1)
-    budget = min(2.0, 100.0 / steps)
-    n_tok = 1024 if budget >= 1.0 else max(128, 64 * int(16 * budget))
-    per = []
-    for _ in range(args.warmup):
-        oracle_sample(cfg, 0, budget_s=0.0, n_tok=128)
-    for _ in range(args.steps):
-        per.append(oracle_sample(cfg, 0, budget_s=budget, n_tok=n_tok))
-    v = sum(p["value"] for p in per) / len(per)
+    from synth import make_inputs
+    # the whole run stays near two minutes: as many whole-expert samples as fit
+    # (at most --steps), each one a step of this arm
+    inp = make_inputs(cfg, seed=0)
+    res = oracle_sample(cfg, inp, budget_s=90.0, max_experts=max(args.steps, 1))
+    v = res["value"]
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.T / v,
+        "steps": res["experts_timed"], "steps_requested": args.steps, "warmup": 0,
+        "ms_per_step": 1000.0 * res["step_s_extrapolated"], "extrapolated": True,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_block(cfg),
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": per[0]["cores"], "kind": "oracle",
-                         "sample": per[0]["sample"]},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                         "sample": res["sample"]},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "what": "each step of this arm is one expert of the workload (all of its routes) on the "
+                "C++ oracle; ms_per_step is the extrapolated time of a whole layer step",
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -271,18 +301,27 @@ def run_ours(args, cfg):
     dom = max(("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"), key=lambda k: stages[k])
     # the dominant GEMM's own launch time: CUDA events recorded by the library
     # around each of its launches during another `steps` whole layer steps
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
     m.profile_start(GEMM_OP[dom])
+    p0.record(stream)
     for _ in range(args.steps):
         step()
+    p1.record(stream)
     kernel_ms_total, kernel_launches = m.profile_stop()
+    region_s = p0.elapsed_time(p1) / 1000.0
     kernel_ms = kernel_ms_total / max(kernel_launches, 1)
     achieved = fl[dom] / (kernel_ms / 1000.0) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
-    peak_note = f"{peaks['source']} sustained bf16 (kernel timed inside the step)"
-    if mx and dom in ("fwd1", "fwd2", "dgrad2", "dgrad1"):
+    # the burst peak for a kernel inside a short timed region, the sustained one
+    # (power-capped, seconds-long) when the region lasts seconds
+    sustained = region_s >= 2.0
+    peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    peak_note = (f"{peaks['source']} {'sustained' if sustained else 'burst'} bf16 (the dominant "
+                 f"kernel timed inside {args.steps} steps, {region_s:.2f} s)")
+    if mx and dom in FP8_OPS:
         # dense fp8 is twice the dense bf16 rate on this part (2.25 -> 4.5 PFLOP/s nominal)
-        peak = 2.0 * peaks["bf16_tflops_sustained"]
-        peak_note = f"{peaks['source']} sustained bf16 x 2 (nominal fp8/bf16 ratio)"
+        peak = 2.0 * peak
+        peak_note += " x 2 (nominal fp8/bf16 ratio)"
     traffic, traffic_note = gemm_traffic(cfg.name, dom)
     roofline = {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({dom})", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
@@ -362,10 +401,9 @@ def run_ours(args, cfg):
     if m.read_error(buf.ws) != 0:
         raise RuntimeError("device error word set during the timed region")
 
-    # the CPU oracle is timed on the bf16 layer; an MXFP8 sample would be dominated
-    # by re-quantising 1.6 G weight values in numpy, so it is not run there
-    cpu = (oracle_sample(cfg, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline
-                                     and not mx) else None)
+    # the C++ oracle on a bounded sample of the same workload (rank 0 at N = 1)
+    cpu = (oracle_sample(cfg, inp) if (rank == 0 and world == 1 and not args.no_cpu_baseline)
+           else None)
     # router GEMM, top-k, scan + slots | dispatch, fwd1, fwd2, combine | combine bwd, dgrad2,
     # wgrad2, dgrad1, wgrad1, dispatch bwd, router bwd (2); MXFP8 adds the three weight-cache
     # quantisers, the dY quantiser and the A and Xd dequantisations
@@ -375,10 +413,7 @@ def run_ours(args, cfg):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8+bf16" if mx else "bf16",
         "data": "synthetic", "config": config_block(cfg),
-        "gemm": {"tflops": gemm_fl / (gemm_ms / 1000.0) / 1e12, "ms": gemm_ms,
-                 "pct_of_bf16_peak": 100.0 * gemm_fl / (gemm_ms / 1000.0) / 1e12
-                 / peaks["bf16_tflops_sustained"],
-                 "bf16_peak_tflops": peaks["bf16_tflops_sustained"]},
+        "gemm": gemm_summary(cfg, stages, fl, peaks, mx),
         "stage_ms": {k: round(v, 5) for k, v in stages.items()},
         "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
         "recompute": recompute, "load_balance": lb_line, "two_batch_overlap": tbo,
@@ -394,6 +429,29 @@ def run_ours(args, cfg):
 
 
 GEMM_OP = {"fwd1": 0, "fwd2": 1, "dgrad2": 2, "dgrad1": 3, "wgrad2": 4, "wgrad1": 5}
+GEMMS = ("fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1")
+FP8_OPS = ("fwd1", "fwd2", "dgrad2", "dgrad1")     # MXFP8 in the MXFP8 layer; weight gradients bf16
+
+
+def gemm_summary(cfg, stages, fl, peaks, mx):
+    """Useful TFLOP/s of the grouped GEMMs per operand type, each against its own
+    dense peak: bf16 the measured burst bf16 figure (the stage calls are timed one
+    by one), MXFP8 twice that (the nominal fp8/bf16 ratio)."""
+    out = {}
+    groups = {"mxfp8": [g for g in GEMMS if g in FP8_OPS], "bf16": [g for g in GEMMS if g not in FP8_OPS]} \
+        if mx else {"bf16": list(GEMMS)}
+    for name, ops in groups.items():
+        ms = sum(stages[g] for g in ops)
+        flops = sum(fl[g] for g in ops)
+        peak = peaks["bf16_tflops"] * (2.0 if name == "mxfp8" else 1.0)
+        tf = flops / (ms / 1000.0) / 1e12
+        out[name] = {"ops": ops, "ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak,
+                     "per_op_frac": {g: fl[g] / (stages[g] / 1000.0) / 1e12 / peak for g in ops},
+                     "peak_source": f"{peaks['source']} burst bf16" + (" x 2 (nominal fp8/bf16 ratio)"
+                                                                         if name == "mxfp8" else "")}
+    all_ms = sum(stages[g] for g in GEMMS)
+    out["all"] = {"ms": all_ms, "tflops": sum(fl[g] for g in GEMMS) / (all_ms / 1000.0) / 1e12}
+    return out
 GEMM_SOURCES = ("moe_expert_layer_softmax_gb300/csrc/gemm.cu",
                 "moe_expert_layer_softmax_gb300/csrc/common.cuh")
 
@@ -413,26 +471,30 @@ def gemm_source_hash(root: str = ROOT) -> str:
     return h.hexdigest()
 
 
+DRAM_RECORD = os.path.join(ROOT, "profiles", "dram_per_launch.json")
+
+
 def gemm_traffic(workload: str, op: str):
-    """DRAM bytes (read + write) of one launch of GEMM `op`, from the committed
-    ncu summary of this workload; None when the GEMM sources changed since."""
-    import re
-    path = os.path.join(ROOT, "profiles", f"grouped_gemm_dram_{workload}.md")
-    if not os.path.exists(path):
-        return None, "no ncu capture for this workload"
-    with open(path) as fh:
-        text = fh.read()
-    mt = re.search(r"<!-- dram: (\{.*?\}) -->", text, re.S)
-    if mt is None:
-        return None, "no dram record in " + os.path.relpath(path, ROOT)
-    rec = json.loads(mt.group(1))
+    """DRAM bytes (read + write) of one launch of GEMM `op` on `workload`, from the
+    committed record of ncu captures (scaled from a reduced case of the same
+    shape when the record says so); None when the GEMM sources changed since."""
+    if not os.path.exists(DRAM_RECORD):
+        return None, "no ncu DRAM record"
+    with open(DRAM_RECORD) as fh:
+        recs = json.load(fh).get("records", [])
+    rec = next((r for r in recs if r.get("workload") == workload), None)
+    if rec is None:
+        return None, f"no ncu capture for the '{workload}' workload"
     if rec.get("source_sha256") != gemm_source_hash():
         return None, "GEMM sources changed since the ncu capture"
     ops = rec.get("ops", {})
     if op not in ops:
         return None, f"{op} not in the ncu capture"
-    return (int(ops[op]["read"]) + int(ops[op]["write"]),
-            "dram__bytes_read.sum + dram__bytes_write.sum, " + os.path.relpath(path, ROOT))
+    scale = float(rec.get("scale", 1.0))
+    note = "dram__bytes_read.sum + dram__bytes_write.sum, " + os.path.relpath(DRAM_RECORD, ROOT)
+    if scale != 1.0:
+        note += f" (captured on '{rec['captured_on']}', x {scale:g} for the full launch)"
+    return int(round((int(ops[op]["read"]) + int(ops[op]["write"])) * scale)), note
 
 
 def load_peaks():
@@ -791,7 +853,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="fine_grained")
+    ap.add_argument("--config", default="mxfp8")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",

@@ -16,7 +16,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 sys.path.insert(0, ROOT)
 
-from oracle import moe_oracle as O          # noqa: E402
+from oracle import cpp as O          # noqa: E402
 from synth import CONFIGS, make_inputs, zipf_expert_bias  # noqa: E402
 
 TARGET = 0.15

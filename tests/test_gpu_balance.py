@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe_oracle as O
+from oracle import cpp as O
 from synth import make_inputs
 from gpu_util import f64, max_abs_rel, to_dev_bf16
 

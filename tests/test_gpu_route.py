@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe_oracle as O
+from oracle import cpp as O
 from synth import CONFIGS, make_inputs
 from gpu_util import max_abs_rel, near_tie_tokens, to_dev_bf16
 

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe_oracle as O
+from oracle import cpp as O
 from synth import bf16_bits_from_f32, make_inputs
 from gpu_util import bf16_bits_of, f64, max_abs_rel, to_dev_bf16
 

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe_oracle as O
+from oracle import cpp as O
 from synth import make_inputs, f32_from_bf16_bits
 
 

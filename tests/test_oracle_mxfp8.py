@@ -12,8 +12,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import moe_oracle as O
-from synth import make_inputs
+from oracle import cpp as O
+from synth import bf16_bits_from_f32, make_inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -131,19 +131,96 @@ def test_payload_bytes_per_value():
     assert g["bf16_bytes_per_value"] == 2
 
 
-def test_mxfp8_layer_without_quantisation_is_the_bf16_layer(monkeypatch):
-    inp = make_inputs(T=40, d=64, E=4, k=2, f=64, seed=12)
+def _block_dot(a, b):
+    """OCP MX block dot product of the rows of a [n, K] and b [m, K], both
+    quantised along K: sum over 32-blocks of 2^(s_a + s_b) times the sum of the
+    E4M3 code-value products of the block (exact in float64)."""
+    ca, sa = O.quantize_mxfp8(a)
+    cb, sb = O.quantize_mxfp8(b)
+    n, K = ca.shape
+    m = cb.shape[0]
+    va = O.E4M3_VALUES[ca].reshape(n, K // 32, 32)
+    vb = O.E4M3_VALUES[cb].reshape(m, K // 32, 32)
+    dots = np.einsum("nbk,mbk->nmb", va, vb)
+    scale = np.exp2(sa.astype(np.int64)[:, None, :] - 127 + sb.astype(np.int64)[None, :, :] - 127)
+    return (dots * scale).sum(-1)
+
+
+def _spread(bits, rng, axes_exp):
+    """bf16 values times 2^(r_row + c_col) (exact): magnitudes that change along
+    both axes, so that the block scales depend on which axis a block runs along."""
+    v = O.as_f64(bits)
+    sh = v.shape
+    e = np.zeros(sh)
+    for ax, lim in axes_exp:
+        shape = [1] * len(sh)
+        shape[ax] = sh[ax]
+        e = e + rng.integers(-lim, lim + 1, shape)
+    return bf16_bits_from_f32((v * np.exp2(e)).astype(np.float32))
+
+
+def test_mxfp8_layer_quantises_each_gemm_operand_along_its_contraction_axis():
+    """Every quantised GEMM of the MXFP8 layer, restated as the MX block dot
+    product of its operands quantised along the contraction axis: x along d
+    (GEMM1, with W_gate/W_up rows along d), A along f (GEMM2, with W_down rows
+    along f), dY along d (data gradient 2, with W_down^T rows along d), dH and
+    dU along f (data gradient 1, with W_gate^T / W_up^T rows along f); the
+    weight gradients use the unquantised gradients and the quantised
+    activations.  Operand magnitudes vary along both axes, and quantising any
+    operand along its other axis is shown to change the result."""
+    rng = np.random.default_rng(31)
+    T, d, E, k, f = 24, 64, 3, 2, 96
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=31)
+    inp["x"] = _spread(inp["x"], rng, [(0, 4), (1, 4)])
+    for n in ("w_gate", "w_up", "w_down"):
+        inp[n] = _spread(inp[n], rng, [(1, 4), (2, 4)])
+    inp["d_out"] = _spread(inp["d_out"], rng, [(0, 3), (1, 3)])
     args = (inp["x"], inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"], inp["w_down"])
-    monkeypatch.setattr(O, "_qdq", lambda a: O.as_f64(a))
-    q = O.layer_forward_mxfp8(*args, k=2, bm=16)
-    b = O.layer_forward(*args, k=2, bm=16)
-    np.testing.assert_allclose(q["out"], b["out"], rtol=1e-13, atol=1e-15)
-    qb = O.layer_backward_mxfp8(q, inp["d_out"], inp["x"], inp["w_router"], inp["w_gate"],
-                                inp["w_up"], inp["w_down"])
-    bb = O.layer_backward(b, inp["d_out"], inp["x"], inp["w_router"], inp["w_gate"],
-                          inp["w_up"], inp["w_down"])
-    for n in ("dx", "dW_gate", "dW_up", "dW_down", "dW_router", "dlogits"):
-        np.testing.assert_allclose(qb[n], bb[n], rtol=1e-12, atol=1e-14, err_msg=n)
+    fwd = O.layer_forward_mxfp8(*args, k=k, bm=8)
+    bwd = O.layer_backward_mxfp8(fwd, inp["d_out"], inp["x"], inp["w_router"], inp["w_gate"],
+                                 inp["w_up"], inp["w_down"])
+    X = O.as_f64(inp["x"])
+    Wg, Wu, Wd = (O.as_f64(inp[n]) for n in ("w_gate", "w_up", "w_down"))
+    ro = fwd["row_offsets"]
+    ros = fwd["route_of_slot"]
+
+    def close(got, want):
+        assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max()
+
+    wrong_axis_seen = 0
+    for e in range(E):
+        a, b = int(ro[e]), int(ro[e + 1])
+        real = ros[a:b] >= 0
+        if not real.any():
+            continue
+        rows = np.arange(a, b)[real]
+        tok = ros[rows] // k
+        H = _block_dot(X[tok], Wg[e])
+        U = _block_dot(X[tok], Wu[e])
+        close(fwd["H"][rows], H)
+        close(fwd["U"][rows], U)
+        A = fwd["A"][rows]
+        close(A, O.silu(H) * U)
+        close(fwd["Y"][rows], _block_dot(A, Wd[e]))
+        dY = bwd["dY"][rows]
+        dA = _block_dot(dY, Wd[e].T)
+        close(bwd["dH"][rows], dA * U * O.silu_grad(H))
+        close(bwd["dU"][rows], dA * O.silu(H))
+        dH, dU = bwd["dH"][rows], bwd["dU"][rows]
+        close(bwd["dXd"][rows], _block_dot(dH, Wg[e].T) + _block_dot(dU, Wu[e].T))
+        Aq = O.dequantize_mxfp8(*O.quantize_mxfp8(A))
+        Xq = O.dequantize_mxfp8(*O.quantize_mxfp8(X[tok]))
+        close(bwd["dW_down"][e], dY.T @ Aq)
+        close(bwd["dW_gate"][e], dH.T @ Xq)
+        close(bwd["dW_up"][e], dU.T @ Xq)
+        # the same operands quantised along the other axis give other numbers
+        Wg_other = O.dequantize_mxfp8(*O.quantize_mxfp8(Wg[e].T)).T
+        Xq_other = O.dequantize_mxfp8(*O.quantize_mxfp8(X[tok].T)).T if len(tok) % 32 == 0 else None
+        if not np.allclose(Xq @ Wg_other.T, H, rtol=0, atol=1e-9 * np.abs(H).max()):
+            wrong_axis_seen += 1
+        if Xq_other is not None:
+            assert not np.allclose(Xq_other, Xq)
+    assert wrong_axis_seen > 0
 
 
 def test_mxfp8_layer_is_close_to_the_bf16_layer():
