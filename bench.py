@@ -309,6 +309,7 @@ def run_ours(args, cfg):
         step()
     p1.record(stream)
     kernel_ms_total, kernel_launches = m.profile_stop()
+    torch.cuda.synchronize()
     region_s = p0.elapsed_time(p1) / 1000.0
     kernel_ms = kernel_ms_total / max(kernel_launches, 1)
     achieved = fl[dom] / (kernel_ms / 1000.0) / 1e12

@@ -186,7 +186,8 @@ MOE_API int moe_route(const moe_shape_t* shape, const void* x, const void* w_rou
  * (256 + roundup256(ceil(T/16)*E*4) + roundup256(T*k*4) bytes) return
  * MOE_ERR_SCRATCH_LIMIT and queue nothing.  Nothing is allocated.
  *   dev_error  device int32 (nullable): receives the call's device error bits.
- * The first call on a device looks up the array's address with that device
+ * The first call on a device (and the first after each moe_init of it, e.g.
+ * following a device reset) looks up the array's address with that device
  * current; make it before any stream capture starts.  All calls share the array
  * (each clears the error word; the rest is rewritten): calls that overlap on the
  * GPU race and must be serialised by the caller. */

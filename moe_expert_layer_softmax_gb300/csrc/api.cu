@@ -316,6 +316,7 @@ int moe_init(int device) {
   int sms = 0;
   MOE_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
   MOE_CUDA(gemm_init_attributes());
+  noalloc_forget_device(device);
   g_dev[device].sm_count = sms;
   g_dev[device].ready = true;
   return MOE_OK;

@@ -167,6 +167,7 @@ cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
 cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t rows, int K,
                                     void* out, cudaStream_t s);
 cudaError_t gemm_init_attributes();
+void noalloc_forget_device(int dev);   // moe_route_noalloc's cached scratch address
 int gemm_set_inject_stall(int mode);   // returns the previous mode
 
 }  // namespace moe

@@ -15,8 +15,9 @@
 //     more are rejected with MOE_ERR_SCRATCH_LIMIT before any work is queued.
 //     Every GPU that loads this library keeps the array until the process ends.
 //   - The first call on a device looks up the array's device address (with that
-//     device current) and caches it.  Make that first call before any stream
-//     capture begins.
+//     device current) and caches it; moe_init drops the cached address, so the
+//     first call after a moe_init (e.g. after a device reset) looks it up
+//     again.  Make that first call before any stream capture begins.
 //   - All calls on a device share the one array and it keeps what the last call
 //     left there.  Each call clears the error word itself; the histograms and
 //     ranks are fully rewritten.  Calls whose work overlaps on the GPU (e.g. on
@@ -59,6 +60,15 @@ int scratch_address(void** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+// moe_init calls this: after a device reset the module is loaded again and the
+// array may sit at another address, so the cached one must not be reused.
+void noalloc_forget_device(int dev) {
+  if (dev < 0 || dev >= kMaxDev) return;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  g_scratch_addr[dev] = nullptr;
+}
+
 }  // namespace moe
 
 using namespace moe;

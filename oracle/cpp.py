@@ -28,6 +28,7 @@ __all__ = [
     "build", "threads", "as_f64", "router_logits", "softmax_topk_gates", "expert_counts",
     "exclusive_scan", "tile_layout", "assign_slots", "dispatch", "silu", "silu_grad",
     "expert_ffn_forward", "combine", "combine_backward", "expert_ffn_backward",
+    "expert_ffn_forward_mxfp8", "expert_ffn_backward_mxfp8",
     "dispatch_backward", "router_backward", "load_balance", "load_balance_dlogits",
     "layer_forward", "layer_backward", "dense_forward", "E4M3_VALUES", "E4M3_MAX",
     "e4m3_encode", "mx_scale_exponent", "quantize_mxfp8", "dequantize_mxfp8",
@@ -244,6 +245,12 @@ def expert_ffn_forward(Xd, w_gate, w_up, w_down, row_offsets):
     return H, U, A, Y
 
 
+def expert_ffn_forward_mxfp8(Xd, w_gate, w_up, w_down, row_offsets):
+    """The MXFP8 forward's per-expert part on dispatched (already quantised)
+    rows: returns H, U, A, Aq, Y."""
+    return _expert_forward(Xd, w_gate, w_up, w_down, row_offsets, True)
+
+
 def combine(Y, gates, slot_of_route, T: int, k: int) -> np.ndarray:
     Y = as_f64(Y)
     g = _c(as_f64(gates).reshape(T, k), np.float64)
@@ -293,6 +300,11 @@ def _expert_backward(dY, Xd, H, U, A, w_gate, w_up, w_down, row_offsets, mx: boo
 
 def expert_ffn_backward(dY, Xd, H, U, A, w_gate, w_up, w_down, row_offsets):
     return _expert_backward(dY, Xd, H, U, A, w_gate, w_up, w_down, row_offsets, False)
+
+
+def expert_ffn_backward_mxfp8(dY, Xd, H, U, Aq, w_gate, w_up, w_down, row_offsets):
+    """The MXFP8 backward's per-expert part (Aq: the forward's quantised A)."""
+    return _expert_backward(dY, Xd, H, U, Aq, w_gate, w_up, w_down, row_offsets, True)
 
 
 def dispatch_backward(dXd, slot_of_route, T: int, k: int) -> np.ndarray:

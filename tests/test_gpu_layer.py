@@ -2,6 +2,8 @@
 the oracle, on small shapes and on the full-size workloads (the same calls and
 launch configuration the benchmark times), plus CUDA-graph capture/replay.
 GPU only."""
+import warnings
+
 import numpy as np
 import pytest
 import torch
@@ -36,6 +38,7 @@ def run_layer(m, dev, inp, k, use_router, logits32=None, backward=True):
     if backward:
         res.update({n: f64(v) for n, v in buf.grads.items()
                     if n in ("dx", "dw_router", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits")})
+    res["_call"] = (buf, t, wr, bias)
     return res
 
 
@@ -94,12 +97,34 @@ def check_full_path(m, dev, inp, k, backward=True):
     if same.all():
         for n in ("counts", "offsets", "tile_offsets", "slot_of_route"):
             np.testing.assert_array_equal(g[n], fwd[n], err_msg=n)
+    else:
+        # the routing metadata then differs by construction; the bit-exact
+        # routing tests (shared logits) cover it
+        warnings.warn(f"{int((~same).sum())} near-tie token(s) routed differently from the "
+                      "oracle: counts/offsets/slots not compared, those tokens left out")
     assert max_abs_rel(g["out"][same], fwd["out"][same]) <= TOL
+    g["_oracle"] = (fwd, None, same)
     if backward:
         bwd = O.layer_backward(fwd, inp["d_out"], inp["x"], inp["w_router"], inp["w_gate"],
                                inp["w_up"], inp["w_down"])
         compare_grads(g, bwd, use_router=True, rows=same)
+        g["_oracle"] = (fwd, bwd, same)
     return g
+
+
+def recompute_matches(m, g, use_router):
+    """Backward again with recompute after overwriting every saved activation
+    and gradient with NaN; the gradients must match the oracle's backward."""
+    buf, t, wr, bias = g["_call"]
+    fwd, bwd, rows = g["_oracle"]
+    for n in ("xd", "h", "u", "a", "y"):
+        buf.saved[n].fill_(float("nan"))
+    for n in GRAD_NAMES:
+        buf.grads[n].fill_(float("nan"))
+    m.backward(buf, t["d_out"], t["x"], wr, t["w_gate"], t["w_up"], t["w_down"], recompute=True)
+    assert m.read_error(buf.ws) == 0
+    got = {n: f64(buf.grads[n]) for n in GRAD_NAMES}
+    compare_grads(got, bwd, use_router=use_router, rows=rows)
 
 
 @pytest.mark.parametrize("T,d,E,k,f", SMALL[:3] + SMALL[5:7], ids=lambda v: str(v))
@@ -119,7 +144,8 @@ def test_tiny_forward_workload(moe_gpu):
 
 @pytest.mark.parametrize("name", ["fine_grained", "large_pool", "skewed"])
 def test_full_size_workload(moe_gpu, name):
-    """Full-size bf16 workloads, forward and backward, same calls as the benchmark."""
+    """Full-size bf16 workloads, forward and backward, same calls as the benchmark;
+    on the fine-grained workload also the backward with per-layer recompute."""
     m, dev = moe_gpu
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, seed=0)
@@ -128,6 +154,65 @@ def test_full_size_workload(moe_gpu, name):
         assert (g["counts"] == 0).sum() >= 4
         empty = np.where(g["counts"] == 0)[0]
         assert (g["dw_gate"][empty] == 0).all() and (g["dw_down"][empty] == 0).all()
+    if name == "fine_grained":
+        recompute_matches(m, g, use_router=True)
+
+
+@pytest.mark.parametrize("T,d,E,k,f", [(1000, 512, 16, 4, 256), (513, 256, 64, 8, 256)],
+                         ids=lambda v: str(v))
+def test_recompute_backward_matches_the_oracle(moe_gpu, T, d, E, k, f):
+    """Per-layer recompute (the report's Section 24.3, Evidence 11): the backward
+    rebuilds Xd, H, U, A, Y from x and the routing metadata; its gradients match
+    the oracle's backward."""
+    m, dev = moe_gpu
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=23 + T)
+    g = check_full_path(m, dev, inp, k)
+    recompute_matches(m, g, use_router=True)
+
+
+def test_two_batch_overlap_on_two_streams_matches_the_oracle(moe_gpu):
+    """Two halves of the batch, each a whole layer forward + backward with its
+    own buffers, run on two streams at once (the single-GPU analogue of the
+    report's two-batch overlap, Section 24.2, Evidence 5): each half's out and dx
+    match the oracle's whole-batch rows, and the two halves' weight gradients
+    add up to the oracle's."""
+    m, dev = moe_gpu
+    T, d, E, k, f = 2048, 512, 16, 4, 512
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=29)
+    L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
+    fwd = O.layer_forward(inp["x"], None, None, inp["w_gate"], inp["w_up"], inp["w_down"], k,
+                          logits=L32)
+    bwd = O.layer_backward(fwd, inp["d_out"], inp["x"], None, inp["w_gate"], inp["w_up"],
+                           inp["w_down"])
+    t = {n: to_dev_bf16(inp[n], dev) for n in ("x", "w_gate", "w_up", "w_down", "d_out")}
+    h = T // 2
+    s2 = m.shape(h, d, E, k, f)
+    bufs = [m.allocate(s2) for _ in range(2)]
+    outs = [torch.empty(h, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    main = torch.cuda.current_stream()
+    for i in range(2):
+        bufs[i].saved["logits"].copy_(torch.from_numpy(L32[i * h:(i + 1) * h]))
+        m.clear_error(bufs[i].ws)
+    torch.cuda.synchronize()
+    for i in range(2):
+        streams[i].wait_stream(main)
+        with torch.cuda.stream(streams[i]):
+            sl = slice(i * h, (i + 1) * h)
+            m.forward(bufs[i], t["x"][sl], None, None, t["w_gate"], t["w_up"], t["w_down"], outs[i],
+                      stream=streams[i])
+            m.backward(bufs[i], t["d_out"][sl], t["x"][sl], None, t["w_gate"], t["w_up"],
+                       t["w_down"], stream=streams[i])
+    for st in streams:
+        main.wait_stream(st)
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert m.read_error(bufs[i].ws) == 0
+    assert max_abs_rel(np.concatenate([f64(o) for o in outs]), fwd["out"]) <= TOL
+    assert max_abs_rel(np.concatenate([f64(b.grads["dx"]) for b in bufs]), bwd["dx"]) <= TOL
+    for mine, ref in [("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down")]:
+        tot = f64(bufs[0].grads[mine]) + f64(bufs[1].grads[mine])
+        assert max_abs_rel(tot, bwd[ref]) <= TOL, mine
 
 
 def test_graph_capture_replays_bitwise(moe_gpu):

@@ -279,18 +279,21 @@ def test_mx_layer_small(mcase):
 
 
 def test_mx_full_size_workload_sampled(moe_gpu):
-    """32768 tokens, d=4096, 64 experts, top-8, f=2048: routing and the dispatched
-    codes in full, two experts' forward rows and weight gradients against the
-    oracle's per-expert MXFP8 math, and the natural-layout weight gradients bit
-    for bit against the layer's."""
+    """32768 tokens, d=4096, 64 experts, top-8, f=2048 (the benchmark's workload
+    and launch configuration): routing and the dispatched codes in full; eight
+    experts in full (H and Y rows, dXd rows and all three weight gradients) and
+    the out, dx and d_gates rows of 256 seeded tokens against the C++ oracle's
+    MXFP8 layer; the natural-layout weight gradients bit for bit against the
+    layer's."""
     m, dev = moe_gpu
     cfg = CONFIGS["mxfp8"]
+    k, E = cfg.k, cfg.E
     inp = make_inputs(cfg, seed=0)
     L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
-    buf, out, err = run_mx_layer(m, dev, inp, cfg.k, L32)
+    buf, out, err = run_mx_layer(m, dev, inp, k, L32)
     assert err == 0
-    idx, gates = O.softmax_topk_gates(L32, cfg.k)
-    counts = O.expert_counts(idx, cfg.E)
+    idx, gates = O.softmax_topk_gates(L32, k)
+    counts = O.expert_counts(idx, E)
     tile_offsets, row_offsets = O.tile_layout(counts, 128)
     sor, ros = O.assign_slots(idx, row_offsets)
     np.testing.assert_array_equal(buf.saved["topk_idx"].cpu().numpy(), idx)
@@ -300,29 +303,47 @@ def test_mx_full_size_workload_sampled(moe_gpu):
     xs_all = sf_unpack(buf.mx["xd_s"].cpu().numpy(), n, cfg.d // 32)
     codes, scales = q_rows(O.as_f64(inp["x"]))
     real = ros >= 0
-    np.testing.assert_array_equal(xq_all[: len(ros)][real], codes[ros[real] // cfg.k])
-    np.testing.assert_array_equal(xs_all[: len(ros)][real], scales[ros[real] // cfg.k])
-    assert torch.isfinite(out.float()).all()
-    Y = f64(buf.saved["y"])
-    H = f64(buf.saved["h"])
+    np.testing.assert_array_equal(xq_all[: len(ros)][real], codes[ros[real] // k])
+    np.testing.assert_array_equal(xs_all[: len(ros)][real], scales[ros[real] // k])
+    xq = O.dequantize_mxfp8(codes, scales)          # the quantised tokens, [T, d]
+    del xq_all, xs_all, codes, scales
     dO = O.as_f64(inp["d_out"])
-    for e in (int(np.argmax(counts)), int(np.argmin(counts))):
-        a, b_ = int(row_offsets[e]), int(row_offsets[e]) + int(counts[e])
-        Xe = O.dequantize_mxfp8(codes, scales)[ros[a:b_] // cfg.k]
-        He = Xe @ O._qdq(inp["w_gate"][e]).T
-        Ue = Xe @ O._qdq(inp["w_up"][e]).T
-        Aq = O._qdq(O.silu(He) * Ue)
-        Ye = Aq @ O._qdq(inp["w_down"][e]).T
-        assert max_abs_rel(H[a:b_], He) <= TOL
-        assert max_abs_rel(Y[a:b_], Ye) <= TOL
-        # weight gradient of W_down for this expert: dY_e^T Aq_e with dY = g * dOut
-        gsel = gates.reshape(-1)[ros[a:b_]]
-        dYe = gsel[:, None] * dO[ros[a:b_] // cfg.k]
-        dWd = dYe.T @ Aq
-        assert max_abs_rel(f64(buf.grads["dw_down"][e]), dWd) <= TOL
+    g = buf.grads
+    rng = np.random.default_rng(0)
+    # ---- eight experts in full
+    big, small = int(np.argmax(counts)), int(np.argmin(counts))
+    others = [int(e) for e in rng.permutation(E) if e not in (big, small)][:6]
+    for e in [big, small] + others:
+        a, c = int(row_offsets[e]), int(counts[e])
+        routes = ros[a:a + c]
+        tok = routes // k
+        ro1 = np.array([0, c])
+        w = [inp[nm][e:e + 1] for nm in ("w_gate", "w_up", "w_down")]
+        H, U, A, Aq, Y = O.expert_ffn_forward_mxfp8(xq[tok], *w, ro1)
+        assert max_abs_rel(f64(buf.saved["h"][a:a + c]), H) <= TOL, ("H", e)
+        assert max_abs_rel(f64(buf.saved["u"][a:a + c]), U) <= TOL, ("U", e)
+        assert max_abs_rel(f64(buf.saved["y"][a:a + c]), Y) <= TOL, ("Y", e)
+        dY = gates.reshape(-1)[routes][:, None] * dO[tok]
+        gb = O.expert_ffn_backward_mxfp8(dY, xq[tok], H, U, Aq, *w, ro1)
+        assert max_abs_rel(f64(g["dxd"][a:a + c]), gb["dXd"]) <= TOL, ("dXd", e)
+        for mine, ref in (("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down")):
+            assert max_abs_rel(f64(g[mine][e]), gb[ref][0]) <= TOL, (mine, e)
+    # ---- out, dx and d_gates of 256 seeded tokens, through all their experts
+    ts = np.sort(rng.choice(cfg.T, 256, replace=False))
+    idx_s, g_s = idx[ts], gates[ts]
+    _, ro_s = O.tile_layout(O.expert_counts(idx_s, E), 1)
+    sor_s, _ = O.assign_slots(idx_s, ro_s)
+    rows_s = int(ro_s[-1])
+    Xd_s = O.dispatch(xq[ts], sor_s, k, rows_s)
+    H, U, A, Aq, Y = O.expert_ffn_forward_mxfp8(Xd_s, inp["w_gate"], inp["w_up"], inp["w_down"], ro_s)
+    assert max_abs_rel(f64(out)[ts], O.combine(Y, g_s, sor_s, 256, k)) <= TOL
+    dg, dY = O.combine_backward(dO[ts], Y, g_s, sor_s, 256, k, rows_s)
+    assert max_abs_rel(f64(g["d_gates"])[ts], dg) <= TOL
+    gb = O.expert_ffn_backward_mxfp8(dY, Xd_s, H, U, Aq, inp["w_gate"], inp["w_up"], inp["w_down"],
+                                     ro_s)
+    assert max_abs_rel(f64(g["dx"])[ts], O.dispatch_backward(gb["dXd"], sor_s, 256, k)) <= TOL
     # the natural-layout weight gradients on the layer's own codes and scales
     # equal, bit for bit, the layer's (global dequantisation + BF16) ones
-    g = buf.grads
     s = m.shape(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, prec=m.MXFP8)
     to = buf.saved["tile_offsets"]
     dWd = torch.empty_like(g["dw_down"])
@@ -334,6 +355,71 @@ def test_mx_full_size_workload_sampled(moe_gpu):
     assert m.read_error(buf.ws) == 0
     assert torch.equal(dWd, g["dw_down"])
     assert torch.equal(dWg, g["dw_gate"]) and torch.equal(dWu, g["dw_up"])
+
+
+def test_mx_recompute_backward_matches_the_oracle(mcase):
+    """MXFP8 backward with recompute (saved activations overwritten with NaN
+    first) against the C++ oracle's MXFP8 backward."""
+    c = mcase
+    m, dev = c["m"], c["dev"]
+    buf, out, err = run_mx_layer(m, dev, c["inp"], c["k"], c["L32"])
+    assert err == 0
+    for n in ("h", "u", "y"):
+        buf.saved[n].fill_(float("nan"))
+    for n in ("xd_q", "a_q"):
+        buf.mx[n].fill_(0x7F)
+    for n in ("dx", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits"):
+        buf.grads[n].fill_(float("nan"))
+    t = {nm: to_dev_bf16(c["inp"][nm], dev) for nm in ("x", "w_gate", "w_up", "w_down", "d_out")}
+    m.backward(buf, t["d_out"], t["x"], None, t["w_gate"], t["w_up"], t["w_down"], recompute=True)
+    assert m.read_error(buf.ws) == 0
+    b = c["bwd"]
+    for mine, ref in [("dx", "dx"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"),
+                      ("dw_down", "dW_down"), ("d_gates", "d_gates"), ("dlogits", "dlogits")]:
+        assert max_abs_rel(f64(buf.grads[mine]), b[ref]) <= TOL, mine
+
+
+def test_mx_graph_capture_replays_bitwise(mcase):
+    """Weight caches + MXFP8 forward + backward capture into one CUDA graph (no
+    host sync inside), replay bit for bit, and match the MXFP8 oracle."""
+    c = mcase
+    m, dev = c["m"], c["dev"]
+    T, d, E, k, f = c["T"], c["d"], c["E"], c["k"], c["f"]
+    s = c["s"]
+    buf = m.allocate(s)
+    t = {nm: to_dev_bf16(c["inp"][nm], dev) for nm in ("x", "w_gate", "w_up", "w_down", "d_out")}
+    buf.saved["logits"].copy_(torch.from_numpy(c["L32"]))
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    names = ("dx", "dw_gate", "dw_up", "dw_down", "d_gates", "dlogits")
+
+    def step():
+        m.build_mx_weights(s, t["w_gate"], t["w_up"], t["w_down"], buf.mx_weights)
+        m.forward(buf, t["x"], None, None, t["w_gate"], t["w_up"], t["w_down"], out)
+        m.backward(buf, t["d_out"], t["x"], None, t["w_gate"], t["w_up"], t["w_down"])
+
+    m.clear_error(buf.ws)
+    step()
+    torch.cuda.synchronize()
+    eager = [out.clone()] + [buf.grads[n].clone() for n in names]
+    graph = torch.cuda.CUDAGraph()
+    s_cap = torch.cuda.Stream()
+    s_cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_cap):
+        with torch.cuda.graph(graph, stream=s_cap, capture_error_mode="global"):
+            step()
+    torch.cuda.current_stream().wait_stream(s_cap)
+    for _ in range(3):
+        out.zero_()
+        for n in names:
+            buf.grads[n].zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, [out] + [buf.grads[n] for n in names]):
+            assert torch.equal(a, b)
+    assert m.read_error(buf.ws) == 0
+    assert max_abs_rel(f64(out), c["fwd"]["out"]) <= TOL
+    assert max_abs_rel(f64(buf.grads["dx"]), c["bwd"]["dx"]) <= TOL
+    assert max_abs_rel(f64(buf.grads["dw_gate"]), c["bwd"]["dW_gate"]) <= TOL
 
 
 def test_mx_recompute_backward_is_bitwise_the_saved_one(mcase):

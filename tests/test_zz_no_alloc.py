@@ -36,7 +36,8 @@ def _args(o):
 
 
 @pytest.mark.parametrize("T,d,E,k,use_router", [(3000, 512, 64, 8, True), (777, 128, 16, 3, False),
-                                                (8192, 2048, 32, 4, True)])
+                                                (8192, 2048, 32, 4, True), (50, 128, 256, 32, False),
+                                                (300, 128, 1, 1, False), (5000, 128, 250, 8, False)])
 def test_noalloc_route_matches_route_twice(moe_gpu, T, d, E, k, use_router):
     m, dev = moe_gpu
     inp = make_inputs(T=T, d=d, E=E, k=k, f=128, seed=T + E, with_grad=False)
