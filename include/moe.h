@@ -183,7 +183,7 @@ MOE_API int moe_route(const moe_shape_t* shape, const void* x, const void* w_rou
  * word, per-block histograms, per-route ranks) lives in one static device
  * array of 2 MiB inside the library, kept by every GPU that loads the library
  * until the process exits.  Shapes needing more scratch than that
- * (256 + roundup256(ceil(T/16)*E*4) + roundup256(T*k*4) bytes) return
+ * (256 + roundup256(ceil(T/128)*E*4) + roundup256(T*k*4) bytes) return
  * MOE_ERR_SCRATCH_LIMIT and queue nothing.  Nothing is allocated.
  *   dev_error  device int32 (nullable): receives the call's device error bits.
  * The first call on a device (and the first after each moe_init of it, e.g.

@@ -112,19 +112,9 @@ int route_impl(const moe_shape_t* s, const void* x, const void* w_router, const 
   int32_t* err = at<int32_t>(ws, 0);
   int32_t* hist = at<int32_t>(ws, w.hist);
   int32_t* rank = at<int32_t>(ws, w.rank);
-  if (w_router != nullptr) {
-    GemmLaunch g = {};
-    g.op = OP_ROUTER;
-    g.T = s->T; g.d = s->d_model; g.E = s->n_experts; g.f = s->d_ff;
-    g.rows_max = rows_max_of(s);
-    g.a0 = x; g.w0 = w_router; g.bias = bias; g.out0 = logits; g.err = err;
-    MOE_CUDA(launch_grouped_gemm(g, st));
-  }
-  MOE_CUDA(launch_route_topk(logits, s->T, s->n_experts, s->top_k, topk_idx, gates, rank, hist,
-                             err, st));
-  MOE_CUDA(launch_route_scan_slots(hist, n_route_blocks(s), topk_idx, rank, s->T, s->n_experts,
-                                   s->top_k, rows_max_of(s), counts, offsets, tile_offsets,
-                                   slot_of_route, route_of_slot, err, st));
+  MOE_CUDA(launch_route(s->T, s->d_model, s->n_experts, s->top_k, rows_max_of(s), x, w_router, bias,
+                        logits, topk_idx, gates, counts, offsets, tile_offsets, slot_of_route,
+                        route_of_slot, err, hist, rank, st));
   return MOE_OK;
 }
 

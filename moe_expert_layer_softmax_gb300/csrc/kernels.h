@@ -28,9 +28,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Tokens handled by one block of the top-k kernel; the per-block expert
-// histograms and route ranks are taken over these tokens.
-constexpr int kRouteTokensPerBlock = 16;
+// Tokens per routing block: the top-k kernels write one expert histogram per
+// block and each route's rank within its expert among the block's routes.
+constexpr int kRouteTokensPerBlock = 128;
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -42,6 +42,8 @@ const DeviceInfo* device_info();
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
                               float* gates, int32_t* local_rank, int32_t* block_hist,
                               int32_t* err, cudaStream_t s);
+// block_hist [ceil(T / kRouteTokensPerBlock), E] is replaced by each block's
+// first row per expert; counts, offsets, tile_offsets written
 cudaError_t launch_route_scan(int32_t* block_hist, int n_blocks, int E, int32_t* counts,
                               int32_t* offsets, int32_t* tile_offsets, cudaStream_t s);
 cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_rank,
@@ -49,13 +51,14 @@ cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_ran
                                const int32_t* tile_offsets, int T, int E, int k, int64_t rows_max,
                                int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
                                cudaStream_t s);
-// scan + slots in one kernel (block_hist is only read)
-cudaError_t launch_route_scan_slots(const int32_t* block_hist, int n_blocks,
-                                    const int32_t* topk_idx, const int32_t* local_rank, int T,
-                                    int E, int k, int64_t rows_max, int32_t* counts,
-                                    int32_t* offsets, int32_t* tile_offsets,
-                                    int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
-                                    cudaStream_t s);
+// The whole routing sequence (moe_route and moe_route_noalloc): the router GEMM
+// when w_router is given, a top-k kernel, the scan, the slots.  hist holds
+// ceil(T / kRouteTokensPerBlock) * E ints, rank T * k ints.
+cudaError_t launch_route(int T, int d, int E, int k, int64_t rows_max, const void* x,
+                         const void* w_router, const float* bias, float* logits,
+                         int32_t* topk_idx, float* gates, int32_t* counts, int32_t* offsets,
+                         int32_t* tile_offsets, int32_t* slot_of_route, int32_t* route_of_slot,
+                         int32_t* err, int32_t* hist, int32_t* rank, cudaStream_t s);
 
 // ---------------------------------------------------------------- data movement
 cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
@@ -150,7 +153,6 @@ struct GemmLaunch {
   int32_t* err;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t s);
-
 // ---------------------------------------------------------------- MXFP8
 // block_axis 1 with group > 0 interleaves: output row (r/group)*2*group + offset + r%group
 cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis, const void* src,

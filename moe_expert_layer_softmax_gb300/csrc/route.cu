@@ -5,10 +5,11 @@
 // Section 24.1: the device-resident metadata removes the host wait without
 // changing the routing calculation).
 //
-// Determinism: a route's slot is (base of its block for its expert) + (its rank
-// among the block's routes of that expert, in (token, choice) order), and the
-// block bases are a scan over blocks in block order.  This is exactly the
-// sequential walk over routes in ascending (t, j) order, independent of timing.
+// Determinism: a route's slot is (base of its 128-token block for its expert) +
+// (its rank among the block's routes of that expert, in (token, choice) order),
+// and the block bases are a scan over blocks in block order.  This is exactly
+// the sequential walk over routes in ascending (t, j) order, independent of
+// timing and of which top-k kernel ran.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -18,12 +19,241 @@ namespace moe {
 
 namespace {
 
-constexpr int kTopkThreads = 256;  // 8 warps; each warp handles 2 of the block's 16 tokens
+constexpr int kTpb = kRouteTokensPerBlock;   // 128 tokens per routing block
 
 // Order used for the selection: larger key first, lower expert id on ties.
 // NaN is treated as -inf so that the selection stays a valid set of k distinct
 // experts; the token is flagged and its gates are zeroed.
 MOE_DEV float route_key(float v) { return (v != v) ? -CUDART_INF_F : v; }
+
+// entry (v, i) goes ahead of (w, j): larger key first, lower expert id on ties
+MOE_DEV bool topk_ahead(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
+
+// gates of the k <= 8 selected keys (largest first): exp(l_j - l_1) / sum_i
+// exp(l_i - l_1), the sum taken in the order of a 32-lane xor butterfly in
+// which only lanes 0..k-1 are non-zero (the order route_topk_kernel uses), so
+// that every top-k kernel gives the same bits
+MOE_DEV float gate_sum8(const float* ex) {
+  return ((ex[0] + ex[4]) + (ex[2] + ex[6])) + ((ex[1] + ex[5]) + (ex[3] + ex[7]));
+}
+
+// Ranks and histogram of one 128-token routing block from per-expert token
+// masks (s_mask[4 e + w] bit b: token 32 w + b of the block chose expert e):
+// a route's rank within its expert is the number of earlier tokens of the
+// block with that expert, which is its place in the stable (t, j) order.
+MOE_DEV int mask_rank(const uint32_t* s_mask, int e, int tl) {
+  const uint32_t* mk = s_mask + 4 * e;
+  int rank = __popc(mk[tl >> 5] & ((1u << (tl & 31)) - 1u));
+  for (int w = 0; w < (tl >> 5); ++w) rank += __popc(mk[w]);
+  return rank;
+}
+MOE_DEV void write_block_hist(const uint32_t* s_mask, int E, int32_t* block_hist, int tid,
+                              int nthreads) {
+  for (int e = tid; e < E; e += nthreads)
+    block_hist[(size_t)blockIdx.x * E + e] = __popc(s_mask[4 * e]) + __popc(s_mask[4 * e + 1]) +
+                                             __popc(s_mask[4 * e + 2]) + __popc(s_mask[4 * e + 3]);
+}
+
+// ---------------------------------------------------------------- top-k kernels
+// (a) E <= EM <= 128, k <= 8: one thread per token with all of its logits in
+// registers, k passes of argmax; a taken expert is marked in a bit mask.
+template <int EM, int KM>
+__global__ void __launch_bounds__(kTpb) route_topk_reg_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gates, int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
+    int32_t* __restrict__ err) {
+  pdl_begin();
+  __shared__ uint32_t s_mask[4 * EM];
+  const int tl = threadIdx.x;
+  const int64_t t = (int64_t)blockIdx.x * kTpb + tl;
+  const bool valid = t < T;
+  for (int i = tl; i < 4 * E; i += kTpb) s_mask[i] = 0u;
+  float v[EM];
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < EM; ++c) v[c] = -CUDART_INF_F;   // columns >= E are never chosen (k <= E)
+  if (valid) {
+    const float* row = logits + t * E;
+    if ((E & 3) == 0) {
+#pragma unroll
+      for (int c = 0; c < EM; c += 4) {
+        if (c < E) {
+          const float4 q = __ldg(reinterpret_cast<const float4*>(row + c));
+          v[c] = q.x; v[c + 1] = q.y; v[c + 2] = q.z; v[c + 3] = q.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < EM; ++c)
+        if (c < E) v[c] = __ldg(row + c);
+    }
+#pragma unroll
+    for (int c = 0; c < EM; ++c) {
+      bad = bad || !isfinite(v[c]) && c < E;
+      v[c] = route_key(v[c]);
+    }
+  }
+  uint32_t taken[EM / 32];
+#pragma unroll
+  for (int w = 0; w < EM / 32; ++w) taken[w] = 0u;
+  int sel[KM];
+  float ex[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ex[j] = 0.0f;
+  float lmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    sel[j] = 0;
+    if (j < k) {
+      float best = 0.0f;
+      int bi = -1;
+#pragma unroll
+      for (int c = 0; c < EM; ++c) {
+        const bool free = ((taken[c >> 5] >> (c & 31)) & 1u) == 0u;
+        if (free && (bi < 0 || v[c] > best)) {   // strict: the lower id keeps a tie
+          best = v[c];
+          bi = c;
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < EM / 32; ++w)
+        if ((bi >> 5) == w) taken[w] |= 1u << (bi & 31);
+      sel[j] = bi;
+      if (j == 0) lmax = best;
+      ex[j] = expf(best - lmax);
+    }
+  }
+  if (valid) {
+    const float sum = gate_sum8(ex);
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
+        topk_idx[t * k + j] = sel[j];
+        gates[t * k + j] = bad ? 0.0f : ex[j] / sum;
+      }
+    }
+    if (bad) raise_error(err, MOE_DEVERR_NONFINITE_LOGIT);
+  }
+  __syncthreads();   // masks cleared
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) atomicOr(&s_mask[4 * sel[j] + (tl >> 5)], 1u << (tl & 31));
+  }
+  __syncthreads();
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) local_rank[t * k + j] = mask_rank(s_mask, sel[j], tl);
+  }
+  write_block_hist(s_mask, E, block_hist, tl, kTpb);
+}
+
+// (b) E > 128, k <= 8: four threads per token; thread q keeps the k largest of
+// columns [q cw, (q + 1) cw) while it reads them, and the four lists are merged
+// through lane shuffles in the same total order.
+constexpr int kTopk4Threads = 4 * kTpb;
+
+template <int KM>
+MOE_DEV void topk_insert(float* tv, int* tix, int k, float kv, int ki) {
+  int pos = 0;   // kept entries that stay ahead of the new one
+#pragma unroll
+  for (int j = 0; j < KM; ++j) pos += (j < k && tix[j] >= 0 && topk_ahead(tv[j], tix[j], kv, ki)) ? 1 : 0;
+#pragma unroll
+  for (int j = KM - 1; j >= 0; --j) {
+    if (j < k && j > pos) {
+      tv[j] = tv[j - 1];
+      tix[j] = tix[j - 1];
+    }
+    if (j < k && j == pos) {
+      tv[j] = kv;
+      tix[j] = ki;
+    }
+  }
+}
+
+template <int KM>
+__global__ void __launch_bounds__(kTopk4Threads) route_topk4_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gates, int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
+    int32_t* __restrict__ err) {
+  pdl_begin();
+  __shared__ uint32_t s_mask[256 * 4];
+  const int tid = threadIdx.x;
+  const int tl = tid >> 2, q = tid & 3;
+  const int64_t t = (int64_t)blockIdx.x * kTpb + tl;
+  const bool valid = t < T;
+  for (int i = tid; i < 4 * E; i += kTopk4Threads) s_mask[i] = 0u;
+  float tv[KM];
+  int tix[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    tv[j] = 0.0f;
+    tix[j] = -1;
+  }
+  bool bad = false;
+  if (valid) {
+    const int cw = (E + 3) >> 2;
+    const int c0 = q * cw, c1 = min(E, c0 + cw);
+    const float* row = logits + t * E;
+#pragma unroll 4
+    for (int c = c0; c < c1; ++c) {
+      const float x = __ldg(row + c);
+      bad = bad || !isfinite(x);
+      topk_insert<KM>(tv, tix, k, route_key(x), c);
+    }
+  }
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {   // every lane ends with the same list
+    float ov[KM];
+    int oi[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      ov[j] = __shfl_xor_sync(0xffffffffu, tv[j], off);
+      oi[j] = __shfl_xor_sync(0xffffffffu, tix[j], off);
+    }
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (oi[j] >= 0) topk_insert<KM>(tv, tix, k, ov[j], oi[j]);
+  }
+  {   // non-finite logits of the token: OR over its four lanes
+    int b = bad ? 1 : 0;
+    b |= __shfl_xor_sync(0xffffffffu, b, 1);
+    b |= __shfl_xor_sync(0xffffffffu, b, 2);
+    bad = b != 0;
+  }
+  if (valid) {
+    float ex[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ex[j] = (j < k && j < KM) ? expf(tv[j < KM ? j : 0] - tv[0]) : 0.0f;
+    const float sum = gate_sum8(ex);
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j < k && (j & 3) == q) {
+        topk_idx[t * k + j] = tix[j];
+        gates[t * k + j] = bad ? 0.0f : ex[j] / sum;
+      }
+    }
+    if (bad && q == 0) raise_error(err, MOE_DEVERR_NONFINITE_LOGIT);
+  }
+  __syncthreads();
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k && (j & 3) == q) atomicOr(&s_mask[4 * tix[j] + (tl >> 5)], 1u << (tl & 31));
+  }
+  __syncthreads();
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k && (j & 3) == q) local_rank[t * k + j] = mask_rank(s_mask, tix[j], tl);
+  }
+  write_block_hist(s_mask, E, block_hist, tid, kTopk4Threads);
+}
+
+// (c) any k (used for k > 8): a warp per token, warp-shuffle arg-max rounds;
+// eight warps take the block's 128 tokens 16 each.
+constexpr int kTopkThreads = 256;
 
 template <int EPL>
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
@@ -31,14 +261,13 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
     float* __restrict__ gates, int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
     int32_t* __restrict__ err) {
   pdl_begin();
-  __shared__ int32_t s_sel[kRouteTokensPerBlock * 32];  // expert of each route of the block
-  __shared__ int32_t s_cnt[256];
+  __shared__ int32_t s_sel[kTpb * 32];   // expert of each route of the block
+  __shared__ uint32_t s_mask[256 * 4];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int t0 = blockIdx.x * kRouteTokensPerBlock;
-  const int ntok = min(kRouteTokensPerBlock, T - t0);
-
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  const int t0 = blockIdx.x * kTpb;
+  const int ntok = min(kTpb, T - t0);
+  for (int i = threadIdx.x; i < 4 * E; i += kTopkThreads) s_mask[i] = 0u;
 
   for (int tl = warp; tl < ntok; tl += kTopkThreads / 32) {
     const int t = t0 + tl;
@@ -94,36 +323,19 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(
     if (lane < k) {
       topk_idx[(size_t)t * k + lane] = my_id;
       gates[(size_t)t * k + lane] = token_bad ? 0.0f : ex / sum;
+      atomicOr(&s_mask[4 * my_id + (tl >> 5)], 1u << (tl & 31));
     }
     if (token_bad && lane == 0) raise_error(err, MOE_DEVERR_NONFINITE_LOGIT);
   }
   __syncthreads();
-
-  // Stable ranks of the block's routes within their experts, in route order.
-  if (warp == 0) {
-    const int n = ntok * k;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < n; base += 32) {
-      const int r = base + lane;
-      const bool active = r < n;
-      const uint32_t act = __ballot_sync(0xffffffffu, active);
-      if (active) {
-        const int e = s_sel[r];
-        const uint32_t peers = __match_any_sync(act, e);
-        const int rank = s_cnt[e] + __popc(peers & lt_mask);
-        local_rank[(size_t)t0 * k + r] = rank;
-        __syncwarp(act);
-        if ((__ffs(peers) - 1) == lane) s_cnt[e] += __popc(peers);
-      }
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[(size_t)blockIdx.x * E + e] = s_cnt[e];
+  for (int r = threadIdx.x; r < ntok * k; r += kTopkThreads)
+    local_rank[(size_t)t0 * k + r] = mask_rank(s_mask, s_sel[r], r / k);
+  write_block_hist(s_mask, E, block_hist, threadIdx.x, kTopkThreads);
 }
 
+// ---------------------------------------------------------------- scan, slots
 // One block of 1024 threads.  Thread (p, e) = (tid / Epad, tid % Epad) owns
-// expert e and the p-th contiguous chunk of the top-k blocks.  block_hist[b][e]
+// expert e and the p-th contiguous chunk of the routing blocks.  block_hist[b][e]
 // (routes of expert e in block b) is replaced by the absolute first row of
 // block b's routes of e; counts, offsets and tile_offsets are written.
 constexpr int kScanThreads = 1024;
@@ -143,8 +355,10 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
   const int b0 = min(n_blocks, p * cb);
   const int b1 = min(n_blocks, b0 + cb);
   int sum = 0;
-  if (e < E)
+  if (e < E) {
+#pragma unroll 8
     for (int b = b0; b < b1; ++b) sum += block_hist[(size_t)b * E + e];
+  }
   s_part[tid] = sum;
   __syncthreads();
   int prefix = 0, total = 0;
@@ -199,6 +413,8 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(
   }
 }
 
+// One thread per route (slot = its block's first row for its expert + its rank),
+// then one per padding row of each expert's last tile (route_of_slot = -1).
 __global__ void __launch_bounds__(256) route_slots_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ local_rank,
     const int32_t* __restrict__ block_base, const int32_t* __restrict__ counts,
@@ -210,7 +426,7 @@ __global__ void __launch_bounds__(256) route_slots_kernel(
   const int64_t R = (int64_t)T * k;
   if (i < R) {
     const int t = (int)(i / k);
-    const int b = t / kRouteTokensPerBlock;
+    const int b = t / kTpb;
     const int e = topk_idx[i];
     const int slot = (e >= 0 && e < E) ? block_base[(size_t)b * E + e] + local_rank[i] : -1;
     if (slot < 0 || slot >= rows_max) {   // never expected
@@ -229,159 +445,48 @@ __global__ void __launch_bounds__(256) route_slots_kernel(
   }
 }
 
-// Scan and slots in one kernel.  Block b < n_route_blk handles the routes of
-// routing blocks [4b, 4b + 4) (64 tokens); the blocks after them mark the
-// padding rows.  Every block re-derives from the per-block histograms (read
-// only, L2-resident) the per-expert totals and tile offsets, and a route block
-// the prefix over the routing blocks before its own; block 0 writes counts,
-// offsets and tile_offsets.  The slots are those of the sequential walk over
-// routes in (t, j) order, as with the separate scan and slots kernels.
-constexpr int kSsThreads = 256;
-constexpr int kSsRouteBlocks = 4;   // routing blocks (16 tokens each) per block
-__global__ void __launch_bounds__(kSsThreads) route_scan_slots_kernel(
-    const int32_t* __restrict__ block_hist, int n_blocks, const int32_t* __restrict__ topk_idx,
-    const int32_t* __restrict__ local_rank, int T, int E, int k, int64_t rows_max,
-    int n_route_blk, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ tile_offsets, int32_t* __restrict__ slot_of_route,
-    int32_t* __restrict__ route_of_slot, int32_t* __restrict__ err) {
-  pdl_begin();
-  __shared__ int32_t s_ptot[4 * kSsThreads];   // [part][expert] partial sums
-  __shared__ int32_t s_ppre[4 * kSsThreads];
-  __shared__ int32_t s_c[256];                   // counts, then their inclusive scan
-  __shared__ int32_t s_t[256];                   // tiles, then their inclusive scan
-  __shared__ int32_t s_pre[256];
-  __shared__ int32_t s_tot[256];
-  __shared__ int32_t s_base[kSsRouteBlocks][256];
-  const int tid = threadIdx.x;
-  const bool route_blk = (int)blockIdx.x < n_route_blk;
-  const int rb0 = route_blk ? (int)blockIdx.x * kSsRouteBlocks : n_blocks;
-
-  // 1. per-expert sums over all routing blocks and over those before rb0:
-  //    thread (part p, column group g) sums V experts over a range of rows
-  const int V = (E % 4 == 0) ? 4 : 1;
-  const int ng = E / V;
-  const int P = kSsThreads / ng;
-  const int p = tid / ng, g = tid - (tid / ng) * ng;
-  if (p < P) {
-    int tot[4] = {0, 0, 0, 0}, pre[4] = {0, 0, 0, 0};
-    const int per = (n_blocks + P - 1) / P;
-    const int r0 = min(n_blocks, p * per), r1 = min(n_blocks, r0 + per);
-    for (int r = r0; r < r1; r += 8) {
-      int4 h[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        h[u] = make_int4(0, 0, 0, 0);
-        if (r + u < r1) {
-          const int32_t* row = block_hist + (size_t)(r + u) * E + V * g;
-          if (V == 4) h[u] = *reinterpret_cast<const int4*>(row);
-          else h[u].x = *row;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        tot[0] += h[u].x; tot[1] += h[u].y; tot[2] += h[u].z; tot[3] += h[u].w;
-        if (r + u < rb0) {
-          pre[0] += h[u].x; pre[1] += h[u].y; pre[2] += h[u].z; pre[3] += h[u].w;
-        }
-      }
-    }
-    for (int c = 0; c < V; ++c) {
-      s_ptot[p * E + V * g + c] = tot[c];
-      s_ppre[p * E + V * g + c] = pre[c];
-    }
-  }
-  __syncthreads();
-  if (tid < 256) {
-    int tot = 0, pre = 0;
-    if (tid < E)
-      for (int q = 0; q < P; ++q) {
-        tot += s_ptot[q * E + tid];
-        pre += s_ppre[q * E + tid];
-      }
-    s_tot[tid] = tot;
-    s_pre[tid] = pre;
-    s_c[tid] = tot;
-    s_t[tid] = (tot + kTileM - 1) / kTileM;
-  }
-  __syncthreads();
-  // 2. inclusive scans of counts and tiles over 256 entries
-  for (int off = 1; off < 256; off <<= 1) {
-    int c = 0, t = 0;
-    if (tid >= off) {
-      c = s_c[tid - off];
-      t = s_t[tid - off];
-    }
-    __syncthreads();
-    s_c[tid] += c;
-    s_t[tid] += t;
-    __syncthreads();
-  }
-  if (blockIdx.x == 0 && tid < E) {
-    counts[tid] = s_tot[tid];
-    offsets[tid + 1] = s_c[tid];
-    tile_offsets[tid + 1] = s_t[tid];
-    if (tid == 0) {
-      offsets[0] = 0;
-      tile_offsets[0] = 0;
-    }
-  }
-  if (!route_blk) {
-    // 3'. padding rows of each expert's last tile
-    const int q = ((int)blockIdx.x - n_route_blk) * kSsThreads + tid;
-    if (q < E * kTileM) {
-      const int e = q / kTileM;
-      const int tile0 = e > 0 ? s_t[e - 1] : 0;
-      const int row = tile0 * kTileM + s_tot[e] + q % kTileM;
-      if (row < s_t[e] * kTileM) route_of_slot[row] = -1;
-    }
-    return;
-  }
-  // 3. first row of each of this block's routing blocks' routes, per expert
-  if (tid < E) {
-    int base = (s_t[tid] - (s_tot[tid] + kTileM - 1) / kTileM) * kTileM + s_pre[tid];
-    for (int j = 0; j < kSsRouteBlocks; ++j) {
-      s_base[j][tid] = base;
-      if (rb0 + j < n_blocks) base += block_hist[(size_t)(rb0 + j) * E + tid];
-    }
-  }
-  __syncthreads();
-  // 4. the slots of this block's routes
-  const int64_t i0 = (int64_t)rb0 * kRouteTokensPerBlock * k;
-  const int64_t i1 = min((int64_t)T, (int64_t)(rb0 + kSsRouteBlocks) * kRouteTokensPerBlock) * k;
-  for (int64_t i = i0 + tid; i < i1; i += kSsThreads) {
-    const int t = (int)(i / k);
-    const int j = t / kRouteTokensPerBlock - rb0;
-    const int e = topk_idx[i];
-    const int slot = (e >= 0 && e < E) ? s_base[j][e] + local_rank[i] : -1;
-    if (slot < 0 || slot >= rows_max) {   // never expected
-      raise_error(err, MOE_DEVERR_BOUNDS);
-      slot_of_route[i] = 0;
-      continue;
-    }
-    slot_of_route[i] = slot;
-    route_of_slot[slot] = (int32_t)i;
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* topk_idx,
                               float* gates, int32_t* local_rank, int32_t* block_hist,
                               int32_t* err, cudaStream_t s) {
-  const int nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  const int nb = (T + kTpb - 1) / kTpb;
+  if (k <= 8 && E <= 128) {
+#define MOE_TOPK_REG(EM, KM)                                                                   \
+  launch_pdl(route_topk_reg_kernel<EM, KM>, dim3(nb), dim3(kTpb), 0, s, logits, T, E, k,     \
+             topk_idx, gates, local_rank, block_hist, err)
+    if (E <= 32) {
+      if (k <= 4) MOE_TOPK_REG(32, 4); else MOE_TOPK_REG(32, 8);
+    } else if (E <= 64) {
+      if (k <= 4) MOE_TOPK_REG(64, 4); else MOE_TOPK_REG(64, 8);
+    } else {
+      if (k <= 4) MOE_TOPK_REG(128, 4); else MOE_TOPK_REG(128, 8);
+    }
+#undef MOE_TOPK_REG
+    return cudaGetLastError();
+  }
+  if (k <= 8) {
+    if (k <= 4)
+      launch_pdl(route_topk4_kernel<4>, dim3(nb), dim3(kTopk4Threads), 0, s, logits, T, E, k,
+                 topk_idx, gates, local_rank, block_hist, err);
+    else
+      launch_pdl(route_topk4_kernel<8>, dim3(nb), dim3(kTopk4Threads), 0, s, logits, T, E, k,
+                 topk_idx, gates, local_rank, block_hist, err);
+    return cudaGetLastError();
+  }
   const int epl = (E + 31) / 32;
   if (epl <= 1)
-    launch_pdl(route_topk_kernel<1>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
-                                                    block_hist, err);
+    launch_pdl(route_topk_kernel<1>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx,
+               gates, local_rank, block_hist, err);
   else if (epl <= 2)
-    launch_pdl(route_topk_kernel<2>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
-                                                    block_hist, err);
+    launch_pdl(route_topk_kernel<2>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx,
+               gates, local_rank, block_hist, err);
   else if (epl <= 4)
-    launch_pdl(route_topk_kernel<4>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
-                                                    block_hist, err);
+    launch_pdl(route_topk_kernel<4>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx,
+               gates, local_rank, block_hist, err);
   else
-    launch_pdl(route_topk_kernel<8>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx, gates, local_rank,
-                                                    block_hist, err);
+    launch_pdl(route_topk_kernel<8>, dim3(nb), dim3(kTopkThreads), 0, s, logits, T, E, k, topk_idx,
+               gates, local_rank, block_hist, err);
   return cudaGetLastError();
 }
 
@@ -389,8 +494,8 @@ cudaError_t launch_route_scan(int32_t* block_hist, int n_blocks, int E, int32_t*
                               int32_t* offsets, int32_t* tile_offsets, cudaStream_t s) {
   int e_pad = 4;
   while (e_pad < E) e_pad <<= 1;   // E <= 256 -> at least 4 chunks per expert
-  launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, block_hist, n_blocks, E, e_pad, counts, offsets,
-                                               tile_offsets);
+  launch_pdl(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, block_hist, n_blocks, E, e_pad,
+             counts, offsets, tile_offsets);
   return cudaGetLastError();
 }
 
@@ -401,23 +506,31 @@ cudaError_t launch_route_slots(const int32_t* topk_idx, const int32_t* local_ran
                                cudaStream_t s) {
   const int64_t n = (int64_t)T * k + (int64_t)E * kTileM;
   const int nb = (int)((n + 255) / 256);
-  launch_pdl(route_slots_kernel, dim3(nb), dim3(256), 0, s, topk_idx, local_rank, block_base, counts, tile_offsets, T,
-                                        E, k, rows_max, slot_of_route, route_of_slot, err);
+  launch_pdl(route_slots_kernel, dim3(nb), dim3(256), 0, s, topk_idx, local_rank, block_base,
+             counts, tile_offsets, T, E, k, rows_max, slot_of_route, route_of_slot, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_scan_slots(const int32_t* block_hist, int n_blocks,
-                                    const int32_t* topk_idx, const int32_t* local_rank, int T,
-                                    int E, int k, int64_t rows_max, int32_t* counts,
-                                    int32_t* offsets, int32_t* tile_offsets,
-                                    int32_t* slot_of_route, int32_t* route_of_slot, int32_t* err,
-                                    cudaStream_t s) {
-  const int n_route_blk = (n_blocks + kSsRouteBlocks - 1) / kSsRouteBlocks;
-  const int n_pad_blk = (E * kTileM + kSsThreads - 1) / kSsThreads;
-  launch_pdl(route_scan_slots_kernel, dim3((unsigned)(n_route_blk + n_pad_blk)), dim3(kSsThreads),
-             0, s, block_hist, n_blocks, topk_idx, local_rank, T, E, k, rows_max, n_route_blk,
-             counts, offsets, tile_offsets, slot_of_route, route_of_slot, err);
-  return cudaGetLastError();
+cudaError_t launch_route(int T, int d, int E, int k, int64_t rows_max, const void* x,
+                         const void* w_router, const float* bias, float* logits,
+                         int32_t* topk_idx, float* gates, int32_t* counts, int32_t* offsets,
+                         int32_t* tile_offsets, int32_t* slot_of_route, int32_t* route_of_slot,
+                         int32_t* err, int32_t* hist, int32_t* rank, cudaStream_t s) {
+  cudaError_t e;
+  if (w_router != nullptr) {
+    GemmLaunch g = {};
+    g.op = OP_ROUTER;
+    g.T = T; g.d = d; g.E = E; g.f = 128;
+    g.rows_max = rows_max;
+    g.a0 = x; g.w0 = w_router; g.bias = bias; g.out0 = logits; g.err = err;
+    if ((e = launch_grouped_gemm(g, s)) != cudaSuccess) return e;
+  }
+  if ((e = launch_route_topk(logits, T, E, k, topk_idx, gates, rank, hist, err, s)) != cudaSuccess)
+    return e;
+  const int nb = (T + kTpb - 1) / kTpb;
+  if ((e = launch_route_scan(hist, nb, E, counts, offsets, tile_offsets, s)) != cudaSuccess) return e;
+  return launch_route_slots(topk_idx, rank, hist, counts, tile_offsets, T, E, k, rows_max,
+                            slot_of_route, route_of_slot, err, s);
 }
 
 }  // namespace moe

@@ -115,21 +115,10 @@ extern "C" MOE_API int moe_route_noalloc(const moe_shape_t* s, const void* x, co
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   if (cudaMemsetAsync(err, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (w_router != nullptr) {
-    GemmLaunch g = {};
-    g.op = OP_ROUTER;
-    g.T = s->T; g.d = s->d_model; g.E = s->n_experts; g.f = s->d_ff;
-    g.rows_max = rows_max;
-    g.a0 = x; g.w0 = w_router; g.bias = logit_bias; g.out0 = logits; g.err = err;
-    if (launch_grouped_gemm(g, st) != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  if (launch_route_topk(logits, s->T, s->n_experts, s->top_k, topk_idx, gates, rank, hist, err,
-                        st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_route_scan(hist, nb, s->n_experts, counts, offsets, tile_offsets, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_route_slots(topk_idx, rank, hist, counts, tile_offsets, s->T, s->n_experts, s->top_k,
-                         rows_max, slot_of_route, route_of_slot, err, st) != cudaSuccess)
+  // the same kernels as moe_route, on the static scratch
+  if (launch_route(s->T, s->d_model, s->n_experts, s->top_k, rows_max, x, w_router, logit_bias,
+                   logits, topk_idx, gates, counts, offsets, tile_offsets, slot_of_route,
+                   route_of_slot, err, hist, rank, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (dev_error != nullptr &&
       cudaMemcpyAsync(dev_error, err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

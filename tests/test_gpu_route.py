@@ -147,3 +147,39 @@ def test_router_projection(moe_gpu, T, d, E, k, routing):
     kth = np.sort(gl, axis=1)[:, ::-1][:, k - 1]
     assert (chosen[:, -1] == kth).all()
     assert (g["counts"].sum() == T * k) and g["err"] == 0
+
+
+@pytest.mark.parametrize("T,d,E,k", [(10000, 256, 64, 8), (12000, 128, 250, 4), (9999, 128, 1, 1),
+                                     (20000, 512, 128, 2), (32768, 256, 256, 8), (3000, 128, 40, 12)],
+                         ids=lambda v: str(v))
+def test_routing_with_router_projection_large(moe_gpu, T, d, E, k):
+    """Router GEMM, top-k (four threads per token for k <= 8, a warp per token
+    above), scan and slots on many routing blocks, a ragged last block and E
+    not a multiple of 4: bit for bit the oracle's routing of the logits the call
+    wrote, which agree with the oracle's own logits to 1e-5."""
+    m, dev = moe_gpu
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=128, seed=T + E, with_grad=False)
+    g = gpu_route(m, dev, T, E, k, x=to_dev_bf16(inp["x"], dev),
+                  w_router=to_dev_bf16(inp["w_router"], dev), bias=inp["bias"], d=d)
+    check_routing(g, g["logits"], k)
+    ref = O.router_logits(inp["x"], inp["w_router"], inp["bias"])
+    assert max_abs_rel(g["logits"], ref) < 1e-5
+
+
+def test_non_finite_logit_from_the_router_projection(moe_gpu):
+    """A NaN in the bias makes one token's logits non-finite: the error bit is
+    set and only that token's gates are zeroed (its neighbours in the same warp
+    and block keep theirs); its k experts are still distinct."""
+    m, dev = moe_gpu
+    T, d, E, k = 10000, 128, 32, 4
+    inp = make_inputs(T=T, d=d, E=E, k=k, f=128, seed=5, with_grad=False)
+    bias = inp["bias"].copy()
+    bias[1234, 7] = np.nan
+    g = gpu_route(m, dev, T, E, k, x=to_dev_bf16(inp["x"], dev),
+                  w_router=to_dev_bf16(inp["w_router"], dev), bias=bias, d=d)
+    assert g["err"] & m.DEVERR_NONFINITE_LOGIT
+    assert (g["gates"][1234] == 0).all()
+    ok = np.ones(T, dtype=bool)
+    ok[1234] = False
+    assert np.abs(g["gates"][ok].sum(1) - 1).max() < 1e-5
+    assert (np.sort(g["topk_idx"], axis=1)[:, 1:] != np.sort(g["topk_idx"], axis=1)[:, :-1]).all()
