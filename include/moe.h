@@ -138,8 +138,19 @@ MOE_API int moe_profile_start(int32_t op);
 MOE_API int moe_profile_stop(float* total_ms, int32_t* launches);
 
 /* Synchronise `stream`, then copy the error word to *code.  Diagnostics only:
- * with moe_profile_stop, the only call that waits for the GPU. */
+ * with moe_profile_stop and moe_checks_read, the only calls that wait for the
+ * GPU. */
 MOE_API int moe_read_error(const void* ws, int32_t* code, void* stream);
+
+/* Check words of the checks build (the pages have no counterpart: this is test
+ * infrastructure standing in for a memory checker).  A library compiled with
+ * -DMOE_CHECKS checks every index that a kernel reads from device data (a
+ * slot, a route, a padding row, a grouped-GEMM tile's rows) against its buffer
+ * before the access: an index outside sets MOE_DEVERR_BOUNDS in a device-side
+ * word and the access is skipped.  This call synchronises the device, ORs
+ * those words into *flags and clears them when `reset` is not 0.  The normal
+ * build has no such words: it returns MOE_ERR_UNSUPPORTED with *flags = 0. */
+MOE_API int moe_checks_read(int32_t* flags, int32_t reset);
 
 /* ------------------------------------------------------------ routing (a1-a3)
  * Router projection, softmax/top-k/gates, counts, offsets and stable slots.

@@ -16,7 +16,10 @@ import os
 from dataclasses import dataclass
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+# MOE_GB300_CHECKS=1 selects the checks build (device-side bounds checks, see
+# moe_checks_read) and guard bands around every buffer allocate() hands out
+CHECKS = os.environ.get("MOE_GB300_CHECKS", "") == "1"
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300_checks.so" if CHECKS else "libmoe_gb300.so")
 
 BF16, MXFP8 = 0, 1
 TILE_M = 128
@@ -45,6 +48,7 @@ EXPORTS = (
     "moe_combine_bwd", "moe_dispatch_bwd", "moe_router_bwd", "moe_layer_fwd", "moe_layer_bwd",
     "moe_route_noalloc", "moe_dequantize_mxfp8", "moe_build_mx_weights",
     "moe_debug_inject_stall", "moe_profile_start", "moe_profile_stop", "moe_load_balance",
+    "moe_checks_read",
 )
 
 
@@ -108,6 +112,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
+    if CHECKS and path == LIB_PATH:
+        from . import _build
+        _build.build(checks=True)
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
                            "(the MoE layer has no CPU or eager fallback)")
@@ -137,6 +144,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_router_bwd": [P(Shape)] + [_vp] * 7 + [_vp],
         "moe_layer_fwd": [P(Shape), P(FwdArgs), P(Saved), _vp, _vp],
         "moe_layer_bwd": [P(Shape), P(BwdArgs), P(Saved), _vp, _vp],
+        "moe_checks_read": [P(i32), i32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -196,6 +204,53 @@ def workspace_size(s: Shape) -> int:
     v = ctypes.c_size_t()
     _check("moe_workspace_size", load().moe_workspace_size(ctypes.byref(s), ctypes.byref(v)))
     return v.value
+
+
+def checks_read(reset: bool = True) -> int:
+    """moe_checks_read: the OR of the checks build's bounds-check words (0 when
+    no index left its buffer); raises MoEError(MOE_ERR_UNSUPPORTED) on the
+    normal build."""
+    v = ctypes.c_int32()
+    _check("moe_checks_read", load().moe_checks_read(ctypes.byref(v), int(bool(reset))))
+    return v.value
+
+
+# ---- guard bands (checks mode): every buffer of allocate() sits between two
+# 4 KB bands of a known byte pattern, verified by check_canaries()
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xA5
+_guarded = {}   # id of a handed-out buffer -> its whole allocation (bands included)
+
+
+def _alloc(shape, dtype, device, zero=False):
+    import torch
+    if not CHECKS:
+        return (torch.zeros if zero else torch.empty)(shape, dtype=dtype, device=device)
+    import math
+    import weakref
+    n = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+    base = torch.full((n + 2 * GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device=device)
+    mid = base[GUARD_BYTES:GUARD_BYTES + n]
+    if zero:
+        mid.zero_()
+    out = mid.view(dtype).view(shape)
+    key = id(out)
+    _guarded[key] = base
+    weakref.finalize(out, _guarded.pop, key, None)   # forgotten with the buffer
+    return out
+
+
+def check_canaries() -> list:
+    """Checks mode: the guard bands of every live buffer from allocate() still
+    hold their pattern.  Returns a description of each band that was written."""
+    bad = []
+    for base in list(_guarded.values()):
+        for name, band in (("front", base[:GUARD_BYTES]), ("back", base[-GUARD_BYTES:])):
+            changed = int((band != GUARD_BYTE).sum().item())
+            if changed:
+                bad.append(f"{changed} byte(s) of the {name} guard of a {base.numel() - 2 * GUARD_BYTES}"
+                           f"-byte buffer were written")
+    return bad
 
 
 def clear_error(ws, stream=None):
@@ -356,43 +411,47 @@ def allocate(s: Shape, device=None, with_grads: bool = True,
     bf = dict(dtype=torch.bfloat16, device=dev)
     i32 = dict(dtype=torch.int32, device=dev)
     f32 = dict(dtype=torch.float32, device=dev)
-    ws = torch.zeros(workspace_size(s), dtype=torch.uint8, device=dev)
+    ws = _alloc((workspace_size(s),), torch.uint8, dev, zero=True)
     u8 = dict(dtype=torch.uint8, device=dev)
     mx = s.prec == MXFP8
+
+    def new(*shape, dtype, device):   # guard bands around it in checks mode
+        return _alloc(shape, dtype, device)
+
     saved = {
-        "logits": torch.empty(T, E, **f32), "topk_idx": torch.empty(T, k, **i32),
-        "gates": torch.empty(T, k, **f32), "counts": torch.empty(E, **i32),
-        "offsets": torch.empty(E + 1, **i32), "tile_offsets": torch.empty(E + 1, **i32),
-        "slot_of_route": torch.empty(T * k, **i32), "route_of_slot": torch.empty(n, **i32),
-        "xd": None if mx else torch.empty(n, d, **bf), "h": torch.empty(n, f, **bf),
-        "u": torch.empty(n, f, **bf), "a": None if mx else torch.empty(n, f, **bf),
-        "y": torch.empty(n, d, **bf),
-        "lb_stats": torch.empty(E + 1, **f32) if load_balance else None,
+        "logits": new(T, E, **f32), "topk_idx": new(T, k, **i32),
+        "gates": new(T, k, **f32), "counts": new(E, **i32),
+        "offsets": new(E + 1, **i32), "tile_offsets": new(E + 1, **i32),
+        "slot_of_route": new(T * k, **i32), "route_of_slot": new(n, **i32),
+        "xd": None if mx else new(n, d, **bf), "h": new(n, f, **bf),
+        "u": new(n, f, **bf), "a": None if mx else new(n, f, **bf),
+        "y": new(n, d, **bf),
+        "lb_stats": new(E + 1, **f32) if load_balance else None,
     }
     grads = {}
     if with_grads:
         grads = {
-            "dx": torch.empty(T, d, **bf), "dw_router": torch.empty(E, d, **f32),
-            "dw_gate": torch.empty(E, f, d, **f32), "dw_up": torch.empty(E, f, d, **f32),
-            "dw_down": torch.empty(E, d, f, **f32), "d_gates": torch.empty(T, k, **f32),
-            "dlogits": torch.empty(T, E, **f32), "dy": torch.empty(n, d, **bf),
-            "dh": torch.empty(n, f, **bf), "du": torch.empty(n, f, **bf),
-            "dxd": torch.empty(n, d, **bf),
+            "dx": new(T, d, **bf), "dw_router": new(E, d, **f32),
+            "dw_gate": new(E, f, d, **f32), "dw_up": new(E, f, d, **f32),
+            "dw_down": new(E, d, f, **f32), "d_gates": new(T, k, **f32),
+            "dlogits": new(T, E, **f32), "dy": new(n, d, **bf),
+            "dh": new(n, f, **bf), "du": new(n, f, **bf),
+            "dxd": new(n, d, **bf),
         }
     mxw = mxb = None
     if mx:
-        mxw = {"gu_q": torch.empty(E, 2 * f, d, **u8), "gu_s": torch.empty(E * 2 * f * d // 32, **u8),
-               "down_q": torch.empty(E, d, f, **u8), "down_s": torch.empty(E * d * f // 32, **u8),
-               "downT_q": torch.empty(E, f, d, **u8), "downT_s": torch.empty(E * f * d // 32, **u8),
-               "gateT_q": torch.empty(E, d, f, **u8), "gateT_s": torch.empty(E * d * f // 32, **u8),
-               "upT_q": torch.empty(E, d, f, **u8), "upT_s": torch.empty(E * d * f // 32, **u8)}
-        mxb = {"xd_q": torch.empty(n, d, **u8), "xd_s": torch.empty(n * d // 32, **u8),
-               "a_q": torch.empty(n, f, **u8), "a_s": torch.empty(n * f // 32, **u8)}
+        mxw = {"gu_q": new(E, 2 * f, d, **u8), "gu_s": new(E * 2 * f * d // 32, **u8),
+               "down_q": new(E, d, f, **u8), "down_s": new(E * d * f // 32, **u8),
+               "downT_q": new(E, f, d, **u8), "downT_s": new(E * f * d // 32, **u8),
+               "gateT_q": new(E, d, f, **u8), "gateT_s": new(E * d * f // 32, **u8),
+               "upT_q": new(E, d, f, **u8), "upT_s": new(E * d * f // 32, **u8)}
+        mxb = {"xd_q": new(n, d, **u8), "xd_s": new(n * d // 32, **u8),
+               "a_q": new(n, f, **u8), "a_s": new(n * f // 32, **u8)}
         if with_grads:
-            mxb.update({"dy_q": torch.empty(n, d, **u8), "dy_s": torch.empty(n * d // 32, **u8),
-                        "dh_q": torch.empty(n, f, **u8), "dh_s": torch.empty(n * f // 32, **u8),
-                        "du_q": torch.empty(n, f, **u8), "du_s": torch.empty(n * f // 32, **u8),
-                        "xd_dq": torch.empty(n, d, **bf), "a_dq": torch.empty(n, f, **bf)})
+            mxb.update({"dy_q": new(n, d, **u8), "dy_s": new(n * d // 32, **u8),
+                        "dh_q": new(n, f, **u8), "dh_s": new(n * f // 32, **u8),
+                        "du_q": new(n, f, **u8), "du_s": new(n * f // 32, **u8),
+                        "xd_dq": new(n, d, **bf), "a_dq": new(n, f, **bf)})
     return LayerBuffers(s, n, ws, saved, grads, mxw, mxb)
 
 

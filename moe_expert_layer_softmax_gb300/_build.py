@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
+# the checks build (-DMOE_CHECKS: device-side bounds checks on every index read
+# from device data; a test build, see moe_checks_read in include/moe.h)
+BUILD_CHECKS = os.path.join(PKG, "_build_checks")
+LIB_CHECKS = os.path.join(PKG, "libmoe_gb300_checks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-DNDEBUG"]
@@ -39,23 +43,27 @@ def _deps():
         [os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link; returns the library path.  Raises on failure."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False,
+          checks: bool = False) -> str:
+    """Compile and link; returns the library path.  Raises on failure.
+    checks=True builds the checks variant (libmoe_gb300_checks.so)."""
+    lib = LIB_CHECKS if checks else LIB
+    bdir = BUILD_CHECKS if checks else BUILD
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DMOE_CHECKS"] if checks else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,15 +78,16 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(verbose=True, force="--force" in sys.argv, ptxas_info="--ptxas" in sys.argv))
+    print(build(verbose=True, force="--force" in sys.argv, ptxas_info="--ptxas" in sys.argv,
+                checks="--checks" in sys.argv))

@@ -326,6 +326,23 @@ int moe_workspace_size(const moe_shape_t* shape, size_t* ws_bytes) {
   return MOE_OK;
 }
 
+int moe_checks_read(int32_t* flags, int32_t reset) {
+  if (flags == nullptr) return MOE_ERR_INVALID;
+  *flags = 0;
+  int32_t* words[] = {check_word_move(), check_word_quant(), check_word_balance(),
+                      check_word_gemm(), check_word_route()};
+  bool any = false;
+  for (int32_t* w : words) {
+    if (w == nullptr) continue;
+    any = true;
+    int32_t v = 0;
+    MOE_CUDA(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost));
+    *flags |= v;
+    if (reset) MOE_CUDA(cudaMemset(w, 0, sizeof(int32_t)));
+  }
+  return any ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
 int moe_clear_error(void* ws, void* stream) {
   if (ws == nullptr) return MOE_ERR_INVALID;
   MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
@@ -500,7 +517,7 @@ int moe_combine(const moe_shape_t* s, const void* y, const float* gates,
   MOE_NONNULL_ALIGNED(gates);
   MOE_NONNULL_ALIGNED(slot_of_route);
   MOE_NONNULL_ALIGNED(out);
-  MOE_CUDA(launch_combine(y, gates, slot_of_route, s->T, s->d_model, s->top_k, out,
+  MOE_CUDA(launch_combine(y, gates, slot_of_route, s->T, s->d_model, s->n_experts, s->top_k, out,
                           static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
@@ -618,7 +635,7 @@ int moe_layer_fwd(const moe_shape_t* s, const moe_fwd_args_t* a, const moe_saved
                                  at<float>(ws, w.lb), sv->lb_stats, st));
   }
   MOE_TRY(expert_forward(s, a->x, a->w_gate, a->w_up, a->w_down, a->mx_weights, a->mx, sv, ws, st));
-  MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->top_k, a->out,
+  MOE_CUDA(launch_combine(sv->y, sv->gates, sv->slot_of_route, s->T, s->d_model, s->n_experts, s->top_k, a->out,
                           st));
   return MOE_OK;
 }

@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(256) dispatch_bwd_dense_kernel(
     for (int j = 0; j < k; ++j) {
       const int slot = slot_of_route[(size_t)t * k + j];
       float f[8];
-      unpack8(__ldg(dxd + (size_t)slot * nv + c0 / 8 + cg), f);
+      uint4 vv = make_uint4(0, 0, 0, 0);
+      MOE_CHECKED(slot, rows_max_of(T, k, E)) vv = __ldg(dxd + (size_t)slot * nv + c0 / 8 + cg);
+      unpack8(vv, f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += f[i];
     }
@@ -263,5 +265,7 @@ cudaError_t launch_router_bwd_dense(const void* x, const float* dlogits, int T, 
              static_cast<const float*>(partial), splits, n, dw_router);
   return cudaGetLastError();
 }
+
+MOE_CHECK_WORD_ACCESSOR(balance)
 
 }  // namespace moe

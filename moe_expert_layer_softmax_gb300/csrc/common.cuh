@@ -43,6 +43,42 @@ MOE_DEV void raise_error(int32_t* err, int bits) {
   if (err != nullptr) atomicOr(err, bits);
 }
 
+// ---------------------------------------------------------------- checks build
+// Built with -DMOE_CHECKS (a test build that stands in for a memory checker),
+// every index that a kernel reads from device data (a slot, a route, a padding
+// row, a tile's rows) is checked against its buffer before the access it
+// guards: an index outside sets MOE_DEVERR_BOUNDS in the translation unit's
+// check word (moe_checks_read() collects them) and the access is skipped.  The
+// normal build compiles none of this: MOE_CHECKED(i, n) { ... } is then a
+// plain block.
+#ifdef MOE_CHECKS
+static __device__ int32_t g_check_word;
+MOE_DEV bool checked_index(int64_t i, int64_t n) {
+  const bool ok = i >= 0 && i < n;
+  if (!ok) atomicOr(&g_check_word, MOE_DEVERR_BOUNDS);
+  return ok;
+}
+#define MOE_CHECKED(i, n) if (::moe::checked_index((int64_t)(i), (int64_t)(n)))
+#define MOE_CHECK_OK(i, n) ::moe::checked_index((int64_t)(i), (int64_t)(n))
+// host side: this translation unit's check word (device address), or NULL
+#define MOE_CHECK_WORD_ACCESSOR(name)                                                  \
+  int32_t* check_word_##name() {                                                       \
+    void* p = nullptr;                                                                 \
+    return cudaGetSymbolAddress(&p, g_check_word) == cudaSuccess ? static_cast<int32_t*>(p) \
+                                                                 : nullptr;            \
+  }
+#else
+#define MOE_CHECKED(i, n)
+#define MOE_CHECK_OK(i, n) true
+#define MOE_CHECK_WORD_ACCESSOR(name) \
+  int32_t* check_word_##name() { return nullptr; }
+#endif
+
+// rows of the dispatched buffers: T*k + E*(MOE_TILE_M-1), rounded up to a tile
+MOE_DEV int64_t rows_max_of(int T, int k, int E) {
+  return ((int64_t)T * k + (int64_t)E * (MOE_TILE_M - 1) + MOE_TILE_M - 1) / MOE_TILE_M * MOE_TILE_M;
+}
+
 MOE_DEV uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

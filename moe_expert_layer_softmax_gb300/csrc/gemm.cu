@@ -153,6 +153,7 @@ struct Params {
   const void* aux0;
   const void* aux1;
   const float* bias;
+  int64_t rows_max;      // rows of the dispatched row buffers
   int64_t ldo;           // leading dimension (elements) of outputs and aux
   int64_t out_group_stride;  // KGROUP: elements between experts' outputs
   int32_t* err;
@@ -713,6 +714,7 @@ MOE_DEV void epilogue_tile(const Params& p, const TileInfo& ti, int r, uint32_t 
     epilogue_router(p, ti, r, tb, c0, c1, v);
     return;
   }
+  if (!MOE_CHECK_OK(ti.m_tile, p.rows_max / kTileM)) return;   // the tile's rows (checks build)
   if (p.epi == EPI_BF16) {
     const int64_t row = (int64_t)ti.m_tile * kTileM + r;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) + row * p.ldo + (int64_t)ti.n_tile * p.BN;
@@ -1351,6 +1353,7 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
   for (int t = (int)blockIdx.x / 2; t < nt; t += (int)gridDim.x / 2, ++it) {
     bool valid;
     const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    valid = valid && MOE_CHECK_OK(ti.m_tile, p.rows_max / kTileM);   // the tile's rows (checks build)
     if (bwd && valid && st.leader) {
       // H and U chunks 0 and 1 of this tile, into sets 0 and 1, once the
       // previous tile's stores have read those sets
@@ -1729,6 +1732,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   bool ok = true;
   p.E = E;
   p.tile_offsets = g.tile_offsets;
+  p.rows_max = g.rows_max;
   p.err = g.err;
   p.k_split = 1 << 30;
   p.m_split = 1 << 30;
@@ -1993,5 +1997,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   return launch_pdl(grouped_gemm_kernel<false, false>, dim3(grid), dim3(kThreads), kSmemBytes,
                     stream, A0, A1, B0, B1, O0, O1, O2, p);
 }
+
+MOE_CHECK_WORD_ACCESSOR(gemm)
 
 }  // namespace moe

@@ -65,7 +65,7 @@ cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
                                  const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                  int E, int k, void* xd, cudaStream_t s);
 cudaError_t launch_combine(const void* y, const float* gates, const int32_t* slot_of_route, int T,
-                           int d, int k, void* out, cudaStream_t s);
+                           int d, int E, int k, void* out, cudaStream_t s);
 cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* gates,
                                const int32_t* topk_idx, const int32_t* slot_of_route,
                                const int32_t* counts, const int32_t* tile_offsets, int T, int d,
@@ -169,6 +169,13 @@ cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
 cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t rows, int K,
                                     void* out, cudaStream_t s);
 cudaError_t gemm_init_attributes();
+// Check words of the checks build (device addresses; NULL in the normal build),
+// one per translation unit with device-data-dependent indexing.
+int32_t* check_word_move();
+int32_t* check_word_quant();
+int32_t* check_word_balance();
+int32_t* check_word_gemm();
+int32_t* check_word_route();
 void noalloc_forget_device(int dev);   // moe_route_noalloc's cached scratch address
 int gemm_set_inject_stall(int mode);   // returns the previous mode
 

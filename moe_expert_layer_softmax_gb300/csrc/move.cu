@@ -59,10 +59,12 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bf16_kernel(
       for (int j = 0; j < k; ++j) {
         const int slot = __shfl_sync(0xffffffffu, my_slot, j);
         uint4* dst = xd + (size_t)slot * nv;
+        MOE_CHECKED(slot, rows_max_of(T, k, E)) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c0 + u * 32 + lane;
-          if (c < nv) dst[c] = v[u];
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < nv) dst[c] = v[u];
+          }
         }
       }
     }
@@ -70,13 +72,13 @@ __global__ void __launch_bounds__(kMoveThreads) dispatch_bf16_kernel(
     const int p = (blockIdx.x - token_blocks) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (p >= E * kTileM) return;
     const int row = pad_row(p, counts, tile_offsets);
-    if (row >= 0) zero_row(xd + (size_t)row * nv, d, lane);
+    if (row >= 0) MOE_CHECKED(row, rows_max_of(T, k, E)) zero_row(xd + (size_t)row * nv, d, lane);
   }
 }
 
 __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
     const uint4* __restrict__ y, const float* __restrict__ gates,
-    const int32_t* __restrict__ slot_of_route, int T, int d, int k, uint4* __restrict__ out) {
+    const int32_t* __restrict__ slot_of_route, int T, int d, int E, int k, uint4* __restrict__ out) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -101,7 +103,9 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
       for (int u = 0; u < 4; ++u) {
         const int slot = __shfl_sync(0xffffffffu, my_slot, j + u);
         g[u] = __shfl_sync(0xffffffffu, my_g, j + u);
-        v[u] = __ldg(y + (size_t)slot * nv + cc);
+        uint4 vv = make_uint4(0, 0, 0, 0);
+        MOE_CHECKED(slot, rows_max_of(T, k, E)) vv = __ldg(y + (size_t)slot * nv + cc);
+        v[u] = vv;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -115,7 +119,9 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
       const int slot = __shfl_sync(0xffffffffu, my_slot, j);
       const float g = __shfl_sync(0xffffffffu, my_g, j);
       float f[kVec];
-      unpack8(__ldg(y + (size_t)slot * nv + cc), f);
+      uint4 vv = make_uint4(0, 0, 0, 0);
+      MOE_CHECKED(slot, rows_max_of(T, k, E)) vv = __ldg(y + (size_t)slot * nv + cc);
+      unpack8(vv, f);
 #pragma unroll
       for (int i = 0; i < kVec; ++i) acc[i] = fmaf(g, f[i], acc[i]);
     }
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
     const int p = (blockIdx.x - token_blocks) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (p >= E * kTileM) return;
     const int row = pad_row(p, counts, tile_offsets);
-    if (row >= 0) zero_row(dy + (size_t)row * nv, d, lane);
+    if (row >= 0) MOE_CHECKED(row, rows_max_of(T, k, E)) zero_row(dy + (size_t)row * nv, d, lane);
     return;
   }
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -164,8 +170,10 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
       unpack8(__ldg(dO + c), a);
       uint4 yv[KM];
 #pragma unroll
-      for (int j = 0; j < KM; ++j)
-        if (j < k) yv[j] = __ldg(y + (size_t)slot[j] * nv + c);
+      for (int j = 0; j < KM; ++j) {
+        yv[j] = make_uint4(0, 0, 0, 0);
+        if (j < k) MOE_CHECKED(slot[j], rows_max_of(T, k, E)) yv[j] = __ldg(y + (size_t)slot[j] * nv + c);
+      }
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
         if (j < k) {
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
             part[j] = fmaf(a[i], b[i], part[j]);
             o[i] = g[j] * a[i];
           }
-          dy[(size_t)slot[j] * nv + c] = pack8(o);
+          MOE_CHECKED(slot[j], rows_max_of(T, k, E)) dy[(size_t)slot[j] * nv + c] = pack8(o);
         }
       }
     }
@@ -263,40 +271,56 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
     id[j] = __shfl_sync(0xffffffffu, my_id, src);
     dl[j] = __shfl_sync(0xffffffffu, my_dl, src);
   }
-  for (int c0 = 0; c0 < nv; c0 += 32) {
-    const int c = c0 + lane;
-    if (c >= nv) continue;
-    uint4 v[KM];
+  // two 32-vector column chunks per pass (KM <= 8): the k rows of both chunks
+  // are loaded before any is used, 2k 16-byte loads in flight per lane
+  constexpr int kCh = KM <= 8 ? 2 : 1;
+  for (int c0 = 0; c0 < nv; c0 += 32 * kCh) {
+    uint4 v[kCh][KM];
 #pragma unroll
-    for (int j = 0; j < KM; ++j)
-      if (j < k) v[j] = __ldg(dxd + (size_t)slot[j] * nv + c);
-    float acc[kVec];
+    for (int h = 0; h < kCh; ++h) {
+      const int c = c0 + 32 * h + lane;
 #pragma unroll
-    for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      if (j < k) {
-        float f[kVec];
-        unpack8(v[j], f);
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) acc[i] += f[i];
+      for (int j = 0; j < KM; ++j) {
+        v[h][j] = make_uint4(0, 0, 0, 0);
+        if (j < k && c < nv)
+          MOE_CHECKED(slot[j], rows_max_of(T, k, E)) v[h][j] = __ldg(dxd + (size_t)slot[j] * nv + c);
       }
     }
-    if (w_router != nullptr) {
 #pragma unroll
-      for (int j = 0; j < KM; ++j)
-        if (j < k) v[j] = __ldg(w_router + (size_t)id[j] * nv + c);
+    for (int h = 0; h < kCh; ++h) {
+      const int c = c0 + 32 * h + lane;
+      if (c >= nv) continue;
+      float acc[kVec];
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
         if (j < k) {
           float f[kVec];
-          unpack8(v[j], f);
+          unpack8(v[h][j], f);
 #pragma unroll
-          for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl[j], f[i], acc[i]);
+          for (int i = 0; i < kVec; ++i) acc[i] += f[i];
         }
       }
+      if (w_router != nullptr) {
+        uint4 w[KM];
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          w[j] = make_uint4(0, 0, 0, 0);
+          if (j < k) MOE_CHECKED(id[j], E) w[j] = __ldg(w_router + (size_t)id[j] * nv + c);
+        }
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          if (j < k) {
+            float f[kVec];
+            unpack8(w[j], f);
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dl[j], f[i], acc[i]);
+          }
+        }
+      }
+      dx[(size_t)t * nv + c] = pack8(acc);
     }
-    dx[(size_t)t * nv + c] = pack8(acc);
   }
 }
 
@@ -311,7 +335,8 @@ constexpr int kRbThreads = kRbGroups * kRbCols;
 __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
     const uint4* __restrict__ x, const float* __restrict__ dlogits,
     const int32_t* __restrict__ route_of_slot, const int32_t* __restrict__ counts,
-    const int32_t* __restrict__ tile_offsets, int d, int E, int k, float* __restrict__ partial) {
+    const int32_t* __restrict__ tile_offsets, int T, int d, int E, int k,
+    float* __restrict__ partial) {
   pdl_begin();
   __shared__ int32_t s_tok[kTileM];
   __shared__ float s_dl[kTileM];
@@ -330,9 +355,17 @@ __global__ void __launch_bounds__(kRbThreads) router_bwd_partial_kernel(
   const int r0 = m * kTileM;
   const int nrows = max(0, min(kTileM, row_end - r0));
   if (threadIdx.x < nrows) {
-    const int t = route_of_slot[r0 + threadIdx.x] / k;
+    int t = 0;
+    float dl = 0.0f;
+    MOE_CHECKED(r0 + threadIdx.x, rows_max_of(T, k, E)) {
+      const int tt = route_of_slot[r0 + threadIdx.x] / k;
+      MOE_CHECKED(tt, T) {
+        t = tt;
+        dl = dlogits[(size_t)tt * E + e];
+      }
+    }
     s_tok[threadIdx.x] = t;
-    s_dl[threadIdx.x] = dlogits[(size_t)t * E + e];
+    s_dl[threadIdx.x] = dl;
   }
   __syncthreads();
   const int ct = threadIdx.x % kRbCols;
@@ -411,10 +444,10 @@ cudaError_t launch_dispatch_bf16(const void* x, const int32_t* slot_of_route,
 }
 
 cudaError_t launch_combine(const void* y, const float* gates, const int32_t* slot_of_route, int T,
-                           int d, int k, void* out, cudaStream_t s) {
+                           int d, int E, int k, void* out, cudaStream_t s) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   launch_pdl(combine_kernel, dim3(tb), dim3(kMoveThreads), 0, s, static_cast<const uint4*>(y), gates, slot_of_route, T,
-                                             d, k, static_cast<uint4*>(out));
+                                             d, E, k, static_cast<uint4*>(out));
   return cudaGetLastError();
 }
 
@@ -470,7 +503,7 @@ cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t
   const int nv = d / kVec;
   dim3 g1((unsigned)tiles_max, (unsigned)((nv + kRbCols - 1) / kRbCols));
   launch_pdl(router_bwd_partial_kernel, dim3(g1), dim3(kRbThreads), 0, s, static_cast<const uint4*>(x), dlogits,
-                                                      route_of_slot, counts, tile_offsets, d, E, k,
+                                                      route_of_slot, counts, tile_offsets, T, d, E, k,
                                                       partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -478,5 +511,7 @@ cudaError_t launch_router_bwd(const void* x, const float* dlogits, const int32_t
   launch_pdl(router_bwd_reduce_kernel, dim3(g2), dim3(256), 0, s, partial, tile_offsets, d, dw_router);
   return cudaGetLastError();
 }
+
+MOE_CHECK_WORD_ACCESSOR(move)
 
 }  // namespace moe

@@ -97,31 +97,37 @@ __global__ void __launch_bounds__(kQThreads) quantize_cols_kernel(
 // Both orientations of a weight from one read: src [R, C] bf16 per matrix ->
 // (1) q_r [R, C] blocked along C (rows interleaved by `group`/`offset` as in
 // quantize_rows_kernel) and (2) q_c [C, R] blocked along R (the transpose, as
-// in quantize_cols_kernel).  Tile: 128 rows x 64 columns; for (1) a thread
-// holds 8 values of a row and 4 neighbouring lanes form one 32-value block.
+// in quantize_cols_kernel).  Tile: 128 rows x 128 columns (32 KB), eight
+// 16-byte loads in flight per thread.  For (1) a thread holds 8 values of a
+// row, 4 neighbouring lanes form one 32-value block and 16 lanes store one
+// whole 128-byte row of codes.  For (2) a thread quantises two 32-row blocks of
+// one column; the 128 x 128 transposed codes are staged in the tile's memory
+// and stored as whole 128-byte rows.
+constexpr int kBR = 128, kBC = 128;
 __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
     const __nv_bfloat16* __restrict__ src, int R, int C, int group, int offset,
     uint8_t* __restrict__ q_r, uint8_t* __restrict__ s_r, uint8_t* __restrict__ q_c,
     uint8_t* __restrict__ s_c) {
   pdl_begin();
-  __shared__ __nv_bfloat16 tile[kTK][kTN];
+  __shared__ __align__(16) __nv_bfloat16 tile[kBR][kBC];
   const int mat = blockIdx.z;
-  const int k0 = blockIdx.y * kTK;
-  const int n0 = blockIdx.x * kTN;
+  const int k0 = blockIdx.y * kBR;
+  const int n0 = blockIdx.x * kBC;
   const __nv_bfloat16* sm = src + (size_t)mat * R * C;
   const int64_t out_rows = group > 0 ? 2 * (int64_t)R : R;
   const int cb = C / 32;
-  uint4 raw[4];   // all four loads in flight before any is used
+  constexpr int kLoads = kBR * kBC / 8 / kQThreads;   // 8
+  uint4 raw[kLoads];   // all loads in flight before any is used
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < kLoads; ++u) {
     const int idx = threadIdx.x + u * kQThreads;
-    raw[u] = __ldg(reinterpret_cast<const uint4*>(sm + (size_t)(k0 + (idx >> 3)) * C + n0 +
-                                                   (idx & 7) * 8));
+    raw[u] = __ldg(reinterpret_cast<const uint4*>(sm + (size_t)(k0 + (idx >> 4)) * C + n0 +
+                                                   (idx & 15) * 8));
   }
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < kLoads; ++u) {
     const int idx = threadIdx.x + u * kQThreads;
-    const int row = idx >> 3, col = (idx & 7) * 8;
+    const int row = idx >> 4, col = (idx & 15) * 8;
     *reinterpret_cast<uint4*>(&tile[row][col]) = raw[u];
     float v[8];
     unpack8(raw[u], v);
@@ -141,35 +147,44 @@ __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
       s_r[(size_t)mat * out_rows * cb + sf_offset(ro, (n0 + col) / 32, cb)] = (uint8_t)(sx + 127);
   }
   __syncthreads();
-  // the transpose, blocked along R (as quantize_cols_kernel)
-  const int n = threadIdx.x & 63;
-  const int kb = threadIdx.x >> 6;
-  float v[32];
-  float amax = 0.0f;
+  // the transpose, blocked along R: column n, row blocks kb and kb + 2
+  const int n = threadIdx.x & 127;
+  uint2 codes[2][4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    v[j] = __bfloat162float(tile[kb * 32 + j][n]);
-    amax = fmaxf(amax, fabsf(v[j]));
+  for (int h = 0; h < 2; ++h) {
+    const int kb = (threadIdx.x >> 7) + 2 * h;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = __bfloat162float(tile[kb * 32 + j][n]);
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    const int e = mx_scale_exp(amax);
+    const float inv = ldexpf(1.0f, -e);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= inv;
+    s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)n0 + n, (k0 / 32) + kb, R / 32)] =
+        (uint8_t)(e + 127);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) codes[h][u] = e4m3x8(v + 8 * u);
   }
-  const int e = mx_scale_exp(amax);
-  const float inv = ldexpf(1.0f, -e);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] *= inv;
-  const size_t row_out = (size_t)n0 + n;
-  s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)row_out, (k0 / 32) + kb, R / 32)] =
-      (uint8_t)(e + 127);
-  // Stage the 64 x 128 codes of the transposed tile in the (now free) tile
+  // Stage the 128 x 128 codes of the transposed tile in the (now free) tile
   // memory, 8-byte chunk q of row n at chunk q ^ (n & 15) (conflict-free for
   // the column-wise writes), then store whole 128-byte rows: 8 lanes per row,
   // 16 bytes each.
   __syncthreads();
-  uint2* st = reinterpret_cast<uint2*>(&tile[0][0]);   // 64 rows x 16 chunks
+  uint2* st = reinterpret_cast<uint2*>(&tile[0][0]);   // 128 rows x 16 chunks
 #pragma unroll
-  for (int u = 0; u < 4; ++u) st[n * 16 + ((kb * 4 + u) ^ (n & 15))] = e4m3x8(v + 8 * u);
+  for (int h = 0; h < 2; ++h) {
+    const int kb = (threadIdx.x >> 7) + 2 * h;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) st[n * 16 + ((kb * 4 + u) ^ (n & 15))] = codes[h][u];
+  }
   __syncthreads();
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int idx = threadIdx.x + u * kQThreads;   // 512 16-byte pieces
+  for (int u = 0; u < 4; ++u) {
+    const int idx = threadIdx.x + u * kQThreads;   // 1024 16-byte pieces
     const int rn = idx >> 3, c = idx & 7;
     const uint2 lo = st[rn * 16 + ((2 * c) ^ (rn & 15))];
     const uint2 hi = st[rn * 16 + ((2 * c + 1) ^ (rn & 15))];
@@ -196,9 +211,11 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
     const int e = p / kTileM;
     const int row = tile_offsets[e] * kTileM + counts[e] + (p % kTileM);
     if (row >= tile_offsets[e + 1] * kTileM) return;
-    uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * d);
-    for (int c = lane; c < nv; c += 32) dst[c] = make_uint2(0, 0);
-    for (int b = lane; b < kb; b += 32) xs[sf_offset(row, b, kb)] = 127;
+    MOE_CHECKED(row, rows_max_of(T, k, E)) {
+      uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * d);
+      for (int c = lane; c < nv; c += 32) dst[c] = make_uint2(0, 0);
+      for (int b = lane; b < kb; b += 32) xs[sf_offset(row, b, kb)] = 127;
+    }
     return;
   }
   const int t = blockIdx.x * warps + (threadIdx.x >> 5);
@@ -223,7 +240,7 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
     const uint2 codes = e4m3x8(v);
     for (int j = 0; j < k; ++j) {
       const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-      if (ok) {
+      if (ok) MOE_CHECKED(slot, rows_max_of(T, k, E)) {
         reinterpret_cast<uint2*>(xq + (size_t)slot * d)[c] = codes;
         if ((lane & 3) == 0) xs[sf_offset(slot, c / 4, kb)] = (uint8_t)(s + 127);
       }
@@ -276,7 +293,7 @@ cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis,
 cudaError_t launch_quantize_mxfp8_both(int batch, int rows, int cols, const void* src, int group,
                                        int offset, uint8_t* q_rows, uint8_t* sf_rows,
                                        uint8_t* q_cols, uint8_t* sf_cols, cudaStream_t s) {
-  dim3 grid((unsigned)(cols / kTN), (unsigned)(rows / kTK), (unsigned)batch);
+  dim3 grid((unsigned)(cols / kBC), (unsigned)(rows / kBR), (unsigned)batch);
   launch_pdl(quantize_both_kernel, grid, dim3(kQThreads), 0, s,
              static_cast<const __nv_bfloat16*>(src), rows, cols, group, offset, q_rows, sf_rows,
              q_cols, sf_cols);
@@ -301,5 +318,7 @@ cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t
       reinterpret_cast<const uint4*>(q), sf, nvec, K, static_cast<uint4*>(out));
   return cudaGetLastError();
 }
+
+MOE_CHECK_WORD_ACCESSOR(quant)
 
 }  // namespace moe

@@ -533,4 +533,6 @@ cudaError_t launch_route(int T, int d, int E, int k, int64_t rows_max, const voi
                             slot_of_route, route_of_slot, err, s);
 }
 
+MOE_CHECK_WORD_ACCESSOR(route)
+
 }  // namespace moe

@@ -41,3 +41,18 @@ def moe_gpu():
     torch.cuda.set_device(0)
     m.init(0)
     return m, torch.device("cuda", 0)
+
+
+@pytest.fixture(autouse=True)
+def _checks_build_guards(request):
+    """With MOE_GB300_CHECKS=1 (the checks build: device-side bounds checks and
+    guard bands around every buffer of allocate()), every GPU test must leave
+    the bounds-check words at zero and every guard band intact."""
+    yield
+    if os.environ.get("MOE_GB300_CHECKS", "") != "1" or "gpu" not in request.keywords:
+        return
+    import moe_expert_layer_softmax_gb300 as m
+    flags = m.checks_read(reset=True)
+    bad = m.check_canaries()
+    assert flags == 0, f"bounds check words {flags:#x}"
+    assert not bad, bad
