@@ -118,6 +118,8 @@ struct Params {
   int n_tiles;
   int BN;                // MMA N (256 when b_dual)
   int n_valid;           // ROUTER: valid columns (E)
+  int n_cols;            // bf16 pairs with N = 128 (mod 256): N; the last 256-wide tile's
+                         // second half lies past it (0: every tile column is valid)
   int k_steps;           // DENSE/MGROUP: K / 64
   int k_parts;           // DENSE: K split into this many parts (1 or 2), summed atomically
   int k_split;           // DENSE/MGROUP: steps >= k_split read maps A1/B1
@@ -581,7 +583,9 @@ MOE_DEV void store_bf16x32(__nv_bfloat16* dst, const uint32_t* v) {
 }
 
 // One MXFP8 block held by one thread: 32 values -> 32 E4M3 codes + 1 scale byte.
-MOE_DEV void mx_store32(const uint32_t* bits, uint8_t* codes, uint8_t* sf_byte) {
+// E4M3 codes of one 32-value block to `codes` (32 bytes, 16-byte aligned);
+// returns the block's E8M0 scale byte
+MOE_DEV uint32_t mx_quant32(const uint32_t* bits, uint8_t* codes) {
   float v[32];
   float amax = 0.0f;
 #pragma unroll
@@ -597,7 +601,11 @@ MOE_DEV void mx_store32(const uint32_t* bits, uint8_t* codes, uint8_t* sf_byte) 
   const uint2 q0 = e4m3x8(v), q1 = e4m3x8(v + 8), q2 = e4m3x8(v + 16), q3 = e4m3x8(v + 24);
   c4[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
   c4[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
-  *sf_byte = (uint8_t)(sx + 127);
+  return (uint32_t)(sx + 127);
+}
+
+MOE_DEV void mx_store32(const uint32_t* bits, uint8_t* codes, uint8_t* sf_byte) {
+  *sf_byte = (uint8_t)mx_quant32(bits, codes);
 }
 
 // Columns [c0, c1) of the tile, 32 at a time.
@@ -1006,7 +1014,9 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
     if (!ok) break;
     tc_fence_after();
     const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.acc_cols);
-    if (valid) {
+    // a column half past N (the last tile when N = 128 mod 256) is neither
+    // read nor written: its operands were zero-filled, its output is clipped
+    if (valid && (p.n_cols == 0 || ti.n_tile * p.BN + c0 < p.n_cols)) {
       if (DQB || (!MX && p.tma_store))
         epilogue_tile_tma<DQB>(p, ti, tb, c0, c1, st, tO0, tO1, tO2);
       else
@@ -1400,13 +1410,16 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
       for (int i = 0; i < 64; ++i)
         v[i] = __float_as_uint(silu_f(__uint_as_float(v[i])) * __uint_as_float(v[64 + i]));
       uint8_t* Aq = static_cast<uint8_t*>(p.out2) + row * p.ldo + fc;
-      mx_store32(v, Aq, p.osf0 + sf_offset(row, fc / 32, p.osf_kb));
-      mx_store32(v + 32, Aq + 32, p.osf0 + sf_offset(row, fc / 32 + 1, p.osf_kb));
+      // blocks fc/32 and fc/32 + 1 (fc/32 even): adjacent scale bytes, one store
+      const uint32_t s0 = mx_quant32(v, Aq), s1 = mx_quant32(v + 32, Aq + 32);
+      *reinterpret_cast<uint16_t*>(p.osf0 + sf_offset(row, fc / 32, p.osf_kb)) =
+          (uint16_t)(s0 | (s1 << 8));
     } else {   // EPI_SWIGLU_BWD_MX: dA for f columns n_tile * 256 + 128 * half + [0, 128)
       const int fc = ti.n_tile * kMxPairBN + 128 * half;
       const int64_t off = row * p.ldo + fc;
       uint8_t* dHq = static_cast<uint8_t*>(p.out2) + off;
       uint8_t* dUq = static_cast<uint8_t*>(p.out3) + off;
+      uint32_t sh = 0, su = 0;   // the four blocks' scale bytes (fc/32 is a multiple of 4)
       bool fine = true;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -1447,10 +1460,12 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
             tma_load_2d(ub, tU, &hu_bar[j], fc + 32 * (c + 2), y);
           }
         }
-        const size_t so = sf_offset(row, fc / 32 + c, p.osf_kb);
-        mx_store32(v + 32 * c, dHq + 32 * c, p.osf0 + so);
-        mx_store32(gu, dUq + 32 * c, p.osf1 + so);
+        sh |= mx_quant32(v + 32 * c, dHq + 32 * c) << (8 * c);
+        su |= mx_quant32(gu, dUq + 32 * c) << (8 * c);
       }
+      const size_t so = sf_offset(row, fc / 32, p.osf_kb);
+      *reinterpret_cast<uint32_t*>(p.osf0 + so) = sh;
+      *reinterpret_cast<uint32_t*>(p.osf1 + so) = su;
       (void)fine;   // a wait that ran out has set the error word and the abort flag
     }
   }
@@ -1924,6 +1939,15 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
   const bool pair = op_uses_pairs(g.op) && !mx && p.tma_store &&
                     (p.mode == MODE_MGROUP || (p.mode == MODE_KGROUP && p.m_tiles % 2 == 0));
   if (p.dq_b && !pair) return cudaErrorInvalidValue;
+  if (pair && p.BN == 128 && g.op != OP_FWD1_SWIGLU) {
+    // N = 128 (mod 256): 256-wide pair tiles (half the operand bytes per flop
+    // of 128-wide ones), the last tile running 128 columns past N
+    const int n_cols = p.n_tiles * 128;
+    max_tiles = max_tiles / p.n_tiles * ((n_cols + 255) / 256);
+    p.BN = 256;
+    p.n_tiles = (n_cols + 255) / 256;
+    p.n_cols = n_cols;
+  }
   if (pair && p.mode == MODE_MGROUP && !p.b_mn && !p.b_dual) {
     // K-major B: each CTA of the pair loads BN/2 rows
     const void* wb = (g.op == OP_FWD2) ? g.w0 : nullptr;
