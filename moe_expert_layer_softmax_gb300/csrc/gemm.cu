@@ -95,6 +95,8 @@ struct __align__(8) Ctl {
   uint64_t bfull[4];             // converted B slot ready (even CTA, both CTAs' converters)
   uint64_t bempty[4];            // B slot free again (the pair's MMAs that read it are done)
   uint64_t hufull[4];            // MXFP8 SwiGLU backward: H and U chunk landed (2 halves x 2 sets)
+  uint64_t huwritten[4];         //   dH and dU written over it by the half's 128 epilogue threads
+  uint64_t codefree[2];          //   the half's code buffer read by the previous chunk's stores
   uint32_t tmem_base;
   int abort;
   int32_t tile_off[kMaxE + 1];
@@ -583,9 +585,9 @@ MOE_DEV void store_bf16x32(__nv_bfloat16* dst, const uint32_t* v) {
 }
 
 // One MXFP8 block held by one thread: 32 values -> 32 E4M3 codes + 1 scale byte.
-// E4M3 codes of one 32-value block to `codes` (32 bytes, 16-byte aligned);
-// returns the block's E8M0 scale byte
-MOE_DEV uint32_t mx_quant32(const uint32_t* bits, uint8_t* codes) {
+// E4M3 codes of one 32-value block: bytes 0-15 in lo, 16-31 in hi; returns
+// the block's E8M0 scale byte
+MOE_DEV uint32_t mx_quant32_regs(const uint32_t* bits, uint4& lo, uint4& hi) {
   float v[32];
   float amax = 0.0f;
 #pragma unroll
@@ -597,11 +599,19 @@ MOE_DEV uint32_t mx_quant32(const uint32_t* bits, uint8_t* codes) {
   const float inv = ldexpf(1.0f, -sx);
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] *= inv;
-  uint4* c4 = reinterpret_cast<uint4*>(codes);
   const uint2 q0 = e4m3x8(v), q1 = e4m3x8(v + 8), q2 = e4m3x8(v + 16), q3 = e4m3x8(v + 24);
-  c4[0] = make_uint4(q0.x, q0.y, q1.x, q1.y);
-  c4[1] = make_uint4(q2.x, q2.y, q3.x, q3.y);
+  lo = make_uint4(q0.x, q0.y, q1.x, q1.y);
+  hi = make_uint4(q2.x, q2.y, q3.x, q3.y);
   return (uint32_t)(sx + 127);
+}
+
+// The same, codes stored to `codes` (32 bytes, 16-byte aligned).
+MOE_DEV uint32_t mx_quant32(const uint32_t* bits, uint8_t* codes) {
+  uint4 lo, hi;
+  const uint32_t sb = mx_quant32_regs(bits, lo, hi);
+  reinterpret_cast<uint4*>(codes)[0] = lo;
+  reinterpret_cast<uint4*>(codes)[1] = hi;
+  return sb;
 }
 
 MOE_DEV void mx_store32(const uint32_t* bits, uint8_t* codes, uint8_t* sf_byte) {
@@ -1198,7 +1208,10 @@ static_assert(kMxPairStages * kMxPairStageBytes + 2 * kMxStageHalfBytes <=
 constexpr int kMxBwdStages = 4;
 constexpr int kMxHuSetBytes = 2 * kTileM * 64;
 constexpr int kMxHuHalfBytes = 2 * kMxHuSetBytes;
-static_assert(kMxBwdStages * kMxPairStageBytes + 2 * kMxHuHalfBytes <=
+// Their E4M3 codes leave the same way: per half one buffer of dH codes and one
+// of dU codes, 128 rows x 32 bytes each (32-byte swizzle), after the H/U sets.
+constexpr int kMxCodeHalfBytes = 2 * kTileM * 32;
+static_assert(kMxBwdStages * kMxPairStageBytes + 2 * kMxHuHalfBytes + 2 * kMxCodeHalfBytes <=
                   kRingBytes + 2 * kStageOutBytes, "MXFP8 pair backward shared memory");
 static_assert(kMxPairStages >= 4 && kMxPairStages <= kMaxStages, "MXFP8 pair ring depth");
 static_assert(kMxSfCol0 + kMxSfColsPerStage * kMxPairStages <= kTmemCols, "MXFP8 pair TMEM");
@@ -1344,8 +1357,7 @@ struct MxStager {
 // thread writes whole 32-byte sectors of codes).
 MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                               int rank, uint8_t* stage_base, const CUtensorMap* tO0,
-                              const CUtensorMap* tO1, const CUtensorMap* tH,
-                              const CUtensorMap* tU) {
+                              const CUtensorMap* tO1) {
   const int nt = total_tiles_pair(p, s);
   const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
   const int quarter = warp & 3;
@@ -1358,33 +1370,17 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
   st.bar_id = 1 + half;
   st.leader = (warp == 4 + 4 * half) && (lane == 0);
   st.r = r;
-  uint64_t* hu_bar = &s.hufull[2 * half];
+  uint64_t* hu_full = &s.hufull[2 * half];
+  uint64_t* hu_written = &s.huwritten[2 * half];
+  uint32_t vt = 0;   // valid tiles done (SwiGLU backward: the sets' use count)
   int it = 0;
   for (int t = (int)blockIdx.x / 2; t < nt; t += (int)gridDim.x / 2, ++it) {
     bool valid;
     const TileInfo ti = decode_pair(p, s, t, rank, valid);
     valid = valid && MOE_CHECK_OK(ti.m_tile, p.rows_max / kTileM);   // the tile's rows (checks build)
-    if (bwd && valid && st.leader) {
-      // H and U chunks 0 and 1 of this tile, into sets 0 and 1, once the
-      // previous tile's stores have read those sets
-      bulk_wait_read_all();
-      const int fc = ti.n_tile * kMxPairBN + 128 * half;
-      for (int j = 0; j < 2; ++j) {
-        uint8_t* set = st.buf + j * kMxHuSetBytes;
-        mbar_arrive_expect_tx(&hu_bar[j], (uint32_t)kMxHuSetBytes);
-        tma_load_2d(set, tH, &hu_bar[j], fc + 32 * j, ti.m_tile * kTileM);
-        tma_load_2d(set + kMxHuSetBytes / 2, tU, &hu_bar[j], fc + 32 * j, ti.m_tile * kTileM);
-      }
-    }
     bool ok = mbar_wait(&s.tfull[0], (uint32_t)it & 1u, &s.abort, p.err);
     // the half's named barriers below need all four of its warps: leave together
-    if (!bar_and(st.bar_id, kEpiThreads / 2, ok)) {
-      if (bwd && st.leader) {   // H/U copies may be in flight: let them land first
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 100000ull) {}
-      }
-      break;
-    }
+    if (!bar_and(st.bar_id, kEpiThreads / 2, ok)) break;
     tc_fence_after();
     uint32_t v[128];
     tmem_ld32x2(tb, tb + 32, v, v + 32);
@@ -1416,9 +1412,7 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
           (uint16_t)(s0 | (s1 << 8));
     } else {   // EPI_SWIGLU_BWD_MX: dA for f columns n_tile * 256 + 128 * half + [0, 128)
       const int fc = ti.n_tile * kMxPairBN + 128 * half;
-      const int64_t off = row * p.ldo + fc;
-      uint8_t* dHq = static_cast<uint8_t*>(p.out2) + off;
-      uint8_t* dUq = static_cast<uint8_t*>(p.out3) + off;
+      uint8_t* cbuf = stage_base + 2 * kMxHuHalfBytes + half * kMxCodeHalfBytes;
       uint32_t sh = 0, su = 0;   // the four blocks' scale bytes (fc/32 is a multiple of 4)
       bool fine = true;
 #pragma unroll
@@ -1426,8 +1420,9 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
         const int j = c & 1;
         uint8_t* hb = st.buf + j * kMxHuSetBytes;
         uint8_t* ub = hb + kMxHuSetBytes / 2;
-        // chunk c is the (c / 2)-th use of set j in this tile
-        fine = fine && mbar_wait(&hu_bar[j], (uint32_t)(c >> 1) & 1u, &s.abort, p.err);
+        // chunk c is use 2 vt + c / 2 of set j
+        const uint32_t u = 2u * vt + (uint32_t)(c >> 1);
+        fine = fine && mbar_wait(&hu_full[j], u & 1u, &s.abort, p.err);
         uint32_t gu[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1447,29 +1442,111 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
           *reinterpret_cast<uint4*>(hb + so16) = pack8(gh);   // dH, dU over H, U
           *reinterpret_cast<uint4*>(ub + so16) = pack8(g2);
         }
+        // this row's E4M3 codes of dH and dU (32 bytes each) into the half's code
+        // buffer, once the stores of the previous chunk have read it
+        uint4 hl, hh, ul, uh;
+        sh |= mx_quant32_regs(v + 32 * c, hl, hh) << (8 * c);
+        su |= mx_quant32_regs(gu, ul, uh) << (8 * c);
+        const uint32_t g = 4u * vt + (uint32_t)c;
+        if (g > 0) fine = fine && mbar_wait(&s.codefree[half], (g - 1u) & 1u, &s.abort, p.err);
+        const int sw = (r >> 2) & 1;   // 32-byte swizzle: granule ^= row bit 2
+        *reinterpret_cast<uint4*>(cbuf + r * 32 + 16 * sw) = hl;
+        *reinterpret_cast<uint4*>(cbuf + r * 32 + 16 * (1 ^ sw)) = hh;
+        *reinterpret_cast<uint4*>(cbuf + kTileM * 32 + r * 32 + 16 * sw) = ul;
+        *reinterpret_cast<uint4*>(cbuf + kTileM * 32 + r * 32 + 16 * (1 ^ sw)) = uh;
         fence_proxy_async_smem();
-        bar_sync(st.bar_id, kEpiThreads / 2);
-        if (st.leader) {
-          tma_store_2d(tO0, hb, fc + 32 * c, y);
-          tma_store_2d(tO1, ub, fc + 32 * c, y);
-          bulk_commit();
-          if (c + 2 < 4) {   // chunk c + 2 into this set once the stores have read it
-            bulk_wait_read_all();
-            mbar_arrive_expect_tx(&hu_bar[j], (uint32_t)kMxHuSetBytes);
-            tma_load_2d(hb, tH, &hu_bar[j], fc + 32 * (c + 2), y);
-            tma_load_2d(ub, tU, &hu_bar[j], fc + 32 * (c + 2), y);
-          }
-        }
-        sh |= mx_quant32(v + 32 * c, dHq + 32 * c) << (8 * c);
-        su |= mx_quant32(gu, dUq + 32 * c) << (8 * c);
+        mbar_arrive(&hu_written[j]);   // the half's mover stores dH, dU, the codes and refills the set
       }
       const size_t so = sf_offset(row, fc / 32, p.osf_kb);
       *reinterpret_cast<uint32_t*>(p.osf0 + so) = sh;
       *reinterpret_cast<uint32_t*>(p.osf1 + so) = su;
       (void)fine;   // a wait that ran out has set the error word and the abort flag
+      ++vt;
     }
   }
   if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
+}
+
+// MXFP8 SwiGLU backward: one thread per column half (lane 0 of warp 2 + half)
+// moves H and U chunks (32 columns x 128 rows each) into the half's two
+// shared-memory sets, and dH, dU and their E4M3 codes out of the sets and the
+// half's code buffer, so that the epilogue warps never wait for a bulk copy to
+// read shared memory.  Set j holds chunks j and j + 2 of each of the CTA's
+// valid tiles in turn; its u-th use completes phase u of hufull[j] (H, U
+// landed) and then of huwritten[j] (the half's 128 epilogue threads wrote dH,
+// dU over them and the chunk's codes into the code buffer).  Phase g of
+// codefree[half] completes when the stores of the CTA's g-th chunk have read
+// the code buffer.  At most one copy per set is in flight.
+MOE_DEV void hu_mover_mx_pair(const Params& p, Ctl& s, int rank, int half, uint8_t* stage_base,
+                              const CUtensorMap* tO0, const CUtensorMap* tO1,
+                              const CUtensorMap* tH, const CUtensorMap* tU,
+                              const CUtensorMap* tQ0, const CUtensorMap* tQ1) {
+  const int nt = total_tiles_pair(p, s);
+  const int step = (int)gridDim.x / 2;
+  uint8_t* buf = stage_base + half * kMxHuHalfBytes;
+  uint8_t* cbuf = stage_base + 2 * kMxHuHalfBytes + half * kMxCodeHalfBytes;
+  uint64_t* full = &s.hufull[2 * half];
+  uint64_t* written = &s.huwritten[2 * half];
+  // the next valid tile at or after t, with its first column and row
+  auto next_valid = [&](int t, int& fc, int& y) -> int {
+    for (; t < nt; t += step) {
+      bool valid;
+      const TileInfo ti = decode_pair(p, s, t, rank, valid);
+      if (valid && MOE_CHECK_OK(ti.m_tile, p.rows_max / kTileM)) {
+        fc = ti.n_tile * kMxPairBN + 128 * half;
+        y = ti.m_tile * kTileM;
+        return t;
+      }
+    }
+    return nt;
+  };
+  uint32_t loads0 = 0, loads1 = 0;   // copies issued into set 0 and set 1
+  auto load = [&](int j, int x, int y) {
+    uint8_t* set = buf + j * kMxHuSetBytes;
+    mbar_arrive_expect_tx(&full[j], (uint32_t)kMxHuSetBytes);
+    tma_load_2d(set, tH, &full[j], x, y);
+    tma_load_2d(set + kMxHuSetBytes / 2, tU, &full[j], x, y);
+    if (j == 0) ++loads0; else ++loads1;
+  };
+  int fc = 0, y = 0, nfc = 0, ny = 0;
+  int t = next_valid((int)blockIdx.x / 2, fc, y);
+  if (t < nt) {
+    load(0, fc, y);
+    load(1, fc + 32, y);
+  }
+  bool ok = true;
+  for (uint32_t vt = 0; ok && t < nt; ++vt) {
+    const int tn = next_valid(t + step, nfc, ny);
+    for (int c = 0; c < 4; ++c) {
+      const int j = c & 1;
+      const uint32_t u = 2u * vt + (uint32_t)(c >> 1);
+      if (!mbar_wait(&written[j], u & 1u, &s.abort, p.err)) { ok = false; break; }
+      uint8_t* set = buf + j * kMxHuSetBytes;
+      tma_store_2d(tO0, set, fc + 32 * c, y);
+      tma_store_2d(tO1, set + kMxHuSetBytes / 2, fc + 32 * c, y);
+      tma_store_2d(tQ0, cbuf, fc + 32 * c, y);
+      tma_store_2d(tQ1, cbuf + kTileM * 32, fc + 32 * c, y);
+      bulk_commit();
+      bulk_wait_read_all();
+      mbar_arrive(&s.codefree[half]);
+      // the set's next use: chunk c + 2 of this tile, else chunk j of the next tile
+      if (c + 2 < 4) load(j, fc + 32 * (c + 2), y);
+      else if (tn < nt) load(j, nfc + 32 * j, ny);
+    }
+    t = tn;
+    fc = nfc;
+    y = ny;
+  }
+  if (!ok) {   // the last copy into each set may still be in flight: let it land
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t n = j == 0 ? loads0 : loads1;
+      if (n == 0) continue;
+      const uint32_t a = smem_u32(&full[j]);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(a, (n - 1u) & 1u) && globaltimer() - t0 < 100000ull) {}
+    }
+  }
+  bulk_wait_all();   // stores complete before the CTA exits
 }
 
 __global__ void __launch_bounds__(kMxPairThreads, 1)
@@ -1484,7 +1561,9 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
                                 const __grid_constant__ CUtensorMap tO0,
                                 const __grid_constant__ CUtensorMap tO1,
                                 const __grid_constant__ CUtensorMap tH,
-                                const __grid_constant__ CUtensorMap tU, const Params p) {
+                                const __grid_constant__ CUtensorMap tU,
+                                const __grid_constant__ CUtensorMap tQ0,
+                                const __grid_constant__ CUtensorMap tQ1, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0) {
     pdl_wait();
@@ -1504,7 +1583,11 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
     }
     mbar_init(&s.tfull[0], 1);
     mbar_init(&s.tempty[0], 2 * kEpiThreads);
-    for (int i = 0; i < 4; ++i) mbar_init(&s.hufull[i], 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&s.hufull[i], 1);
+      mbar_init(&s.huwritten[i], kEpiThreads / 2);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&s.codefree[i], 1);
     mbar_init(&s.fin, 1);
     s.abort = 0;
     fence_barrier_init();
@@ -1535,6 +1618,8 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
     if (p.epi == EPI_SWIGLU_BWD_MX) {
       prefetch_tensormap(&tH);
       prefetch_tensormap(&tU);
+      prefetch_tensormap(&tQ0);
+      prefetch_tensormap(&tQ1);
     }
   }
   if (warp == 1) tmem_alloc_pair(&s.tmem_base, kTmemCols);
@@ -1550,11 +1635,14 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
       producer_mx_pair(p, s, ring, rank, mp);
     } else if (warp == 1 && lane == 0) {
       mma_issuer_mx_pair(p, s, ring, tmem_base, rank);
+    } else if (warp >= 2 && lane == 0 && p.epi == EPI_SWIGLU_BWD_MX) {
+      hu_mover_mx_pair(p, s, rank, warp - 2, ring + p.stages * p.stage_bytes, &tO0, &tO1, &tH,
+                       &tU, &tQ0, &tQ1);
     }
   } else {
     setmaxnreg_inc<kMxPairEpiRegs>();
     epilogue_mx_pair(p, s, tmem_base, warp, lane, rank, ring + p.stages * p.stage_bytes, &tO0,
-                     &tO1, &tH, &tU);
+                     &tO1);
   }
 
   tc_fence_before();
@@ -1607,7 +1695,8 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   cuuint32_t estr[2] = {1, 1};
   return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle == 64    ? CU_TENSOR_MAP_SWIZZLE_64B
+                  swizzle == 32    ? CU_TENSOR_MAP_SWIZZLE_32B
+                  : swizzle == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                   : swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1679,10 +1768,13 @@ cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A
   O1 = O0;
   if (ok && p.out1 != nullptr) ok = make_map(&O1, p.out1, ocols, rows, 32, kTileM, MAP_BF16, 64);
   // SwiGLU backward: H (aux0) and U (aux1) in the same 32-column boxes
-  CUtensorMap MH = O0, MU = O0;
+  // and the E4M3 codes of dH (out2) and dU (out3): 32-byte boxes, 32-byte swizzle
+  CUtensorMap MH = O0, MU = O0, QH = O0, QU = O0;
   if (ok && p.epi == EPI_SWIGLU_BWD_MX)
     ok = make_map(&MH, p.aux0, ocols, rows, 32, kTileM, MAP_BF16, 64) &&
-         make_map(&MU, p.aux1, ocols, rows, 32, kTileM, MAP_BF16, 64);
+         make_map(&MU, p.aux1, ocols, rows, 32, kTileM, MAP_BF16, 64) &&
+         make_map(&QH, p.out2, ocols, rows, 32, kTileM, MAP_U8, 32) &&
+         make_map(&QU, p.out3, ocols, rows, 32, kTileM, MAP_U8, 32);
   if (!ok) return cudaErrorInvalidValue;
   // the register split above assumes the launch allocation it was computed for
   // (a smaller one would leave setmaxnreg.inc waiting for registers forever)
@@ -1711,7 +1803,7 @@ cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_mx_pair_kernel, A0, A1, B0, B1, SA0, SA1, SB0, SB1,
-                            O0, O1, MH, MU, p);
+                            O0, O1, MH, MU, QH, QU, p);
 }
 
 }  // namespace

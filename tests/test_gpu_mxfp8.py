@@ -229,8 +229,16 @@ def test_mx_dgrad2_swiglu_bwd(mcase):
     u = c["used"]
     assert max_abs_rel(f64(dH)[:u], c["bwd"]["dH"]) <= TOL
     assert max_abs_rel(f64(dU)[:u], c["bwd"]["dU"]) <= TOL
-    dq = O.dequantize_mxfp8(dHq.cpu().numpy(), sf_unpack(dHs.cpu().numpy(), n, f // 32))
-    assert max_abs_rel(dq[:u], c["bwd"]["dH"]) <= TOL
+    for q, sc, val, ref in ((dHq, dHs, dH, "dH"), (dUq, dUs, dU, "dU")):
+        sf = sf_unpack(sc.cpu().numpy(), n, f // 32)
+        dq = O.dequantize_mxfp8(q.cpu().numpy(), sf)
+        assert max_abs_rel(dq[:u], c["bwd"][ref]) <= TOL, ref
+        # every code sits in its own row and column: within E4M3 rounding (2^-4
+        # relative, half a subnormal step 2^(s-10) absolute) of the kernel's own
+        # bf16 value, plus that value's bf16 rounding (2^-8 relative)
+        x = f64(val)[:u]
+        step = np.repeat(np.exp2(sf[:u].astype(np.float64) - 127.0 - 10.0), 32, axis=1)
+        assert np.all(np.abs(dq[:u] - x) <= (2.0 ** -4 + 2.0 ** -8) * np.abs(x) + step), ref
 
 
 def test_mx_dgrad1(mcase):
