@@ -169,13 +169,6 @@ MOE_DEV void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, i
       "r"(smem_u32(smem_src)), "r"(x), "r"(y)
       : "memory");
 }
-// Bring a 2-D box of the tensor into L2 (no shared memory, no completion).
-MOE_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
 MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has read its source.
 MOE_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
