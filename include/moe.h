@@ -210,13 +210,16 @@ MOE_API int moe_route_noalloc(const moe_shape_t* shape, const void* x, const voi
 
 /* ------------------------------------------------------------ dispatch (a4)
  * Rowwise dispatch: xd[slot_of_route[t*k+j]] = x[t]; padding rows of every
- * expert are written as zeros.  BF16 mode: xd is bf16 [rows_max, d] and
- * xd_scales must be NULL.  MXFP8 mode: x[t] is quantised once (a15) and the
- * codes go to xd (uint8 E4M3 [rows_max, d]) and the scales to xd_scales (E8M0,
- * MOE_SF layout below); the payload is 33/32 byte per value. */
+ * expert are written as zeros.  BF16 mode: xd is bf16 [rows_max, d];
+ * xd_scales and xd_dq must be NULL.  MXFP8 mode: x[t] is quantised once (a15)
+ * and the codes go to xd (uint8 E4M3 [rows_max, d]) and the scales to
+ * xd_scales (E8M0, MOE_SF layout below); the payload is 33/32 byte per value.
+ * xd_dq (MXFP8 mode, nullable): also the dequantised rows, bf16 [rows_max, d],
+ * bit for bit what moe_dequantize_mxfp8 gives for xd (for the BF16 weight
+ * gradient). */
 MOE_API int moe_dispatch(const moe_shape_t* shape, const void* x, const int32_t* slot_of_route,
                  const int32_t* counts, const int32_t* tile_offsets, void* xd,
-                 uint8_t* xd_scales, void* stream);
+                 uint8_t* xd_scales, void* xd_dq, void* stream);
 
 /* ------------------------------------------------------------ MXFP8 (a15)
  * Quantise a bf16 matrix src [rows, cols] with one E8M0 scale per 32
@@ -324,13 +327,17 @@ typedef struct {
  * MXFP8 MMAs (E4M3 x E4M3, E8M0 scales, fp32 accumulation); every a and w operand is
  * uint8 codes with its scales in the matching sf array (MOE_SF layout):
  *   FWD1_SWIGLU   a0 = Xd_q [rows,d]; w0 = gu_q cache      out0 = H, out1 = U (bf16),
- *                                                          out2 = A_q [rows,f], osf0 = its scales
+ *                                                          out2 = A_q [rows,f], osf0 = its scales,
+ *                                                          out3 (nullable) = A dequantised, bf16
+ *                                                          [rows,f], bit for bit what
+ *                                                          moe_dequantize_mxfp8 gives for A_q
  *   FWD2          a0 = A_q; w0 = down_q cache              out0 = Y (bf16)
  *   DGRAD2_SWIGLU a0 = dY_q [rows,d]; w0 = downT_q cache;  out0 = dH, out1 = dU (bf16),
  *                 aux0 = H, aux1 = U (bf16)                out2 = dH_q, out3 = dU_q, osf0/osf1
  *   DGRAD1        a0 = dH_q, a1 = dU_q; w0 = gateT_q,      out0 = dXd (bf16)
  *                 w1 = upT_q
- * WGRAD1/WGRAD2 stay BF16 (on dequantised activations, moe_dequantize_mxfp8).
+ * WGRAD1/WGRAD2 stay BF16 (on dequantised activations: the dispatch's xd_dq,
+ * FWD1_SWIGLU's out3, or moe_dequantize_mxfp8).
  *
  * Weight gradients on the forward's natural MXFP8 layout ("MXFP8 Wgrad",
  * Section 24.2, Evidence 7 / Table 33 of "Supercharging Olmo-core for
@@ -364,11 +371,19 @@ MOE_API int moe_combine(const moe_shape_t* shape, const void* y, const float* ga
  *                   (padding rows zeroed)
  *   dlogits[t,e]  = g_j (dg_j - sum_i g_i dg_i) if e = topk_idx[t,j], else 0
  *                   fp32 [T, E] (exact gradient through the renormalised
- *                   softmax for the fixed selection) */
+ *                   softmax for the fixed selection)
+ *   dy_q, dy_scales  (both NULL, or both set): the MXFP8 quantisation of dy
+ *                   along d (a15) in the same pass, uint8 E4M3 [rows_max, d]
+ *                   and E8M0 scales in the MOE_SF layout: byte for byte what
+ *                   moe_quantize_mxfp8(block_axis = 1) gives for the bf16 dy
+ *                   rows of every tile (padding rows: zero codes, scale 2^0);
+ *                   rows past the last tile are not written.  One set without
+ *                   the other returns MOE_ERR_INVALID. */
 MOE_API int moe_combine_bwd(const moe_shape_t* shape, const void* d_out, const void* y,
                     const float* gates, const int32_t* topk_idx, const int32_t* slot_of_route,
                     const int32_t* counts, const int32_t* tile_offsets, void* dy,
-                    float* d_gates, float* dlogits, void* stream);
+                    float* d_gates, float* dlogits, uint8_t* dy_q, uint8_t* dy_scales,
+                    void* stream);
 
 /* ------------------------------------------------- dispatch / router backward (a13, a14)
  * dx[t] = sum_j dxd[slot(t,j)] + sum_j dlogits[t, e_tj] * W_r[e_tj]  (bf16 [T, d];
@@ -421,7 +436,9 @@ typedef struct {
 
 /* MXFP8 activation buffers (rows_max rows; scales in the MOE_SF layout).
  * xd_q/xd_s and a_q/a_s are written by the forward and read by the backward;
- * the rest is backward scratch. */
+ * so are xd_dq and a_dq (the forward writes them when they are non-NULL; the
+ * backward needs them, from the forward or from its own recompute); the rest
+ * is backward scratch. */
 typedef struct moe_mx_buffers {
   uint8_t* xd_q;  /* [rows_max, d] dispatched tokens, quantised once per token */
   uint8_t* xd_s;
@@ -498,9 +515,9 @@ MOE_API int moe_layer_fwd(const moe_shape_t* shape, const moe_fwd_args_t* args, 
  * "Section 24: Conclusion", Evidence 11, trades repeated dispatch and expert
  * compute for activation memory).  Recomputed values equal the saved ones bit
  * for bit (the same deterministic kernels on the same inputs).
- * MXFP8 mode: dY is quantised after the combine backward, DGRAD2/DGRAD1 run on
- * MXFP8 (the second weight cache), and the weight gradients run in BF16 on
- * dequantised Xd and A. */
+ * MXFP8 mode: dY is quantised in the combine backward's pass, DGRAD2/DGRAD1 run
+ * on MXFP8 (the second weight cache), and the weight gradients run in BF16 on
+ * the dequantised Xd and A that the forward (or the recompute) wrote. */
 MOE_API int moe_layer_bwd(const moe_shape_t* shape, const moe_bwd_args_t* args, const moe_saved_t* saved,
                   void* ws, void* stream);
 

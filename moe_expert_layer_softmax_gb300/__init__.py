@@ -133,13 +133,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_profile_stop": [_vp, _vp],
         "moe_route": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
         "moe_route_noalloc": [P(Shape)] + [_vp] * 11 + [_vp, _vp],
-        "moe_dispatch": [P(Shape)] + [_vp] * 6 + [_vp],
+        "moe_dispatch": [P(Shape)] + [_vp] * 7 + [_vp],
         "moe_quantize_mxfp8": [i32, i32, i32, i32, _vp, _vp, _vp, _vp],
         "moe_dequantize_mxfp8": [ctypes.c_int64, i32, _vp, _vp, _vp, _vp],
         "moe_build_mx_weights": [P(Shape), _vp, _vp, _vp, P(MxWeights), _vp],
         "moe_grouped_gemm": [P(Shape), i32, P(GemmArgs), _vp, _vp],
         "moe_combine": [P(Shape)] + [_vp] * 4 + [_vp],
-        "moe_combine_bwd": [P(Shape)] + [_vp] * 10 + [_vp],
+        "moe_combine_bwd": [P(Shape)] + [_vp] * 12 + [_vp],
         "moe_dispatch_bwd": [P(Shape)] + [_vp] * 6 + [_vp],
         "moe_router_bwd": [P(Shape)] + [_vp] * 7 + [_vp],
         "moe_layer_fwd": [P(Shape), P(FwdArgs), P(Saved), _vp, _vp],
@@ -310,10 +310,11 @@ def route_noalloc(s, x, w_router, logit_bias, logits, topk_idx, gates, counts, o
         _ptr(route_of_slot), _ptr(dev_error), _stream(stream)))
 
 
-def dispatch(s, x, slot_of_route, counts, tile_offsets, xd, xd_scales=None, stream=None):
+def dispatch(s, x, slot_of_route, counts, tile_offsets, xd, xd_scales=None, stream=None,
+             xd_dq=None):
     _check("moe_dispatch", load().moe_dispatch(
         ctypes.byref(s), _ptr(x), _ptr(slot_of_route), _ptr(counts), _ptr(tile_offsets), _ptr(xd),
-        _ptr(xd_scales), _stream(stream)))
+        _ptr(xd_scales), _ptr(xd_dq), _stream(stream)))
 
 
 def quantize_mxfp8(batch, rows, cols, block_axis, src, q, scales, stream=None):
@@ -345,10 +346,11 @@ def combine(s, y, gates, slot_of_route, out, stream=None):
 
 
 def combine_bwd(s, d_out, y, gates, topk_idx, slot_of_route, counts, tile_offsets, dy, d_gates,
-                dlogits, stream=None):
+                dlogits, stream=None, dy_q=None, dy_scales=None):
     _check("moe_combine_bwd", load().moe_combine_bwd(
         ctypes.byref(s), _ptr(d_out), _ptr(y), _ptr(gates), _ptr(topk_idx), _ptr(slot_of_route),
-        _ptr(counts), _ptr(tile_offsets), _ptr(dy), _ptr(d_gates), _ptr(dlogits), _stream(stream)))
+        _ptr(counts), _ptr(tile_offsets), _ptr(dy), _ptr(d_gates), _ptr(dlogits), _ptr(dy_q),
+        _ptr(dy_scales), _stream(stream)))
 
 
 def dispatch_bwd(s, dxd, slot_of_route, topk_idx, dlogits, w_router, dx, stream=None):

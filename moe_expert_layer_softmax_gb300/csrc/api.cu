@@ -171,7 +171,7 @@ int check_gemm_args_mx(int op, const moe_gemm_args_t* a) {
     case MOE_GEMM_FWD1_SWIGLU:
       MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->sfa0); MOE_NONNULL_ALIGNED(a->w0);
       MOE_NONNULL_ALIGNED(a->sfb0); MOE_NONNULL_ALIGNED(a->out0); MOE_NONNULL_ALIGNED(a->out1);
-      MOE_NONNULL_ALIGNED(a->out2); MOE_NONNULL_ALIGNED(a->osf0);
+      MOE_NONNULL_ALIGNED(a->out2); MOE_NONNULL_ALIGNED(a->osf0); MOE_ALIGNED_OR_NULL(a->out3);
       break;
     case MOE_GEMM_FWD2:
       MOE_NONNULL_ALIGNED(a->a0); MOE_NONNULL_ALIGNED(a->sfa0); MOE_NONNULL_ALIGNED(a->w0);
@@ -270,11 +270,13 @@ int expert_forward(const moe_shape_t* s, const void* x, const void* w_gate, cons
                    const moe_saved_t* sv, void* ws, cudaStream_t st) {
   moe_gemm_args_t g = {};
   if (s->prec == MOE_MXFP8) {
+    // the dequantised Xd and A (for the weight gradients) come out of the same passes
     MOE_CUDA(launch_dispatch_mxfp8(x, sv->slot_of_route, sv->counts, sv->tile_offsets, s->T,
-                                   s->d_model, s->n_experts, s->top_k, b->xd_q, b->xd_s, st));
+                                   s->d_model, s->n_experts, s->top_k, b->xd_q, b->xd_s, st,
+                                   b->xd_dq));
     g.tile_offsets = sv->tile_offsets;
     g.a0 = b->xd_q; g.sfa0 = b->xd_s; g.w0 = w->gu_q; g.sfb0 = w->gu_s;
-    g.out0 = sv->h; g.out1 = sv->u; g.out2 = b->a_q; g.osf0 = b->a_s;
+    g.out0 = sv->h; g.out1 = sv->u; g.out2 = b->a_q; g.osf0 = b->a_s; g.out3 = b->a_dq;
     MOE_TRY(gemm_impl(s, MOE_GEMM_FWD1_SWIGLU, &g, ws, st));
     g = moe_gemm_args_t{};
     g.tile_offsets = sv->tile_offsets;
@@ -419,7 +421,7 @@ int moe_route(const moe_shape_t* s, const void* x, const void* w_router, const f
 
 int moe_dispatch(const moe_shape_t* s, const void* x, const int32_t* slot_of_route,
                  const int32_t* counts, const int32_t* tile_offsets, void* xd, uint8_t* xd_scales,
-                 void* stream) {
+                 void* xd_dq, void* stream) {
   MOE_TRY(check_shape(s));
   MOE_TRY(ready_or_error());
   MOE_NONNULL_ALIGNED(x);
@@ -429,12 +431,13 @@ int moe_dispatch(const moe_shape_t* s, const void* x, const int32_t* slot_of_rou
   MOE_NONNULL_ALIGNED(xd);
   if (s->prec == MOE_MXFP8) {
     MOE_NONNULL_ALIGNED(xd_scales);
+    MOE_ALIGNED_OR_NULL(xd_dq);
     MOE_CUDA(launch_dispatch_mxfp8(x, slot_of_route, counts, tile_offsets, s->T, s->d_model,
                                    s->n_experts, s->top_k, static_cast<uint8_t*>(xd), xd_scales,
-                                   static_cast<cudaStream_t>(stream)));
+                                   static_cast<cudaStream_t>(stream), xd_dq));
     return MOE_OK;
   }
-  if (xd_scales != nullptr) return MOE_ERR_INVALID;
+  if (xd_scales != nullptr || xd_dq != nullptr) return MOE_ERR_INVALID;
   MOE_CUDA(launch_dispatch_bf16(x, slot_of_route, counts, tile_offsets, s->T, s->d_model,
                                 s->n_experts, s->top_k, xd, static_cast<cudaStream_t>(stream)));
   return MOE_OK;
@@ -525,7 +528,7 @@ int moe_combine(const moe_shape_t* s, const void* y, const float* gates,
 int moe_combine_bwd(const moe_shape_t* s, const void* d_out, const void* y, const float* gates,
                     const int32_t* topk_idx, const int32_t* slot_of_route, const int32_t* counts,
                     const int32_t* tile_offsets, void* dy, float* d_gates, float* dlogits,
-                    void* stream) {
+                    uint8_t* dy_q, uint8_t* dy_scales, void* stream) {
   MOE_TRY(check_shape(s));
   MOE_TRY(ready_or_error());
   MOE_NONNULL_ALIGNED(d_out);
@@ -538,9 +541,12 @@ int moe_combine_bwd(const moe_shape_t* s, const void* d_out, const void* y, cons
   MOE_NONNULL_ALIGNED(dy);
   MOE_NONNULL_ALIGNED(d_gates);
   MOE_ALIGNED_OR_NULL(dlogits);
+  MOE_ALIGNED_OR_NULL(dy_q);
+  MOE_ALIGNED_OR_NULL(dy_scales);
+  if ((dy_q == nullptr) != (dy_scales == nullptr)) return MOE_ERR_INVALID;
   MOE_CUDA(launch_combine_bwd(d_out, y, gates, topk_idx, slot_of_route, counts, tile_offsets, s->T,
                               s->d_model, s->n_experts, s->top_k, dy, d_gates, dlogits,
-                              static_cast<cudaStream_t>(stream)));
+                              static_cast<cudaStream_t>(stream), nullptr, 0.0f, dy_q, dy_scales));
   return MOE_OK;
 }
 
@@ -674,14 +680,14 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
   if (!isfinite(a->lb_coef)) return MOE_ERR_INVALID;
   const bool lb = a->lb_coef != 0.0f;
   const float lb_scale = lb ? a->lb_coef * (float)s->n_experts / (float)s->T : 0.0f;
+  // MXFP8: dY is quantised along d (for GEMM2's data gradient) in the same pass
   MOE_CUDA(launch_combine_bwd(a->d_out, sv->y, sv->gates, sv->topk_idx, sv->slot_of_route,
                               sv->counts, sv->tile_offsets, s->T, s->d_model, s->n_experts,
-                              s->top_k, a->dy, a->d_gates, a->dlogits, st, sv->logits, lb_scale));
+                              s->top_k, a->dy, a->d_gates, a->dlogits, st, sv->logits, lb_scale,
+                              mx ? a->mx->dy_q : nullptr, mx ? a->mx->dy_s : nullptr));
   if (mx) {
     const moe_mx_weights_t* w = a->mx_weights;
     const moe_mx_buffers_t* b = a->mx;
-    const int64_t rows = rows_max_of(s);
-    MOE_CUDA(launch_quantize_mxfp8(1, (int)rows, s->d_model, 1, a->dy, b->dy_q, b->dy_s, st));
     moe_gemm_args_t g = {};
     g.tile_offsets = sv->tile_offsets;
     g.a0 = b->dy_q; g.sfa0 = b->dy_s; g.w0 = w->downT_q; g.sfb0 = w->downT_s;
@@ -689,7 +695,6 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
     g.out0 = a->dh; g.out1 = a->du; g.out2 = b->dh_q; g.out3 = b->du_q;
     g.osf0 = b->dh_s; g.osf1 = b->du_s;
     MOE_TRY(gemm_impl(s, MOE_GEMM_DGRAD2_SWIGLU, &g, ws, st));
-    MOE_CUDA(launch_dequantize_mxfp8(b->a_q, b->a_s, rows, s->d_ff, b->a_dq, st));
     g = moe_gemm_args_t{};
     g.tile_offsets = sv->tile_offsets;
     g.a0 = a->dy; g.a1 = b->a_dq; g.out0 = a->dw_down;
@@ -700,7 +705,6 @@ int moe_layer_bwd(const moe_shape_t* s, const moe_bwd_args_t* a, const moe_saved
     g.w0 = w->gateT_q; g.sfb0 = w->gateT_s; g.w1 = w->upT_q; g.sfb1 = w->upT_s;
     g.out0 = a->dxd;
     MOE_TRY(gemm_impl(s, MOE_GEMM_DGRAD1, &g, ws, st));
-    MOE_CUDA(launch_dequantize_mxfp8(b->xd_q, b->xd_s, rows, s->d_model, b->xd_dq, st));
     g = moe_gemm_args_t{};
     g.tile_offsets = sv->tile_offsets;
     g.a0 = a->dh; g.a1 = a->du; g.aux0 = b->xd_dq; g.out0 = a->dw_gate; g.out1 = a->dw_up;

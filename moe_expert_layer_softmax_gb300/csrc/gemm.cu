@@ -94,8 +94,8 @@ struct __align__(8) Ctl {
   uint64_t rawfull[kMaxStages];  // in-kernel dequantisation: this CTA's codes + scales landed
   uint64_t bfull[4];             // converted B slot ready (even CTA, both CTAs' converters)
   uint64_t bempty[4];            // B slot free again (the pair's MMAs that read it are done)
-  uint64_t hufull[4];            // MXFP8 SwiGLU backward: H and U chunk landed (2 halves x 2 sets)
-  uint64_t huwritten[4];         //   dH and dU written over it by the half's 128 epilogue threads
+  uint64_t hufull[2];            // MXFP8 SwiGLU backward, per column half: H and U chunk landed,
+  uint64_t huwritten[2];         //   dH and dU written over it by the half's 128 epilogue threads,
   uint64_t codefree[2];          //   the half's code buffer read by the previous chunk's stores
   uint32_t tmem_base;
   int abort;
@@ -1201,13 +1201,15 @@ constexpr uint32_t kMxSfColsPerStage = 16;
 constexpr int kMxStageHalfBytes = kTileM * 64;
 static_assert(kMxPairStages * kMxPairStageBytes + 2 * kMxStageHalfBytes <=
                   kRingBytes + 2 * kStageOutBytes, "MXFP8 pair shared memory");
-// The SwiGLU backward also reads H and U: each half has two sets of (H, U)
-// 32-column chunks (8 KB each, the output layout), TMA-loaded one chunk ahead;
-// dH and dU overwrite them in place and leave by TMA store.  A 4-stage ring
-// makes room.
-constexpr int kMxBwdStages = 4;
+// The SwiGLU backward also reads H and U: each half has one set of (H, U)
+// 32-column chunks (8 KB each, the output layout), TMA-loaded as soon as the
+// previous chunk has left; dH and dU overwrite them in place and leave by TMA
+// store.  A 5-stage ring makes room (measured on 8 experts x 4096 rows,
+// d = 4096, f = 2048: 4 stages with two sets per half 0.278 ms, 5 stages with
+// one set 0.255 ms: the main loop waited for operands 30 % of its time).
+constexpr int kMxBwdStages = 5;
 constexpr int kMxHuSetBytes = 2 * kTileM * 64;
-constexpr int kMxHuHalfBytes = 2 * kMxHuSetBytes;
+constexpr int kMxHuHalfBytes = kMxHuSetBytes;
 // Their E4M3 codes leave the same way: per half one buffer of dH codes and one
 // of dU codes, 128 rows x 32 bytes each (32-byte swizzle), after the H/U sets.
 constexpr int kMxCodeHalfBytes = 2 * kTileM * 32;
@@ -1327,6 +1329,9 @@ struct MxStager {
     if (leader) bulk_wait_read_all();
     bar_sync(bar_id, kEpiThreads / 2);
   }
+  MOE_DEV void put16(int j, uint4 v) const {   // 16 raw bytes: granule j of row r
+    *reinterpret_cast<uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) = v;
+  }
   MOE_DEV void put32(const uint32_t* v) const {   // 32 fp32 -> 32 bf16 of row r
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -1352,12 +1357,13 @@ struct MxStager {
 };
 
 // Thread (lane quarter q, column half h) owns accumulator row 32q + lane,
-// columns [128h, 128h + 128).  bf16 outputs go through the half's stager
-// (maps tO0, tO1), E4M3 codes and E8M0 scales are stored directly (each
-// thread writes whole 32-byte sectors of codes).
+// columns [128h, 128h + 128).  bf16 outputs and E4M3 codes leave through
+// shared memory and TMA stores (maps tO0, tO1: bf16 outputs; SwiGLU forward:
+// tQ1 = A's codes, tQ0 = A dequantised), E8M0 scales by direct stores.
 MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                               int rank, uint8_t* stage_base, const CUtensorMap* tO0,
-                              const CUtensorMap* tO1) {
+                              const CUtensorMap* tO1, const CUtensorMap* tQ0,
+                              const CUtensorMap* tQ1) {
   const int nt = total_tiles_pair(p, s);
   const uint32_t tempty0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
   const int quarter = warp & 3;
@@ -1370,8 +1376,8 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
   st.bar_id = 1 + half;
   st.leader = (warp == 4 + 4 * half) && (lane == 0);
   st.r = r;
-  uint64_t* hu_full = &s.hufull[2 * half];
-  uint64_t* hu_written = &s.huwritten[2 * half];
+  uint64_t* hu_full = &s.hufull[half];
+  uint64_t* hu_written = &s.huwritten[half];
   uint32_t vt = 0;   // valid tiles done (SwiGLU backward: the sets' use count)
   int it = 0;
   for (int t = (int)blockIdx.x / 2; t < nt; t += (int)gridDim.x / 2, ++it) {
@@ -1405,11 +1411,37 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
 #pragma unroll
       for (int i = 0; i < 64; ++i)
         v[i] = __float_as_uint(silu_f(__uint_as_float(v[i])) * __uint_as_float(v[64 + i]));
-      uint8_t* Aq = static_cast<uint8_t*>(p.out2) + row * p.ldo + fc;
-      // blocks fc/32 and fc/32 + 1 (fc/32 even): adjacent scale bytes, one store
-      const uint32_t s0 = mx_quant32(v, Aq), s1 = mx_quant32(v + 32, Aq + 32);
+      // A's blocks fc/32 and fc/32 + 1 (fc/32 even): adjacent scale bytes, one
+      // store; the row's 64 code bytes through the stager
+      uint4 q[4];
+      const uint32_t s0 = mx_quant32_regs(v, q[0], q[1]), s1 = mx_quant32_regs(v + 32, q[2], q[3]);
       *reinterpret_cast<uint16_t*>(p.osf0 + sf_offset(row, fc / 32, p.osf_kb)) =
           (uint16_t)(s0 | (s1 << 8));
+      st.begin();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st.put16(j, q[j]);
+      st.end(tQ1, fc, y);
+      if (p.out3 != nullptr) {
+        // A dequantised for the weight gradient: code value x 2^(scale - 127),
+        // rounded to bf16, as the dequantiser computes it
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const float sc = ldexpf(1.0f, (int)(b ? s1 : s0) - 127);
+          const uint32_t w[8] = {q[2 * b].x, q[2 * b].y, q[2 * b].z, q[2 * b].w,
+                                 q[2 * b + 1].x, q[2 * b + 1].y, q[2 * b + 1].z, q[2 * b + 1].w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            float lo0, hi0, lo1, hi1;
+            e4m3x2_to_f32(w[u] & 0xFFFFu, lo0, hi0);
+            e4m3x2_to_f32(w[u] >> 16, lo1, hi1);
+            v[64 + 4 * u + 0] = __float_as_uint(lo0 * sc);
+            v[64 + 4 * u + 1] = __float_as_uint(hi0 * sc);
+            v[64 + 4 * u + 2] = __float_as_uint(lo1 * sc);
+            v[64 + 4 * u + 3] = __float_as_uint(hi1 * sc);
+          }
+          st.store32(v + 64, tQ0, fc + 32 * b, y);
+        }
+      }
     } else {   // EPI_SWIGLU_BWD_MX: dA for f columns n_tile * 256 + 128 * half + [0, 128)
       const int fc = ti.n_tile * kMxPairBN + 128 * half;
       uint8_t* cbuf = stage_base + 2 * kMxHuHalfBytes + half * kMxCodeHalfBytes;
@@ -1417,12 +1449,11 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
       bool fine = true;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int j = c & 1;
-        uint8_t* hb = st.buf + j * kMxHuSetBytes;
+        uint8_t* hb = st.buf;
         uint8_t* ub = hb + kMxHuSetBytes / 2;
-        // chunk c is use 2 vt + c / 2 of set j
-        const uint32_t u = 2u * vt + (uint32_t)(c >> 1);
-        fine = fine && mbar_wait(&hu_full[j], u & 1u, &s.abort, p.err);
+        // chunk c is use 4 vt + c of the half's set
+        const uint32_t u = 4u * vt + (uint32_t)c;
+        fine = fine && mbar_wait(hu_full, u & 1u, &s.abort, p.err);
         uint32_t gu[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1455,7 +1486,7 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
         *reinterpret_cast<uint4*>(cbuf + kTileM * 32 + r * 32 + 16 * sw) = ul;
         *reinterpret_cast<uint4*>(cbuf + kTileM * 32 + r * 32 + 16 * (1 ^ sw)) = uh;
         fence_proxy_async_smem();
-        mbar_arrive(&hu_written[j]);   // the half's mover stores dH, dU, the codes and refills the set
+        mbar_arrive(hu_written);   // the half's mover stores dH, dU, the codes and refills the set
       }
       const size_t so = sf_offset(row, fc / 32, p.osf_kb);
       *reinterpret_cast<uint32_t*>(p.osf0 + so) = sh;
@@ -1468,25 +1499,24 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
 }
 
 // MXFP8 SwiGLU backward: one thread per column half (lane 0 of warp 2 + half)
-// moves H and U chunks (32 columns x 128 rows each) into the half's two
-// shared-memory sets, and dH, dU and their E4M3 codes out of the sets and the
-// half's code buffer, so that the epilogue warps never wait for a bulk copy to
-// read shared memory.  Set j holds chunks j and j + 2 of each of the CTA's
-// valid tiles in turn; its u-th use completes phase u of hufull[j] (H, U
-// landed) and then of huwritten[j] (the half's 128 epilogue threads wrote dH,
-// dU over them and the chunk's codes into the code buffer).  Phase g of
-// codefree[half] completes when the stores of the CTA's g-th chunk have read
-// the code buffer.  At most one copy per set is in flight.
+// moves H and U chunks (32 columns x 128 rows each) into the half's set and
+// dH, dU and their E4M3 codes out of the set and the half's code buffer, so
+// that the epilogue warps never wait for a bulk copy to read shared memory.
+// The set holds chunks 0-3 of each of the CTA's valid tiles in turn; its g-th
+// use completes phase g of hufull (H, U landed) and then of huwritten (the
+// half's 128 epilogue threads wrote dH, dU over them and the chunk's codes into
+// the code buffer); phase g of codefree completes when the g-th chunk's stores
+// have read the set and the code buffer.  One copy is in flight at most.
 MOE_DEV void hu_mover_mx_pair(const Params& p, Ctl& s, int rank, int half, uint8_t* stage_base,
                               const CUtensorMap* tO0, const CUtensorMap* tO1,
                               const CUtensorMap* tH, const CUtensorMap* tU,
                               const CUtensorMap* tQ0, const CUtensorMap* tQ1) {
   const int nt = total_tiles_pair(p, s);
   const int step = (int)gridDim.x / 2;
-  uint8_t* buf = stage_base + half * kMxHuHalfBytes;
+  uint8_t* set = stage_base + half * kMxHuHalfBytes;
   uint8_t* cbuf = stage_base + 2 * kMxHuHalfBytes + half * kMxCodeHalfBytes;
-  uint64_t* full = &s.hufull[2 * half];
-  uint64_t* written = &s.huwritten[2 * half];
+  uint64_t* full = &s.hufull[half];
+  uint64_t* written = &s.huwritten[half];
   // the next valid tile at or after t, with its first column and row
   auto next_valid = [&](int t, int& fc, int& y) -> int {
     for (; t < nt; t += step) {
@@ -1500,28 +1530,21 @@ MOE_DEV void hu_mover_mx_pair(const Params& p, Ctl& s, int rank, int half, uint8
     }
     return nt;
   };
-  uint32_t loads0 = 0, loads1 = 0;   // copies issued into set 0 and set 1
-  auto load = [&](int j, int x, int y) {
-    uint8_t* set = buf + j * kMxHuSetBytes;
-    mbar_arrive_expect_tx(&full[j], (uint32_t)kMxHuSetBytes);
-    tma_load_2d(set, tH, &full[j], x, y);
-    tma_load_2d(set + kMxHuSetBytes / 2, tU, &full[j], x, y);
-    if (j == 0) ++loads0; else ++loads1;
+  uint32_t loads = 0;
+  auto load = [&](int x, int y) {
+    mbar_arrive_expect_tx(full, (uint32_t)kMxHuSetBytes);
+    tma_load_2d(set, tH, full, x, y);
+    tma_load_2d(set + kMxHuSetBytes / 2, tU, full, x, y);
+    ++loads;
   };
   int fc = 0, y = 0, nfc = 0, ny = 0;
   int t = next_valid((int)blockIdx.x / 2, fc, y);
-  if (t < nt) {
-    load(0, fc, y);
-    load(1, fc + 32, y);
-  }
+  if (t < nt) load(fc, y);
   bool ok = true;
-  for (uint32_t vt = 0; ok && t < nt; ++vt) {
+  for (uint32_t g = 0; ok && t < nt; g += 4) {
     const int tn = next_valid(t + step, nfc, ny);
     for (int c = 0; c < 4; ++c) {
-      const int j = c & 1;
-      const uint32_t u = 2u * vt + (uint32_t)(c >> 1);
-      if (!mbar_wait(&written[j], u & 1u, &s.abort, p.err)) { ok = false; break; }
-      uint8_t* set = buf + j * kMxHuSetBytes;
+      if (!mbar_wait(written, (g + (uint32_t)c) & 1u, &s.abort, p.err)) { ok = false; break; }
       tma_store_2d(tO0, set, fc + 32 * c, y);
       tma_store_2d(tO1, set + kMxHuSetBytes / 2, fc + 32 * c, y);
       tma_store_2d(tQ0, cbuf, fc + 32 * c, y);
@@ -1529,22 +1552,18 @@ MOE_DEV void hu_mover_mx_pair(const Params& p, Ctl& s, int rank, int half, uint8
       bulk_commit();
       bulk_wait_read_all();
       mbar_arrive(&s.codefree[half]);
-      // the set's next use: chunk c + 2 of this tile, else chunk j of the next tile
-      if (c + 2 < 4) load(j, fc + 32 * (c + 2), y);
-      else if (tn < nt) load(j, nfc + 32 * j, ny);
+      // the set's next chunk: c + 1 of this tile, else chunk 0 of the next tile
+      if (c + 1 < 4) load(fc + 32 * (c + 1), y);
+      else if (tn < nt) load(nfc, ny);
     }
     t = tn;
     fc = nfc;
     y = ny;
   }
-  if (!ok) {   // the last copy into each set may still be in flight: let it land
-    for (int j = 0; j < 2; ++j) {
-      const uint32_t n = j == 0 ? loads0 : loads1;
-      if (n == 0) continue;
-      const uint32_t a = smem_u32(&full[j]);
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(a, (n - 1u) & 1u) && globaltimer() - t0 < 100000ull) {}
-    }
+  if (!ok && loads > 0) {   // the last copy into the set may still be in flight: let it land
+    const uint32_t a = smem_u32(full);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, (loads - 1u) & 1u) && globaltimer() - t0 < 100000ull) {}
   }
   bulk_wait_all();   // stores complete before the CTA exits
 }
@@ -1583,11 +1602,11 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
     }
     mbar_init(&s.tfull[0], 1);
     mbar_init(&s.tempty[0], 2 * kEpiThreads);
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s.hufull[i], 1);
       mbar_init(&s.huwritten[i], kEpiThreads / 2);
+      mbar_init(&s.codefree[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&s.codefree[i], 1);
     mbar_init(&s.fin, 1);
     s.abort = 0;
     fence_barrier_init();
@@ -1642,7 +1661,7 @@ __global__ void __launch_bounds__(kMxPairThreads, 1)
   } else {
     setmaxnreg_inc<kMxPairEpiRegs>();
     epilogue_mx_pair(p, s, tmem_base, warp, lane, rank, ring + p.stages * p.stage_bytes, &tO0,
-                     &tO1);
+                     &tO1, &tQ0, &tQ1);
   }
 
   tc_fence_before();
@@ -1775,6 +1794,12 @@ cudaError_t launch_mx_pair(Params p, const CUtensorMap& A0, const CUtensorMap& A
          make_map(&MU, p.aux1, ocols, rows, 32, kTileM, MAP_BF16, 64) &&
          make_map(&QH, p.out2, ocols, rows, 32, kTileM, MAP_U8, 32) &&
          make_map(&QU, p.out3, ocols, rows, 32, kTileM, MAP_U8, 32);
+  // SwiGLU forward: A's codes (out2, 64-byte boxes) and, when asked for, A
+  // dequantised (out3, bf16, 32-column boxes), both with the 64-byte swizzle
+  if (ok && p.epi == EPI_SWIGLU_FWD_MX) {
+    ok = make_map(&QU, p.out2, ocols, rows, 64, kTileM, MAP_U8, 64);
+    if (ok && p.out3 != nullptr) ok = make_map(&QH, p.out3, ocols, rows, 32, kTileM, MAP_BF16, 64);
+  }
   if (!ok) return cudaErrorInvalidValue;
   // the register split above assumes the launch allocation it was computed for
   // (a smaller one would leave setmaxnreg.inc waiting for registers forever)
@@ -1984,7 +2009,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
            make_map(&B0, g.w0, d, (uint64_t)E * 2 * f, 128, 128, MAP_U8);
       A1 = A0; B1 = B0;
       p.sfa0 = p.sfa1 = g.sfa0; p.sfb0 = p.sfb1 = g.sfb0; p.sf_ka = p.sf_kb = d / 128;
-      p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.osf0 = g.osf0; p.osf_kb = f / 32;
+      p.out0 = g.out0; p.out1 = g.out1; p.out2 = g.out2; p.out3 = g.out3; p.osf0 = g.osf0;
+      p.osf_kb = f / 32;
       p.ldo = f;
       max_tiles = (int64_t)(rows / kTileM) * p.n_tiles;
       break;

@@ -71,7 +71,8 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                int E, int k, void* dy, float* d_gates, float* dlogits,
                                cudaStream_t s,
-                               const float* lb_logits = nullptr, float lb_scale = 0.0f);
+                               const float* lb_logits = nullptr, float lb_scale = 0.0f,
+                               uint8_t* dyq = nullptr, uint8_t* dys = nullptr);
 cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
                                 const int32_t* topk_idx, const float* dlogits,
                                 const void* w_router, int T, int d, int E, int k, void* dx,
@@ -165,7 +166,8 @@ cudaError_t launch_quantize_mxfp8_both(int batch, int rows, int cols, const void
                                        uint8_t* q_cols, uint8_t* sf_cols, cudaStream_t s);
 cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
                                   const int32_t* counts, const int32_t* tile_offsets, int T, int d,
-                                  int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s);
+                                  int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s,
+                                  void* xdq = nullptr);
 cudaError_t launch_dequantize_mxfp8(const uint8_t* q, const uint8_t* sf, int64_t rows, int K,
                                     void* out, cudaStream_t s);
 cudaError_t gemm_init_attributes();

@@ -27,6 +27,13 @@ MOE_DEV void zero_row(uint4* base, int d, int lane) {
   for (int c = lane; c < nv; c += 32) base[c] = z;
 }
 
+// MXFP8 codes of an all-zero row: zero codes, every block scale 2^0 (byte 127).
+MOE_DEV void zero_row_mx(uint8_t* codes, uint8_t* scales, int64_t row, int d, int lane) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int c = lane; c < d / 16; c += 32) reinterpret_cast<uint4*>(codes)[c] = z;
+  for (int b = lane; b < d / 32; b += 32) scales[sf_offset(row, b, d / 32)] = 127;
+}
+
 // Padding rows of expert e: [128*tile_off[e] + counts[e], 128*tile_off[e+1]).
 // `p` enumerates E*128 candidates; returns the row or -1.
 MOE_DEV int pad_row(int p, const int32_t* counts, const int32_t* tile_offsets) {
@@ -131,14 +138,17 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(
 
 // KM = compile-time bound on k (4 and 8 cover the workloads; 32 is the generic
 // fallback).  Per 256-column chunk a lane loads dOut once and the k rows of y
-// together, so k + 1 16-byte loads are in flight per lane.
+// together, so k + 1 16-byte loads are in flight per lane.  With dyq non-null
+// every dy row is also quantised to MXFP8 along d (the bf16 values stored in
+// dy, 32 per block: four lanes' vectors), exactly as the row quantiser would.
 template <int KM>
 __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1)) combine_bwd_kernel(
     const uint4* __restrict__ d_out, const uint4* __restrict__ y, const float* __restrict__ gates,
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
-    int E, int k, int token_blocks, uint4* __restrict__ dy, float* __restrict__ d_gates,
-    float* __restrict__ dlogits, const float* __restrict__ lb_logits, float lb_scale) {
+    int E, int k, int token_blocks, uint4* __restrict__ dy, uint8_t* __restrict__ dyq,
+    uint8_t* __restrict__ dys, float* __restrict__ d_gates, float* __restrict__ dlogits,
+    const float* __restrict__ lb_logits, float lb_scale) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nv = d / kVec;
@@ -146,7 +156,10 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
     const int p = (blockIdx.x - token_blocks) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (p >= E * kTileM) return;
     const int row = pad_row(p, counts, tile_offsets);
-    if (row >= 0) MOE_CHECKED(row, rows_max_of(T, k, E)) zero_row(dy + (size_t)row * nv, d, lane);
+    if (row >= 0) MOE_CHECKED(row, rows_max_of(T, k, E)) {
+      zero_row(dy + (size_t)row * nv, d, lane);
+      if (dyq != nullptr) zero_row_mx(dyq + (size_t)row * d, dys, row, d, lane);
+    }
     return;
   }
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -163,28 +176,58 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
     part[j] = 0.0f;
   }
   const uint4* dO = d_out + (size_t)t * nv;
+  // d is a multiple of 128 (nv of 16): the four lanes of a 32-column block are
+  // all in range or all out of it, and every lane takes part in the shuffles
   for (int c0 = 0; c0 < nv; c0 += 32) {      // warp-uniform
     const int c = c0 + lane;
-    if (c < nv) {
-      float a[kVec];
-      unpack8(__ldg(dO + c), a);
-      uint4 yv[KM];
+    const bool act = c < nv;
+    float a[kVec];
+    unpack8(act ? __ldg(dO + c) : make_uint4(0, 0, 0, 0), a);
+    uint4 yv[KM];
 #pragma unroll
-      for (int j = 0; j < KM; ++j) {
-        yv[j] = make_uint4(0, 0, 0, 0);
-        if (j < k) MOE_CHECKED(slot[j], rows_max_of(T, k, E)) yv[j] = __ldg(y + (size_t)slot[j] * nv + c);
+    for (int j = 0; j < KM; ++j) {
+      yv[j] = make_uint4(0, 0, 0, 0);
+      const int sj = KM > 8 ? __shfl_sync(0xffffffffu, my_slot, j < k ? j : 0) : slot[j];
+      if (j < k && act) MOE_CHECKED(sj, rows_max_of(T, k, E)) yv[j] = __ldg(y + (size_t)sj * nv + c);
+    }
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
+        float b[kVec];
+        unpack8(yv[j], b);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) part[j] = fmaf(a[i], b[i], part[j]);
       }
+    }
+    // the k dy rows (g_j dOut[t]) once the y rows are no longer held
 #pragma unroll
-      for (int j = 0; j < KM; ++j) {
-        if (j < k) {
-          float b[kVec], o[kVec];
-          unpack8(yv[j], b);
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
+        // k > 8: the route's slot and gate from the lane that holds them
+        const int sj = KM > 8 ? __shfl_sync(0xffffffffu, my_slot, j) : slot[j];
+        const float gj = KM > 8 ? __shfl_sync(0xffffffffu, my_g, j) : g[j];
+        float o[kVec];
 #pragma unroll
-          for (int i = 0; i < kVec; ++i) {
-            part[j] = fmaf(a[i], b[i], part[j]);
-            o[i] = g[j] * a[i];
+        for (int i = 0; i < kVec; ++i) o[i] = gj * a[i];
+        const uint4 ob = pack8(o);
+        if (act) MOE_CHECKED(sj, rows_max_of(T, k, E)) dy[(size_t)sj * nv + c] = ob;
+        if (dyq != nullptr) {   // warp-uniform
+          float q[kVec];
+          unpack8(ob, q);
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) amax = fmaxf(amax, fabsf(q[i]));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          const int sx = mx_scale_exp(amax);
+          const float inv = ldexpf(1.0f, -sx);
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) q[i] *= inv;
+          const uint2 code = e4m3x8(q);
+          if (act) MOE_CHECKED(sj, rows_max_of(T, k, E)) {
+            reinterpret_cast<uint2*>(dyq + (size_t)sj * d)[c] = code;
+            if ((lane & 3) == 0) dys[sf_offset(sj, c / 4, d / 32)] = (uint8_t)(sx + 127);
           }
-          MOE_CHECKED(slot[j], rows_max_of(T, k, E)) dy[(size_t)slot[j] * nv + c] = pack8(o);
         }
       }
     }
@@ -455,23 +498,24 @@ cudaError_t launch_combine_bwd(const void* d_out, const void* y, const float* ga
                                const int32_t* topk_idx, const int32_t* slot_of_route,
                                const int32_t* counts, const int32_t* tile_offsets, int T, int d,
                                int E, int k, void* dy, float* d_gates, float* dlogits,
-                               cudaStream_t s, const float* lb_logits, float lb_scale) {
+                               cudaStream_t s, const float* lb_logits, float lb_scale,
+                               uint8_t* dyq, uint8_t* dys) {
   const int tb = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (k <= 4)
     launch_pdl(combine_bwd_kernel<4>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s,
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
-        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-        dlogits, lb_logits, lb_scale);
+        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), dyq, dys,
+        d_gates, dlogits, lb_logits, lb_scale);
   else if (k <= 8)
     launch_pdl(combine_bwd_kernel<8>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
-        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-        dlogits, lb_logits, lb_scale);
+        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), dyq, dys,
+        d_gates, dlogits, lb_logits, lb_scale);
   else
     launch_pdl(combine_bwd_kernel<32>, dim3(tb + pad_blocks(E)), dim3(kMoveThreads), 0, s, 
         static_cast<const uint4*>(d_out), static_cast<const uint4*>(y), gates, topk_idx,
-        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), d_gates,
-        dlogits, lb_logits, lb_scale);
+        slot_of_route, counts, tile_offsets, T, d, E, k, tb, static_cast<uint4*>(dy), dyq, dys,
+        d_gates, dlogits, lb_logits, lb_scale);
   return cudaGetLastError();
 }
 

@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
 __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ slot_of_route,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ tile_offsets, int T, int d,
-    int E, int k, int token_blocks, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+    int E, int k, int token_blocks, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+    uint4* __restrict__ xdq) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = kQThreads / 32;
@@ -215,6 +216,8 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
       uint2* dst = reinterpret_cast<uint2*>(xq + (size_t)row * d);
       for (int c = lane; c < nv; c += 32) dst[c] = make_uint2(0, 0);
       for (int b = lane; b < kb; b += 32) xs[sf_offset(row, b, kb)] = 127;
+      if (xdq != nullptr)
+        for (int c = lane; c < nv; c += 32) xdq[(size_t)row * nv + c] = make_uint4(0, 0, 0, 0);
     }
     return;
   }
@@ -238,11 +241,25 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= inv;
     const uint2 codes = e4m3x8(v);
+    // dequantised copy (the dequantiser's arithmetic: code value x 2^s, bf16)
+    uint4 dq = make_uint4(0, 0, 0, 0);
+    if (xdq != nullptr) {
+      const float sc = ldexpf(1.0f, s);
+      float f[8];
+      e4m3x2_to_f32(codes.x & 0xFFFFu, f[0], f[1]);
+      e4m3x2_to_f32(codes.x >> 16, f[2], f[3]);
+      e4m3x2_to_f32(codes.y & 0xFFFFu, f[4], f[5]);
+      e4m3x2_to_f32(codes.y >> 16, f[6], f[7]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] *= sc;
+      dq = pack8(f);
+    }
     for (int j = 0; j < k; ++j) {
       const int slot = __shfl_sync(0xffffffffu, my_slot, j);
       if (ok) MOE_CHECKED(slot, rows_max_of(T, k, E)) {
         reinterpret_cast<uint2*>(xq + (size_t)slot * d)[c] = codes;
         if ((lane & 3) == 0) xs[sf_offset(slot, c / 4, kb)] = (uint8_t)(s + 127);
+        if (xdq != nullptr) xdq[(size_t)slot * nv + c] = dq;
       }
     }
   }
@@ -302,12 +319,14 @@ cudaError_t launch_quantize_mxfp8_both(int batch, int rows, int cols, const void
 
 cudaError_t launch_dispatch_mxfp8(const void* x, const int32_t* slot_of_route,
                                   const int32_t* counts, const int32_t* tile_offsets, int T, int d,
-                                  int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s) {
+                                  int E, int k, uint8_t* xq, uint8_t* xs, cudaStream_t s,
+                                  void* xdq) {
   const int warps = kQThreads / 32;
   const int tb = (T + warps - 1) / warps;
   const int pb = (E * kTileM + warps - 1) / warps;
   launch_pdl(dispatch_mxfp8_kernel, dim3(tb + pb), dim3(kQThreads), 0, s, static_cast<const uint4*>(x), slot_of_route,
-                                                      counts, tile_offsets, T, d, E, k, tb, xq, xs);
+                                                      counts, tile_offsets, T, d, E, k, tb, xq, xs,
+                                                      static_cast<uint4*>(xdq));
   return cudaGetLastError();
 }
 

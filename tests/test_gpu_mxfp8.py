@@ -185,6 +185,16 @@ def test_mx_dispatch_writes_the_oracle_codes(mcase):
     want_s[real] = scales[ros[real] // c["k"]]
     np.testing.assert_array_equal(xq.cpu().numpy()[:used], want_q)
     np.testing.assert_array_equal(sf_unpack(xs.cpu().numpy(), n, d // 32)[:used], want_s)
+    # with the dequantised copy: the same codes, and that copy bit for bit the dequantiser's
+    xq2 = torch.full((n, d), 0x55, dtype=torch.uint8, device=dev)
+    xs2 = torch.full((n * d // 32,), 0x66, dtype=torch.uint8, device=dev)
+    xdq = torch.full((n, d), 7.0, dtype=torch.bfloat16, device=dev)
+    m.dispatch(c["s"], to_dev_bf16(c["inp"]["x"], dev), c["slot"], c["counts"], c["tile_offsets"],
+               xq2, xs2, xd_dq=xdq)
+    assert torch.equal(xq2[:used], xq[:used]) and torch.equal(xs2, xs)
+    ref = torch.empty(n, d, dtype=torch.bfloat16, device=dev)
+    m.dequantize_mxfp8(n, d, xq2, xs2, ref)
+    assert torch.equal(xdq[:used].view(torch.int16), ref[:used].view(torch.int16))
 
 
 def test_mx_fwd1_swiglu(mcase):
@@ -193,16 +203,21 @@ def test_mx_fwd1_swiglu(mcase):
     H, U = (torch.empty(n, f, dtype=torch.bfloat16, device=dev) for _ in range(2))
     Aq = torch.empty(n, f, dtype=torch.uint8, device=dev)
     As = torch.empty(n * f // 32, dtype=torch.uint8, device=dev)
+    Adq = torch.empty(n, f, dtype=torch.bfloat16, device=dev)
     xq, xs = c["rows_q"](c["fwd"]["Xd"], c["d"])
     m.grouped_gemm(c["s"], m.GEMM_FWD1_SWIGLU, c["ws"], tile_offsets=c["tile_offsets"], a0=xq,
                    sfa0=xs, w0=c["cache"]["gu_q"], sfb0=c["cache"]["gu_s"], out0=H, out1=U,
-                   out2=Aq, osf0=As)
+                   out2=Aq, osf0=As, out3=Adq)
     u = c["used"]
     assert m.read_error(c["ws"]) == 0
     assert max_abs_rel(f64(H)[:u], c["fwd"]["H"]) <= TOL
     assert max_abs_rel(f64(U)[:u], c["fwd"]["U"]) <= TOL
     a_deq = O.dequantize_mxfp8(Aq.cpu().numpy(), sf_unpack(As.cpu().numpy(), n, f // 32))
     assert max_abs_rel(a_deq[:u], c["fwd"]["Aq"]) <= TOL
+    # the dequantised copy is bit for bit the dequantiser's
+    ref = torch.empty(n, f, dtype=torch.bfloat16, device=dev)
+    m.dequantize_mxfp8(n, f, Aq, As, ref)
+    assert torch.equal(Adq[:u].view(torch.int16), ref[:u].view(torch.int16))
 
 
 def test_mx_fwd2(mcase):
@@ -239,6 +254,44 @@ def test_mx_dgrad2_swiglu_bwd(mcase):
         x = f64(val)[:u]
         step = np.repeat(np.exp2(sf[:u].astype(np.float64) - 127.0 - 10.0), 32, axis=1)
         assert np.all(np.abs(dq[:u] - x) <= (2.0 ** -4 + 2.0 ** -8) * np.abs(x) + step), ref
+
+
+def test_mx_combine_bwd_quantises_dy_in_the_same_pass(mcase):
+    # the fused quantisation writes byte for byte what the row quantiser gives
+    # for the dy rows the same call wrote (padding rows: zero codes, scale 2^0)
+    c = mcase
+    m, dev, n, d, T, k, E = c["m"], c["dev"], c["n"], c["d"], c["T"], c["k"], c["E"]
+    fwd = c["fwd"]
+    gates = torch.from_numpy(fwd["gates"].astype(np.float32)).to(dev)
+    topk = torch.from_numpy(fwd["topk_idx"].astype(np.int32)).to(dev)
+    y = c["rows_bf"](fwd["Y"], d)
+    dO = to_dev_bf16(c["inp"]["d_out"], dev)
+
+    def run(quant):
+        dy = torch.full((n, d), 5.0, dtype=torch.bfloat16, device=dev)
+        dg = torch.empty(T, k, dtype=torch.float32, device=dev)
+        dl = torch.empty(T, E, dtype=torch.float32, device=dev)
+        q = torch.full((n, d), 0x55, dtype=torch.uint8, device=dev) if quant else None
+        sc = torch.full((n * d // 32,), 0x66, dtype=torch.uint8, device=dev) if quant else None
+        m.combine_bwd(c["s"], dO, y, gates, topk, c["slot"], c["counts"], c["tile_offsets"], dy,
+                      dg, dl, dy_q=q, dy_scales=sc)
+        return dy, dg, dl, q, sc
+
+    dy, dg, dl, q, sc = run(True)
+    dy0, dg0, dl0, _, _ = run(False)
+    u = c["used"]
+    assert torch.equal(dy[:u].view(torch.int16), dy0[:u].view(torch.int16))
+    assert torch.equal(dg, dg0) and torch.equal(dl, dl0)
+    rq = torch.empty(n, d, dtype=torch.uint8, device=dev)
+    rs = torch.empty(n * d // 32, dtype=torch.uint8, device=dev)
+    m.quantize_mxfp8(1, n, d, 1, dy, rq, rs)
+    np.testing.assert_array_equal(q.cpu().numpy()[:u], rq.cpu().numpy()[:u])
+    np.testing.assert_array_equal(sf_unpack(sc.cpu().numpy(), n, d // 32)[:u],
+                                  sf_unpack(rs.cpu().numpy(), n, d // 32)[:u])
+    assert max_abs_rel(f64(dy)[:u], c["bwd"]["dY"]) <= TOL
+    with pytest.raises(m.MoEError):     # codes without scales
+        m.combine_bwd(c["s"], dO, y, gates, topk, c["slot"], c["counts"], c["tile_offsets"], dy,
+                      dg, dl, dy_q=q)
 
 
 def test_mx_dgrad1(mcase):
