@@ -432,15 +432,24 @@ MOE_DEV void tmem_dealloc_pair(uint32_t base, uint32_t ncols) {
 // One E8M0 scale per 32 consecutive values along the contraction axis:
 // 2^s with s the smallest integer such that amax <= 448 * 2^s, clamped to
 // [-127, 127] (s = 0 for an all-zero block); codes are E4M3(v / 2^s), round
-// to nearest even, saturating.  With amax = fr * 2^ex (fr in [0.5, 1)) and
-// 448 = 0.875 * 2^9: s = ex - 9 when fr <= 0.875, else ex - 8.
+// to nearest even, saturating.  From the bits of amax = 1.m * 2^(B - 127)
+// (B its biased exponent) and 448 = 1.75 * 2^8: s = B - 135 when 1.m <= 1.75
+// (mantissa field <= 0x600000), else B - 134.  A subnormal amax (< 2^-126)
+// gives s < -127, clamped.
 MOE_DEV int mx_scale_exp(float amax) {
-  if (!(amax > 0.0f)) return 0;
-  if (!isfinite(amax)) return 127;
-  int ex;
-  const float fr = frexpf(amax, &ex);
-  const int s = (fr <= 0.875f) ? ex - 9 : ex - 8;
-  return s < -127 ? -127 : (s > 127 ? 127 : s);
+  if (!(amax > 0.0f)) return 0;                 // zero block (a NaN never wins fmaxf)
+  const uint32_t bits = __float_as_uint(amax);
+  const int B = (int)(bits >> 23);              // sign bit clear
+  if (B == 255) return 127;                     // infinite
+  if (B == 0) return -127;
+  const int s = B - ((bits & 0x7FFFFFu) <= 0x600000u ? 135 : 134);
+  return s < -127 ? -127 : s;                   // B <= 254: s <= 120
+}
+
+// 2^e for e in [-127, 128], exactly (2^-127 is the subnormal with the top
+// mantissa bit; 2^128 is +inf): the block scales and their inverses.
+MOE_DEV float exp2i(int e) {
+  return e > -127 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
 // Two floats -> two E4M3 bytes (lo in the low byte), RNE, satfinite.

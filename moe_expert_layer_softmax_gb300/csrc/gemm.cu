@@ -596,7 +596,7 @@ MOE_DEV uint32_t mx_quant32_regs(const uint32_t* bits, uint4& lo, uint4& hi) {
     amax = fmaxf(amax, fabsf(v[i]));
   }
   const int sx = mx_scale_exp(amax);
-  const float inv = ldexpf(1.0f, -sx);
+  const float inv = exp2i(-sx);
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] *= inv;
   const uint2 q0 = e4m3x8(v), q1 = e4m3x8(v + 8), q2 = e4m3x8(v + 16), q3 = e4m3x8(v + 24);
@@ -1426,7 +1426,7 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
         // rounded to bf16, as the dequantiser computes it
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-          const float sc = ldexpf(1.0f, (int)(b ? s1 : s0) - 127);
+          const float sc = exp2i((int)(b ? s1 : s0) - 127);
           const uint32_t w[8] = {q[2 * b].x, q[2 * b].y, q[2 * b].z, q[2 * b].w,
                                  q[2 * b + 1].x, q[2 * b + 1].y, q[2 * b + 1].z, q[2 * b + 1].w};
 #pragma unroll

@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
           const int sx = mx_scale_exp(amax);
-          const float inv = ldexpf(1.0f, -sx);
+          const float inv = exp2i(-sx);
 #pragma unroll
           for (int i = 0; i < kVec; ++i) q[i] *= inv;
           const uint2 code = e4m3x8(q);

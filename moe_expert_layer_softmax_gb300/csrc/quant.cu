@@ -22,6 +22,12 @@ constexpr int kQThreads = 256;
 // One thread per 32-value block of a [rows, cols] bf16 matrix (K = cols).
 // Output row of input row r: r, or with `group` > 0 (interleaving two matrices
 // into one of 2*rows rows): (r / group) * 2 * group + offset + r % group.
+// `group` is a power of two (the launchers refuse others).
+MOE_DEV int64_t interleaved_row(int64_t r, int group, int offset) {
+  if (group <= 0) return r;
+  const int sh = __ffs(group) - 1;
+  return ((r >> sh) << (sh + 1)) + offset + (r & (group - 1));
+}
 __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     const uint4* __restrict__ src, int64_t nblocks, int rows, int cols, int group, int offset,
     uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
@@ -35,7 +41,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
   const int64_t r = rem / kb;
   const int b = (int)(rem - r * kb);
   const int64_t out_rows = group > 0 ? 2 * (int64_t)rows : rows;
-  const int64_t ro = group > 0 ? (r / group) * 2 * group + offset + r % group : r;
+  const int64_t ro = interleaved_row(r, group, offset);
   float v[32];
 #pragma unroll
   for (int u = 0; u < 4; ++u) unpack8(__ldg(src + i * 4 + u), v + 8 * u);
@@ -43,7 +49,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
 #pragma unroll
   for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
   const int s = mx_scale_exp(amax);
-  const float inv = ldexpf(1.0f, -s);
+  const float inv = exp2i(-s);
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] *= inv;
   uint2* out = reinterpret_cast<uint2*>(q + ((size_t)mat * out_rows + ro) * cols + (size_t)b * 32);
@@ -83,7 +89,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_cols_kernel(
     amax = fmaxf(amax, fabsf(v[j]));
   }
   const int e = mx_scale_exp(amax);
-  const float inv = ldexpf(1.0f, -e);
+  const float inv = exp2i(-e);
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] *= inv;
   const size_t row_out = (size_t)n0 + n;
@@ -137,11 +143,11 @@ __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int sx = mx_scale_exp(amax);
-    const float inv = ldexpf(1.0f, -sx);
+    const float inv = exp2i(-sx);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= inv;
     const int64_t r = k0 + row;
-    const int64_t ro = group > 0 ? (r / group) * 2 * group + offset + r % group : r;
+    const int64_t ro = interleaved_row(r, group, offset);
     *reinterpret_cast<uint2*>(q_r + ((size_t)mat * out_rows + ro) * C + n0 + col) = e4m3x8(v);
     if ((idx & 3) == 0)
       s_r[(size_t)mat * out_rows * cb + sf_offset(ro, (n0 + col) / 32, cb)] = (uint8_t)(sx + 127);
@@ -161,7 +167,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
       amax = fmaxf(amax, fabsf(v[j]));
     }
     const int e = mx_scale_exp(amax);
-    const float inv = ldexpf(1.0f, -e);
+    const float inv = exp2i(-e);
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= inv;
     s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)n0 + n, (k0 / 32) + kb, R / 32)] =
@@ -237,14 +243,14 @@ __global__ void __launch_bounds__(kQThreads) dispatch_mxfp8_kernel(
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int s = mx_scale_exp(amax);
-    const float inv = ldexpf(1.0f, -s);
+    const float inv = exp2i(-s);
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] *= inv;
     const uint2 codes = e4m3x8(v);
     // dequantised copy (the dequantiser's arithmetic: code value x 2^s, bf16)
     uint4 dq = make_uint4(0, 0, 0, 0);
     if (xdq != nullptr) {
-      const float sc = ldexpf(1.0f, s);
+      const float sc = exp2i(s);
       float f[8];
       e4m3x2_to_f32(codes.x & 0xFFFFu, f[0], f[1]);
       e4m3x2_to_f32(codes.x >> 16, f[2], f[3]);
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kQThreads) dequantize_kernel(
   const int64_t r = i / per_row;
   const int c16 = (int)(i - r * per_row);
   const int b = c16 / 2;
-  const float scale = ldexpf(1.0f, (int)sf[sf_offset(r, b, K / 32)] - 127);
+  const float scale = exp2i((int)sf[sf_offset(r, b, K / 32)] - 127);
   const uint4 v = __ldg(q + i);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   float f[16];
@@ -295,6 +301,7 @@ __global__ void __launch_bounds__(kQThreads) dequantize_kernel(
 
 cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis, const void* src,
                                   uint8_t* q, uint8_t* sf, cudaStream_t s, int group, int offset) {
+  if (group < 0 || (group & (group - 1)) != 0) return cudaErrorInvalidValue;
   if (block_axis == 1) {
     const int64_t n = (int64_t)batch * rows * (cols / 32);
     launch_pdl(quantize_rows_kernel, dim3((unsigned)((n + kQThreads - 1) / kQThreads)), dim3(kQThreads), 0, s, 
@@ -310,6 +317,7 @@ cudaError_t launch_quantize_mxfp8(int batch, int rows, int cols, int block_axis,
 cudaError_t launch_quantize_mxfp8_both(int batch, int rows, int cols, const void* src, int group,
                                        int offset, uint8_t* q_rows, uint8_t* sf_rows,
                                        uint8_t* q_cols, uint8_t* sf_cols, cudaStream_t s) {
+  if (group < 0 || (group & (group - 1)) != 0) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(cols / kBC), (unsigned)(rows / kBR), (unsigned)batch);
   launch_pdl(quantize_both_kernel, grid, dim3(kQThreads), 0, s,
              static_cast<const __nv_bfloat16*>(src), rows, cols, group, offset, q_rows, sf_rows,
