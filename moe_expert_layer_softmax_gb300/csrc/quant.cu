@@ -103,19 +103,20 @@ __global__ void __launch_bounds__(kQThreads) quantize_cols_kernel(
 // Both orientations of a weight from one read: src [R, C] bf16 per matrix ->
 // (1) q_r [R, C] blocked along C (rows interleaved by `group`/`offset` as in
 // quantize_rows_kernel) and (2) q_c [C, R] blocked along R (the transpose, as
-// in quantize_cols_kernel).  Tile: 128 rows x 128 columns (32 KB), eight
-// 16-byte loads in flight per thread.  For (1) a thread holds 8 values of a
-// row, 4 neighbouring lanes form one 32-value block and 16 lanes store one
-// whole 128-byte row of codes.  For (2) a thread quantises two 32-row blocks of
-// one column; the 128 x 128 transposed codes are staged in the tile's memory
-// and stored as whole 128-byte rows.
+// in quantize_cols_kernel).  Tile: 128 rows x 128 columns (32 KB) staged in
+// shared memory from eight 16-byte loads in flight per thread, 16-byte chunk c
+// of row r at chunk c ^ (r % 16), which keeps the row reads of (1) and the
+// column reads of (2) free of bank conflicts.  (1): a thread quantises two
+// 32-value blocks of one row.  (2): a thread quantises one 32-row block of two
+// adjacent columns (32-bit reads).  Both code sets are then staged in the
+// tile's memory (16 KB each) and stored as whole 128-byte rows.
 constexpr int kBR = 128, kBC = 128;
-__global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
+__global__ void __launch_bounds__(kQThreads, 4) quantize_both_kernel(
     const __nv_bfloat16* __restrict__ src, int R, int C, int group, int offset,
     uint8_t* __restrict__ q_r, uint8_t* __restrict__ s_r, uint8_t* __restrict__ q_c,
     uint8_t* __restrict__ s_c) {
   pdl_begin();
-  __shared__ __align__(16) __nv_bfloat16 tile[kBR][kBC];
+  __shared__ __align__(16) uint8_t tile[kBR * kBC * 2];
   const int mat = blockIdx.z;
   const int k0 = blockIdx.y * kBR;
   const int n0 = blockIdx.x * kBC;
@@ -133,69 +134,113 @@ __global__ void __launch_bounds__(kQThreads) quantize_both_kernel(
 #pragma unroll
   for (int u = 0; u < kLoads; ++u) {
     const int idx = threadIdx.x + u * kQThreads;
-    const int row = idx >> 4, col = (idx & 15) * 8;
-    *reinterpret_cast<uint4*>(&tile[row][col]) = raw[u];
-    float v[8];
-    unpack8(raw[u], v);
+    const int row = idx >> 4, c = idx & 15;
+    *reinterpret_cast<uint4*>(tile + row * 256 + ((c ^ (row & 15)) << 4)) = raw[u];
+  }
+  __syncthreads();
+  // (1) row `rr`, 32-value blocks b0 and b0 + 1 of the tile's four
+  const int rr = threadIdx.x >> 1;
+  const int b0 = 2 * (threadIdx.x & 1);
+  uint4 rcode[4];
+  uint32_t rsb = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int b = b0 + h;
+    uint32_t pk[16];   // the block's 32 bf16 values, two per word (unpacked at use)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 c4 =
+          *reinterpret_cast<const uint4*>(tile + rr * 256 + (((4 * b + u) ^ (rr & 15)) << 4));
+      pk[4 * u] = c4.x; pk[4 * u + 1] = c4.y; pk[4 * u + 2] = c4.z; pk[4 * u + 3] = c4.w;
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    for (int j = 0; j < 16; ++j)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(pk[j] << 16)),
+                               fabsf(__uint_as_float(pk[j] & 0xFFFF0000u))));
     const int sx = mx_scale_exp(amax);
     const float inv = exp2i(-sx);
+    uint2 q[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] *= inv;
-    const int64_t r = k0 + row;
-    const int64_t ro = interleaved_row(r, group, offset);
-    *reinterpret_cast<uint2*>(q_r + ((size_t)mat * out_rows + ro) * C + n0 + col) = e4m3x8(v);
-    if ((idx & 3) == 0)
-      s_r[(size_t)mat * out_rows * cb + sf_offset(ro, (n0 + col) / 32, cb)] = (uint8_t)(sx + 127);
+    for (int g = 0; g < 4; ++g) {
+      float t[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        t[2 * i] = __uint_as_float(pk[4 * g + i] << 16) * inv;
+        t[2 * i + 1] = __uint_as_float(pk[4 * g + i] & 0xFFFF0000u) * inv;
+      }
+      q[g] = e4m3x8(t);
+    }
+    rcode[2 * h] = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+    rcode[2 * h + 1] = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
+    rsb |= (uint32_t)(sx + 127) << (8 * h);
   }
-  __syncthreads();
-  // the transpose, blocked along R: column n, row blocks kb and kb + 2
-  const int n = threadIdx.x & 127;
-  uint2 codes[2][4];
+  {   // blocks b0 and b0 + 1 (b0 even): adjacent scale bytes
+    const int64_t ro = interleaved_row(k0 + rr, group, offset);
+    *reinterpret_cast<uint16_t*>(s_r + (size_t)mat * out_rows * cb +
+                                 sf_offset(ro, n0 / 32 + b0, cb)) = (uint16_t)rsb;
+  }
+  // (2) columns 2 cp and 2 cp + 1, rows 32 kb .. 32 kb + 31
+  const int cpair = threadIdx.x & 63;
+  const int kb = threadIdx.x >> 6;
+  uint32_t w[32];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int kb = (threadIdx.x >> 7) + 2 * h;
-    float v[32];
+  for (int j = 0; j < 32; ++j) {
+    const int r = 32 * kb + j;
+    w[j] = *reinterpret_cast<const uint32_t*>(tile + r * 256 + (((cpair >> 2) ^ (r & 15)) << 4) +
+                                              4 * (cpair & 3));
+  }
+  uint4 ccode[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {   // column 2 cpair + i: the low (i = 0) or high bf16 halves
+    auto val = [&](int j) {
+      return __uint_as_float(i ? (w[j] & 0xFFFF0000u) : (w[j] << 16));
+    };
     float amax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = __bfloat162float(tile[kb * 32 + j][n]);
-      amax = fmaxf(amax, fabsf(v[j]));
-    }
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(val(j)));
     const int e = mx_scale_exp(amax);
     const float inv = exp2i(-e);
+    uint2 q[4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= inv;
-    s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)n0 + n, (k0 / 32) + kb, R / 32)] =
+    for (int g = 0; g < 4; ++g) {
+      float t[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t[j] = val(8 * g + j) * inv;
+      q[g] = e4m3x8(t);
+    }
+    ccode[2 * i] = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+    ccode[2 * i + 1] = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
+    s_c[(size_t)mat * C * (R / 32) + sf_offset((int64_t)n0 + 2 * cpair + i, (k0 / 32) + kb, R / 32)] =
         (uint8_t)(e + 127);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) codes[h][u] = e4m3x8(v + 8 * u);
   }
-  // Stage the 128 x 128 codes of the transposed tile in the (now free) tile
-  // memory, 8-byte chunk q of row n at chunk q ^ (n & 15) (conflict-free for
-  // the column-wise writes), then store whole 128-byte rows: 8 lanes per row,
-  // 16 bytes each.
+  // Stage both code sets in the tile's memory once every read of it is done:
+  // q_r codes of tile row r in bytes [0, 16 KB), 16-byte chunk c at c ^ (r % 8);
+  // q_c codes of output row n in [16 KB, 32 KB), chunk c at c ^ ((n / 2) % 8).
   __syncthreads();
-  uint2* st = reinterpret_cast<uint2*>(&tile[0][0]);   // 128 rows x 16 chunks
+  uint8_t* st_r = tile;
+  uint8_t* st_c = tile + kBR * kBC;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int kb = (threadIdx.x >> 7) + 2 * h;
+  for (int q = 0; q < 4; ++q)   // chunks 2 b0 .. 2 b0 + 3 of row rr
+    *reinterpret_cast<uint4*>(st_r + rr * 128 + (((2 * b0 + q) ^ (rr & 7)) << 4)) = rcode[q];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) st[n * 16 + ((kb * 4 + u) ^ (n & 15))] = codes[h][u];
+  for (int i = 0; i < 2; ++i) {
+    const int n = 2 * cpair + i;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)   // chunks 2 kb, 2 kb + 1 of output row n
+      *reinterpret_cast<uint4*>(st_c + n * 128 + (((2 * kb + q) ^ ((n >> 1) & 7)) << 4)) =
+          ccode[2 * i + q];
   }
   __syncthreads();
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    const int idx = threadIdx.x + u * kQThreads;   // 1024 16-byte pieces
+    const int idx = threadIdx.x + u * kQThreads;   // 1024 16-byte pieces per code set
     const int rn = idx >> 3, c = idx & 7;
-    const uint2 lo = st[rn * 16 + ((2 * c) ^ (rn & 15))];
-    const uint2 hi = st[rn * 16 + ((2 * c + 1) ^ (rn & 15))];
+    const int64_t ro = interleaved_row(k0 + rn, group, offset);
+    *reinterpret_cast<uint4*>(q_r + ((size_t)mat * out_rows + ro) * C + n0 + 16 * c) =
+        *reinterpret_cast<const uint4*>(st_r + rn * 128 + ((c ^ (rn & 7)) << 4));
     *reinterpret_cast<uint4*>(q_c + (size_t)mat * C * R + ((size_t)n0 + rn) * R + k0 + 16 * c) =
-        make_uint4(lo.x, lo.y, hi.x, hi.y);
+        *reinterpret_cast<const uint4*>(st_c + rn * 128 + ((c ^ ((rn >> 1) & 7)) << 4));
   }
 }
 
