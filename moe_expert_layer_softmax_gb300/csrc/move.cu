@@ -367,6 +367,75 @@ __global__ void __launch_bounds__(kMoveThreads, KM <= 4 ? 4 : (KM <= 8 ? 3 : 1))
   }
 }
 
+// k > 8 (up to 32 routes per token): the route's slot, expert and dlogit come
+// from the lane that holds them, and the rows are loaded 8 routes at a time
+// (8 16-byte loads in flight per lane); same sums, in route order, as above.
+__global__ void __launch_bounds__(kMoveThreads) dispatch_bwd_wide_kernel(
+    const uint4* __restrict__ dxd, const int32_t* __restrict__ slot_of_route,
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ dlogits,
+    const uint4* __restrict__ w_router, int T, int d, int E, int k, uint4* __restrict__ dx) {
+  pdl_begin();
+  constexpr int G = 8;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int nv = d / kVec;
+  const int my_slot = (lane < k) ? slot_of_route[(size_t)t * k + lane] : 0;
+  const int my_id = (lane < k) ? topk_idx[(size_t)t * k + lane] : 0;
+  const float my_dl =
+      (lane < k && w_router != nullptr) ? dlogits[(size_t)t * E + my_id] : 0.0f;
+  for (int c0 = 0; c0 < nv; c0 += 32) {     // warp-uniform
+    const int c = c0 + lane;
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += G) {
+      uint4 v[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int j = j0 + g;
+        const int sj = __shfl_sync(0xffffffffu, my_slot, j < k ? j : 0);
+        v[g] = make_uint4(0, 0, 0, 0);
+        if (j < k && c < nv)
+          MOE_CHECKED(sj, rows_max_of(T, k, E)) v[g] = __ldg(dxd + (size_t)sj * nv + c);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (j0 + g < k) {
+          float f[kVec];
+          unpack8(v[g], f);
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) acc[i] += f[i];
+        }
+      }
+    }
+    if (w_router != nullptr) {
+      for (int j0 = 0; j0 < k; j0 += G) {
+        uint4 w[G];
+        float dlj[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int j = j0 + g;
+          const int ij = __shfl_sync(0xffffffffu, my_id, j < k ? j : 0);
+          dlj[g] = __shfl_sync(0xffffffffu, my_dl, j < k ? j : 0);
+          w[g] = make_uint4(0, 0, 0, 0);
+          if (j < k && c < nv) MOE_CHECKED(ij, E) w[g] = __ldg(w_router + (size_t)ij * nv + c);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          if (j0 + g < k) {
+            float f[kVec];
+            unpack8(w[g], f);
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) acc[i] = fmaf(dlj[g], f[i], acc[i]);
+          }
+        }
+      }
+    }
+    if (c < nv) dx[(size_t)t * nv + c] = pack8(acc);
+  }
+}
+
 // Pass 1: partial[m][col] = sum over the real rows s of tile m of
 // dlogits[t(s), e(m)] * x[t(s)][col], for a 1024-column chunk: 128 column
 // threads x 8 columns, and four row groups (rows g, g + 4, g + 8, ...) whose
@@ -533,7 +602,7 @@ cudaError_t launch_dispatch_bwd(const void* dxd, const int32_t* slot_of_route,
         static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
         static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
   else
-    launch_pdl(dispatch_bwd_kernel<32>, dim3(tb), dim3(kMoveThreads), 0, s, 
+    launch_pdl(dispatch_bwd_wide_kernel, dim3(tb), dim3(kMoveThreads), 0, s,
         static_cast<const uint4*>(dxd), slot_of_route, topk_idx, dlogits,
         static_cast<const uint4*>(w_router), T, d, E, k, static_cast<uint4*>(dx));
   return cudaGetLastError();

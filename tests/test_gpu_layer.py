@@ -60,7 +60,7 @@ SMALL = [(256, 128, 8, 2, 256), (300, 256, 6, 2, 384), (1000, 512, 16, 4, 256), 
          (1, 128, 4, 2, 128),
          # k in 5..8 and k > 8 take the wider gather kernels; 256 experts and
          # top-32 are the envelope's maxima; T = 513 is not a multiple of the
-         # 16-token routing block
+         # 128-token routing block
          (513, 256, 64, 8, 256), (200, 128, 256, 32, 128), (129, 128, 3, 3, 128)]
 
 
