@@ -53,7 +53,9 @@ def check_routing(g, logits32, k):
 
 
 @pytest.mark.parametrize("T,E,k", [(256, 8, 2), (1000, 32, 4), (777, 128, 4), (3000, 64, 8),
-                                   (50, 256, 32), (300, 1, 1), (100, 8, 8), (1, 16, 3), (65, 40, 5)])
+                                   (50, 256, 32), (300, 1, 1), (100, 8, 8), (1, 16, 3), (65, 40, 5),
+                                   # E not a multiple of 4 over many 128-token blocks
+                                   (20000, 7, 3), (5000, 250, 8)])
 def test_random_logits(moe_gpu, T, E, k):
     m, dev = moe_gpu
     rng = np.random.default_rng(T * 7 + E)
