@@ -98,3 +98,60 @@ def test_stalled_natural_wgrad_times_out_and_context_survives(moe_gpu):
     m.grouped_gemm(s, m.GEMM_WGRAD2, ws, tile_offsets=to, a0=dY, a1=Adq, out0=ref)
     assert m.read_error(ws) == 0
     assert torch.equal(dW, ref)
+
+
+def test_stalled_mxfp8_pair_gemm_times_out_and_context_survives(moe_gpu):
+    """The same hook on the MXFP8 CTA-pair GEMM in its SwiGLU-backward form,
+    where two mover threads per CTA also wait on mbarriers (for dH/dU written by
+    the epilogue): every role gives up within its bound, the kernel reports the
+    timeout, and the next launch equals a clean launch made before, bit for bit."""
+    m, dev = moe_gpu
+    T, d, E, k, f = 300, 256, 4, 2, 256
+    rng = np.random.default_rng(79)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts = O.expert_counts(idx, E)
+    tile_offsets, row_offsets = O.tile_layout(counts, 128)
+    s = m.shape(T, d, E, k, f, prec=m.MXFP8)
+    n = m.rows_max(s)
+    used = int(row_offsets[-1])
+    ws = torch.zeros(m.workspace_size(s), dtype=torch.uint8, device=dev)
+    bf = lambda *sh: torch.from_numpy(rng.standard_normal(sh).astype(np.float32)).to(dev).to(torch.bfloat16)
+    dY = torch.zeros(n, d, dtype=torch.bfloat16, device=dev)
+    dY[:used] = bf(used, d)
+    H, U = bf(n, f), bf(n, f)
+    dYq = torch.empty(n, d, dtype=torch.uint8, device=dev)
+    dYs = torch.empty(n * d // 32, dtype=torch.uint8, device=dev)
+    m.quantize_mxfp8(1, n, d, 1, dY, dYq, dYs)
+    buf = m.allocate(s, with_grads=False)
+    w = buf.mx_weights
+    m.build_mx_weights(s, 0.02 * bf(E, f, d), 0.02 * bf(E, f, d), 0.02 * bf(E, d, f), w)
+    to = torch.from_numpy(tile_offsets.astype(np.int32)).to(dev)
+
+    def run():
+        o = dict(out0=torch.zeros(n, f, dtype=torch.bfloat16, device=dev),
+                 out1=torch.zeros(n, f, dtype=torch.bfloat16, device=dev),
+                 out2=torch.zeros(n, f, dtype=torch.uint8, device=dev),
+                 out3=torch.zeros(n, f, dtype=torch.uint8, device=dev),
+                 osf0=torch.zeros(n * f // 32, dtype=torch.uint8, device=dev),
+                 osf1=torch.zeros(n * f // 32, dtype=torch.uint8, device=dev))
+        m.grouped_gemm(s, m.GEMM_DGRAD2_SWIGLU, ws, tile_offsets=to, a0=dYq, sfa0=dYs,
+                       w0=w["downT_q"], sfb0=w["downT_s"], aux0=H, aux1=U, **o)
+        return o
+
+    m.clear_error(ws)
+    clean = run()
+    assert m.read_error(ws) == 0
+    prev = m.debug_inject_stall(1)
+    try:
+        m.clear_error(ws)
+        run()
+        err = m.read_error(ws)
+    finally:
+        m.debug_inject_stall(prev)
+    assert err & m.DEVERR_TIMEOUT
+    m.clear_error(ws)
+    again = run()
+    assert m.read_error(ws) == 0
+    for key in clean:
+        assert torch.equal(clean[key][:used] if clean[key].dim() == 2 else clean[key],
+                           again[key][:used] if again[key].dim() == 2 else again[key]), key
