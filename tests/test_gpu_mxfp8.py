@@ -130,8 +130,10 @@ def test_dequantize_is_exact(moe_gpu):
 
 # ------------------------------------------------------------------ stages
 # f = 384: DGRAD2 (N = f) on the single-CTA MXFP8 kernel; d = 384: FWD2 and
-# DGRAD1 (N = d) there; the other GEMMs on CTA pairs
-SHAPES = [(300, 256, 6, 2, 256), (1000, 512, 8, 8, 384), (200, 384, 4, 2, 256)]
+# DGRAD1 (N = d) there; the other GEMMs on CTA pairs; top-12 takes the k > 8
+# gathers (the combine backward's fused dY quantisation included)
+SHAPES = [(300, 256, 6, 2, 256), (1000, 512, 8, 8, 384), (200, 384, 4, 2, 256),
+          (160, 256, 16, 12, 256)]
 
 
 @pytest.fixture(scope="module", params=SHAPES, ids=lambda v: "x".join(map(str, v)))
