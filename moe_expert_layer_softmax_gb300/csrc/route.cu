@@ -149,6 +149,139 @@ __global__ void __launch_bounds__(kTpb) route_topk_reg_kernel(
   write_block_hist(s_mask, E, block_hist, tl, kTpb);
 }
 
+// (a2) 32 < E <= 2 EH, k <= 8: two threads per token (the two lanes of a pair
+// in one warp): lane h ranks experts [h EH, (h + 1) EH) in registers (k passes
+// of argmax, the lower id first on ties), and both lanes merge the two sorted
+// lists through shuffles of their heads - lane 0's head goes first unless lane
+// 1's key is strictly larger, since lane 0 holds the lower ids - so that both
+// hold the same k experts in the order of (a).  Twice the threads of (a) for
+// the same tokens: the selection is latency-bound at one thread per token.
+constexpr int kTopk2Threads = 2 * kTpb;
+template <int EH, int KM>
+__global__ void __launch_bounds__(kTopk2Threads) route_topk2_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gates, int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
+    int32_t* __restrict__ err) {
+  pdl_begin();
+  __shared__ uint32_t s_mask[4 * 2 * EH];
+  const int tid = threadIdx.x;
+  const int tl = tid >> 1;              // token of the block
+  const int h = tid & 1;                // which half of the experts
+  const int64_t t = (int64_t)blockIdx.x * kTpb + tl;
+  const bool valid = t < T;
+  for (int i = tid; i < 4 * E; i += kTopk2Threads) s_mask[i] = 0u;
+  const int c0 = h * EH;
+  float v[EH];
+  bool bad = false;
+#pragma unroll
+  for (int c = 0; c < EH; ++c) v[c] = -CUDART_INF_F;   // columns >= E are never chosen (k <= E)
+  if (valid) {
+    const float* row = logits + t * E + c0;
+    if ((E & 3) == 0) {
+#pragma unroll
+      for (int c = 0; c < EH; c += 4) {
+        if (c0 + c < E) {
+          const float4 q = __ldg(reinterpret_cast<const float4*>(row + c));
+          v[c] = q.x; v[c + 1] = q.y; v[c + 2] = q.z; v[c + 3] = q.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < EH; ++c)
+        if (c0 + c < E) v[c] = __ldg(row + c);
+    }
+#pragma unroll
+    for (int c = 0; c < EH; ++c) {
+      bad = bad || !isfinite(v[c]) && c0 + c < E;
+      v[c] = route_key(v[c]);
+    }
+  }
+  bad = bad || __shfl_xor_sync(0xffffffffu, bad ? 1 : 0, 1) != 0;
+  // this lane's k largest, in order
+  uint32_t taken[EH / 32];
+#pragma unroll
+  for (int w = 0; w < EH / 32; ++w) taken[w] = 0u;
+  float lk[KM];
+  int li[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    lk[j] = -CUDART_INF_F;
+    li[j] = c0;
+    if (j < k) {
+      float best = 0.0f;
+      int bi = -1;
+#pragma unroll
+      for (int c = 0; c < EH; ++c) {
+        const bool free = ((taken[c >> 5] >> (c & 31)) & 1u) == 0u;
+        if (free && (bi < 0 || v[c] > best)) {   // strict: the lower id keeps a tie
+          best = v[c];
+          bi = c;
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < EH / 32; ++w)
+        if ((bi >> 5) == w) taken[w] |= 1u << (bi & 31);
+      lk[j] = best;
+      li[j] = c0 + bi;
+    }
+  }
+  // merge: both lanes step through the two lists in the same way
+  const int lane = tid & 31;
+  int sel[KM];
+  float ex[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ex[j] = 0.0f;
+  float lmax = 0.0f;
+  int pa = 0, pb = 0;
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    sel[j] = 0;
+    if (j < k) {
+      const int pm = h ? pb : pa;          // this lane's next entry (< k: 2k entries, k taken)
+      float hk = lk[0];
+      int hi = li[0];
+#pragma unroll
+      for (int q = 1; q < KM; ++q)
+        if (q == pm) { hk = lk[q]; hi = li[q]; }
+      const float ak = __shfl_sync(0xffffffffu, hk, lane & ~1);
+      const int ai = __shfl_sync(0xffffffffu, hi, lane & ~1);
+      const float bk = __shfl_sync(0xffffffffu, hk, lane | 1);
+      const int bidx = __shfl_sync(0xffffffffu, hi, lane | 1);
+      const bool take_b = bk > ak;
+      const float best = take_b ? bk : ak;
+      sel[j] = take_b ? bidx : ai;
+      pa += take_b ? 0 : 1;
+      pb += take_b ? 1 : 0;
+      if (j == 0) lmax = best;
+      ex[j] = expf(best - lmax);
+    }
+  }
+  if (valid && h == 0) {
+    const float sum = gate_sum8(ex);
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
+        topk_idx[t * k + j] = sel[j];
+        gates[t * k + j] = bad ? 0.0f : ex[j] / sum;
+      }
+    }
+    if (bad) raise_error(err, MOE_DEVERR_NONFINITE_LOGIT);
+  }
+  __syncthreads();   // masks cleared
+  if (valid && h == 0) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) atomicOr(&s_mask[4 * sel[j] + (tl >> 5)], 1u << (tl & 31));
+  }
+  __syncthreads();
+  if (valid && h == 0) {
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) local_rank[t * k + j] = mask_rank(s_mask, sel[j], tl);
+  }
+  write_block_hist(s_mask, E, block_hist, tid, kTopk2Threads);
+}
+
 // (b) E > 128, k <= 8: four threads per token; thread q keeps the k largest of
 // columns [q cw, (q + 1) cw) while it reads them, and the four lists are merged
 // through lane shuffles in the same total order.
@@ -455,13 +588,17 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 #define MOE_TOPK_REG(EM, KM)                                                                   \
   launch_pdl(route_topk_reg_kernel<EM, KM>, dim3(nb), dim3(kTpb), 0, s, logits, T, E, k,     \
              topk_idx, gates, local_rank, block_hist, err)
+#define MOE_TOPK2(EH, KM)                                                                      \
+  launch_pdl(route_topk2_kernel<EH, KM>, dim3(nb), dim3(kTopk2Threads), 0, s, logits, T, E, k, \
+             topk_idx, gates, local_rank, block_hist, err)
     if (E <= 32) {
       if (k <= 4) MOE_TOPK_REG(32, 4); else MOE_TOPK_REG(32, 8);
     } else if (E <= 64) {
-      if (k <= 4) MOE_TOPK_REG(64, 4); else MOE_TOPK_REG(64, 8);
+      if (k <= 4) MOE_TOPK2(32, 4); else MOE_TOPK2(32, 8);
     } else {
-      if (k <= 4) MOE_TOPK_REG(128, 4); else MOE_TOPK_REG(128, 8);
+      if (k <= 4) MOE_TOPK2(64, 4); else MOE_TOPK2(64, 8);
     }
+#undef MOE_TOPK2
 #undef MOE_TOPK_REG
     return cudaGetLastError();
   }
