@@ -100,7 +100,8 @@ struct __align__(8) Ctl {
   uint32_t tmem_base;
   int abort;
   int32_t tile_off[kMaxE + 1];
-  int32_t pair_off[kMaxE + 1];   // CTA pairs: exclusive scan of ceil(m-tiles / 2) per expert
+  int32_t pair_off[kMaxE + 1];   // CTA pairs, M-grouped: exclusive scan of ceil(m-tiles / 2)
+                                 // per expert; K-grouped: the experts in tile order
 };
 
 // the dynamic shared memory is declared 1024-byte aligned (the swizzled tiles
@@ -379,19 +380,38 @@ MOE_DEV void mma_issuer(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_ba
 // Tile `t` of the pair schedule, seen from CTA `rank`.  M-grouped: the pair
 // covers m-tiles (2j, 2j + 1) of one expert; when the expert has an odd number
 // of m-tiles the odd CTA of its last pair reloads the even CTA's rows and
-// stores nothing (`valid` false).  K-grouped: m-tiles (2i, 2i + 1).
+// stores nothing (`valid` false).  K-grouped: m-tiles (2i, 2i + 1), the experts
+// taken in the order kgroup_order sets up.
 MOE_DEV int total_tiles_pair(const Params& p, const Ctl& s) {
   if (p.mode == MODE_MGROUP) return s.pair_off[p.E] * p.n_tiles;
   return p.E * (p.m_tiles / 2) * p.n_tiles;
 }
+// Every pair takes one tile of each round of nclusters tiles.  With experts of
+// more than twice the mean rows (long tiles), odd rounds run backwards, so the
+// pair that got the first (longest) tile of one round gets the last of the next;
+// otherwise (pair_off[E] == 0) every round runs forwards.
+MOE_DEV int kgroup_snake(const Params& p, const Ctl& s, int t) {
+  const int np = (int)gridDim.x / 2;
+  const int round = t / np;
+  if (!(round & 1)) return t;
+  const int n_r = min(np, total_tiles_pair(p, s) - round * np);
+  return round * np + (n_r - 1 - (t - round * np));
+}
+
+// KG: the kernel runs K-grouped schedules only, else M-grouped ones only (each
+// kernel is compiled for one of the two, with no code of the other).
+template <bool KG>
 MOE_DEV TileInfo decode_pair(const Params& p, const Ctl& s, int t, int rank, bool& valid) {
   TileInfo ti;
   valid = true;
   ti.kb = 0;
-  if (p.mode == MODE_KGROUP) {
+  if constexpr (KG) {
+    const bool skew = s.pair_off[p.E] > 0;
+    if (skew) t = kgroup_snake(p, s, t);
     const int per = (p.m_tiles / 2) * p.n_tiles;
-    ti.e = t / per;
-    const int r = t - ti.e * per;
+    const int g = t / per;              // the g-th expert of kgroup_order's order
+    ti.e = skew ? s.pair_off[g] : g;
+    const int r = t - g * per;
     const int pm = r / p.n_tiles;
     ti.n_tile = r - pm * p.n_tiles;
     ti.m_tile = 2 * pm + rank;
@@ -473,7 +493,7 @@ MOE_DEV void drain_stages(uint64_t* bars, long issued, int stages) {
   }
 }
 
-template <bool DQB>
+template <bool DQB, bool KG>
 MOE_DEV void producer_pair(const Params& p, Ctl& s, uint8_t* ring, int rank,
                            const CUtensorMap* tA0, const CUtensorMap* tA1, const CUtensorMap* tB0,
                            const CUtensorMap* tB1) {
@@ -487,7 +507,7 @@ MOE_DEV void producer_pair(const Params& p, Ctl& s, uint8_t* ring, int rank,
   bool ok = true;
   for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters) {
     bool valid;
-    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    const TileInfo ti = decode_pair<KG>(p, s, t, rank, valid);
     for (int ks = 0; ks < ti.ks; ++ks) {
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
       if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)p.pair_half_bytes);
@@ -512,7 +532,7 @@ MOE_DEV void producer_pair(const Params& p, Ctl& s, uint8_t* ring, int rank,
   }
 }
 
-template <bool DQB>
+template <bool DQB, bool KG>
 MOE_DEV void mma_issuer_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tmem_base, int rank) {
   if (rank == 0) {
     uint8_t* slots = ring + p.stages * p.stage_bytes;   // DQB: the converted B tiles
@@ -528,7 +548,7 @@ MOE_DEV void mma_issuer_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t tm
     bool ok = true;
     for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters, ++it) {
       bool valid;
-      const TileInfo ti = decode_pair(p, s, t, 0, valid);
+      const TileInfo ti = decode_pair<KG>(p, s, t, 0, valid);
       const int acc = it % p.num_acc;
       const uint32_t use = (uint32_t)(it / p.num_acc);
       if (!mbar_wait(&s.tempty[acc], (use & 1u) ^ 1u, &s.abort, p.err)) { ok = false; break; }
@@ -687,7 +707,7 @@ MOE_DEV void converter_pair(const Params& p, Ctl& s, uint8_t* ring, int ctid, in
   uint32_t phase = 0, sphase = 0;
   for (int t = (int)blockIdx.x / 2; t < nt; t += nclusters) {
     bool valid;
-    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    const TileInfo ti = decode_pair<true>(p, s, t, rank, valid);
     for (int ks = 0; ks < ti.ks; ++ks) {
       bool ok = mbar_wait(&s.rawfull[stage], phase, &s.abort, p.err);
       ok = ok && mbar_wait(&s.bempty[slot], sphase ^ 1u, &s.abort, p.err);
@@ -985,7 +1005,7 @@ MOE_DEV void epilogue_tile_tma(const Params& p, const TileInfo& ti, uint32_t tb,
   }
 }
 
-template <bool MX, bool PAIR, bool DQB>
+template <bool MX, bool PAIR, bool DQB, bool KG>
 MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int lane,
                       uint8_t* stage_out, const CUtensorMap* tO0, const CUtensorMap* tO1,
                       const CUtensorMap* tO2, int rank) {
@@ -1015,7 +1035,7 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   int it = 0;
   for (int t = t_first; t < nt; t += t_step, ++it) {
     bool valid = true;
-    const TileInfo ti = PAIR ? decode_pair(p, s, t, rank, valid) : decode_tile(p, s.tile_off, t);
+    const TileInfo ti = PAIR ? decode_pair<KG>(p, s, t, rank, valid) : decode_tile(p, s.tile_off, t);
     const int acc = it % p.num_acc;
     const uint32_t use = (uint32_t)(it / p.num_acc);
     bool ok = mbar_wait(&s.tfull[acc], use & 1u, &s.abort, p.err);
@@ -1041,7 +1061,41 @@ MOE_DEV void epilogue(const Params& p, Ctl& s, uint32_t tmem_base, int warp, int
   if (st.leader) bulk_wait_all();   // stores complete before the CTA exits
 }
 
-template <bool MX, bool PAIR, bool DQB = false>
+// K-grouped pair tiles: the number of long experts (pair_off[E]) and, if there
+// are any, the expert order of the schedule (pair_off[0..E-1]; else id order);
+// every thread of the CTA calls it
+__device__ __noinline__ void kgroup_order(const Params& p, Ctl& s) {
+  // weight gradients: a tile's main loop runs over its expert's rows.  The
+  // experts with more than twice the mean rows go first, most rows first (the
+  // lower id on ties), so that no long tile starts last; the others keep their
+  // id order, which mixes short store-bound tiles with longer ones.
+  // pair_off[E] keeps the number of such experts.
+  const int total = s.tile_off[p.E] - s.tile_off[0];
+  int mine = 0;
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x)
+    mine += ((s.tile_off[e + 1] - s.tile_off[e]) * p.E > 2 * total) ? 1 : 0;
+  static_assert(kMaxE <= kThreads, "one expert per thread at most");
+  const int nh = __syncthreads_count(mine);
+  for (int e = threadIdx.x; e < p.E && nh > 0; e += blockDim.x) {
+    const int ke = s.tile_off[e + 1] - s.tile_off[e];
+    const bool heavy_e = ke * p.E > 2 * total;
+    int g = 0;
+    for (int o = 0; o < p.E; ++o) {
+      const int ko = s.tile_off[o + 1] - s.tile_off[o];
+      const bool heavy_o = ko * p.E > 2 * total;
+      if (heavy_e)
+        g += (heavy_o && (ko > ke || (ko == ke && o < e))) ? 1 : 0;
+      else
+        g += (!heavy_o && o < e) ? 1 : 0;
+    }
+    s.pair_off[heavy_e ? g : nh + g] = e;
+  }
+  if (threadIdx.x == 0) s.pair_off[p.E] = nh;
+}
+
+// KG (CTA pairs): compiled for K-grouped schedules (weight gradients) only, else
+// for M-grouped ones only; the dequantising kernel (DQB) is K-grouped.
+template <bool MX, bool PAIR, bool DQB = false, bool KG = DQB>
 __global__ void __launch_bounds__(DQB ? kThreadsDq : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tA0,
                         const __grid_constant__ CUtensorMap tA1,
@@ -1090,7 +1144,9 @@ __global__ void __launch_bounds__(DQB ? kThreadsDq : kThreads, 1)
   }
   if (PAIR) {
     __syncthreads();
-    if (threadIdx.x == 0 && p.mode == MODE_MGROUP) {
+    if constexpr (KG) {
+      kgroup_order(p, s);
+    } else if (threadIdx.x == 0) {
       int run = 0;
       for (int e = 0; e < p.E; ++e) {
         s.pair_off[e] = run;
@@ -1125,19 +1181,19 @@ __global__ void __launch_bounds__(DQB ? kThreadsDq : kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       if (PAIR)
-        producer_pair<DQB>(p, s, ring, rank, &tA0, &tA1, &tB0, &tB1);
+        producer_pair<DQB, KG>(p, s, ring, rank, &tA0, &tA1, &tB0, &tB1);
       else
         producer<MX>(p, s, ring, &tA0, &tA1, &tB0, &tB1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       if (PAIR)
-        mma_issuer_pair<DQB>(p, s, ring, tmem_base, rank);
+        mma_issuer_pair<DQB, KG>(p, s, ring, tmem_base, rank);
       else
         mma_issuer<MX>(p, s, ring, tmem_base);
     }
   } else if (warp < kThreads / 32) {
-    epilogue<MX, PAIR, DQB>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
+    epilogue<MX, PAIR, DQB, KG>(p, s, tmem_base, warp, lane, stage_out, &tO0, &tO1, &tO2, rank);
   } else if (DQB && PAIR) {
     converter_pair(p, s, ring, (int)threadIdx.x - kThreads, lane);
   }
@@ -1251,7 +1307,7 @@ MOE_DEV void producer_mx_pair(const Params& p, Ctl& s, uint8_t* ring, int rank, 
   bool ok = true;
   for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters) {
     bool valid;
-    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    const TileInfo ti = decode_pair<false>(p, s, t, rank, valid);
     for (int ks = 0; ks < ti.ks; ++ks) {
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, &s.abort, p.err)) { ok = false; break; }
       if (rank == 0) mbar_arrive_expect_tx(&s.full[stage], 2u * (uint32_t)kMxPairTx);
@@ -1279,7 +1335,7 @@ MOE_DEV void mma_issuer_mx_pair(const Params& p, Ctl& s, uint8_t* ring, uint32_t
     bool ok = true;
     for (int t = (int)blockIdx.x / 2; ok && t < nt; t += nclusters, ++it) {
       bool valid;
-      const TileInfo ti = decode_pair(p, s, t, 0, valid);
+      const TileInfo ti = decode_pair<false>(p, s, t, 0, valid);
       if (!mbar_wait(&s.tempty[0], ((uint32_t)it & 1u) ^ 1u, &s.abort, p.err)) { ok = false; break; }
       tc_fence_after();
       for (int ks = 0; ks < ti.ks; ++ks) {
@@ -1382,7 +1438,7 @@ MOE_DEV void epilogue_mx_pair(const Params& p, Ctl& s, uint32_t tmem_base, int w
   int it = 0;
   for (int t = (int)blockIdx.x / 2; t < nt; t += (int)gridDim.x / 2, ++it) {
     bool valid;
-    const TileInfo ti = decode_pair(p, s, t, rank, valid);
+    const TileInfo ti = decode_pair<false>(p, s, t, rank, valid);
     valid = valid && MOE_CHECK_OK(ti.m_tile, p.rows_max / kTileM);   // the tile's rows (checks build)
     bool ok = mbar_wait(&s.tfull[0], (uint32_t)it & 1u, &s.abort, p.err);
     // the half's named barriers below need all four of its warps: leave together
@@ -1521,7 +1577,7 @@ MOE_DEV void hu_mover_mx_pair(const Params& p, Ctl& s, int rank, int half, uint8
   auto next_valid = [&](int t, int& fc, int& y) -> int {
     for (; t < nt; t += step) {
       bool valid;
-      const TileInfo ti = decode_pair(p, s, t, rank, valid);
+      const TileInfo ti = decode_pair<false>(p, s, t, rank, valid);
       if (valid && MOE_CHECK_OK(ti.m_tile, p.rows_max / kTileM)) {
         fc = ti.n_tile * kMxPairBN + 128 * half;
         y = ti.m_tile * kTileM;
@@ -1843,6 +1899,9 @@ cudaError_t gemm_init_attributes() {
   e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true, false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -2130,6 +2189,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& g, cudaStream_t stream) {
     if (p.dq_b)
       return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true, true>, A0, A1, B0, B1, O0,
                                 O1, O2, p);
+    if (p.mode == MODE_KGROUP)
+      return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true, false, true>, A0, A1, B0, B1,
+                                O0, O1, O2, p);
     return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<false, true>, A0, A1, B0, B1, O0, O1, O2,
                               p);
   }

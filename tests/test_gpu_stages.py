@@ -20,7 +20,12 @@ SHAPES = [
     (1000, 512, 8, 4, 256),
     (129, 128, 3, 1, 128),
     (500, 256, 16, 8, 256),    # k = 8: the wider gather kernels
+    # skewed: experts 5, 11 and 30 get 1446, 687 and 409 of the 4000 routes (more
+    # than twice the mean), the weight gradients hand their tiles out first, and
+    # 640 / 320 pair tiles run several rounds over the CTA pairs
+    (2000, 1024, 40, 2, 512, "skew"),
 ]
+SKEW_BIAS = ((5, 3.0), (11, 2.0), (30, 1.5))
 
 
 def bf(a, dev):
@@ -39,9 +44,12 @@ def f32(a, dev):
 @pytest.fixture(scope="module", params=SHAPES, ids=lambda s: "x".join(map(str, s)))
 def case(request, moe_gpu):
     m, dev = moe_gpu
-    T, d, E, k, f = request.param
+    T, d, E, k, f = request.param[:5]
     inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=T + E)
     inp["bias"][:, min(2, E - 1) if E > 2 else 0] -= (100.0 if E > 2 else 0.0)
+    if len(request.param) > 5:
+        for e, b in SKEW_BIAS:
+            inp["bias"][:, e] += b
     L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
     fwd = O.layer_forward(inp["x"], inp["w_router"], None, inp["w_gate"], inp["w_up"],
                           inp["w_down"], k, logits=L32)
