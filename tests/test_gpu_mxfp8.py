@@ -133,15 +133,23 @@ def test_dequantize_is_exact(moe_gpu):
 # DGRAD1 (N = d) there; the other GEMMs on CTA pairs; top-12 takes the k > 8
 # gathers (the combine backward's fused dY quantisation included)
 SHAPES = [(300, 256, 6, 2, 256), (1000, 512, 8, 8, 384), (200, 384, 4, 2, 256),
-          (160, 256, 16, 12, 256)]
+          (160, 256, 16, 12, 256),
+          # skewed: experts 5, 11 and 30 take 1492, 806 and 447 of the 4000 routes
+          # (more than twice the mean), so the weight gradients, natural layout
+          # included, hand their tiles out first, over several rounds of pairs
+          (2000, 512, 40, 2, 512, "skew")]
+SKEW_BIAS = ((5, 3.0), (11, 2.0), (30, 1.5))
 
 
 @pytest.fixture(scope="module", params=SHAPES, ids=lambda v: "x".join(map(str, v)))
 def mcase(request, moe_gpu):
     m, dev = moe_gpu
-    T, d, E, k, f = request.param
+    T, d, E, k, f = request.param[:5]
     inp = make_inputs(T=T, d=d, E=E, k=k, f=f, seed=T + 7)
     inp["bias"][:, 2] -= 100.0                  # one empty expert
+    if len(request.param) > 5:
+        for e, b in SKEW_BIAS:
+            inp["bias"][:, e] += b
     L32 = O.router_logits(inp["x"], inp["w_router"], inp["bias"]).astype(np.float32)
     fwd = O.layer_forward_mxfp8(inp["x"], None, None, inp["w_gate"], inp["w_up"], inp["w_down"],
                                 k, logits=L32)
